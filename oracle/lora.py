@@ -1,0 +1,183 @@
+"""Plain float64 definition of the LoRA block projections, forward and backward.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py``; never by the CUDA library, which shares no code
+with it.
+
+Sources (web pages; each function names the passage it follows):
+
+* "Model Patches and Kernels" (opake user guide), section "Fused LoRA operations",
+  kernel table: the single LoRA linear ``x @ W.T + x @ A @ B * s`` (row
+  ``opake_lora_w``), three projections sharing one input (row ``opake_lora_qkv``) and
+  gate + up + activation + down in one call (row ``opake_lora_mlp``); MLP fusion
+  is bias-free.
+* same page, section "Triton kernels", "Activation functions" table:
+  SwiGLU ``silu(gate) * up`` and GeGLU Approx ``gelu_tanh(gate) * up``.
+* same page, section "Fused linear cross-entropy", "Key design decisions": a frozen
+  weight gets no gradient.  Base weights W are frozen here, so backward returns
+  dX and the adapter gradients dA, dB only.
+* "monkeypatch.lora_kernels" (axolotl API reference), ``apply_lora_kernel_patches``
+  note: adapters have no dropout and no bias; ``original_apply_qkv`` returns
+  (query, key, value) from one hidden-state input; ``original_apply_o`` is the
+  output projection.
+
+Readings where the pages leave a step open (plainest reading, stated once here):
+
+1. ``s`` is alpha / r.
+2. Layout is the PEFT one: A is [r, in], B is [out, r], so the page's
+   ``x @ A @ B`` is ``x A^T B^T`` here.
+3. In the gated MLP the ``gate`` projection is activated and ``up`` is linear.
+4. ``gelu_tanh(g) = 0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3)))``, the
+   tanh approximation of GELU with its published constants.
+5. Backward is the chain rule of the forward above, with no weight gradient, and
+   dA/dB are the full gradients of the scalar <dY, Y> (no accumulation into old
+   values).
+6. Nothing is rounded: inputs are the bf16 values widened to float64.
+
+Every function is pinned by tests that do not restate its formula: the LoRA
+merged-weight identity, the B = 0 reduction to a base MLP built from library
+routines, central finite differences of <dY, Y>, closed-form activation
+derivatives against finite differences, and linearity in s.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+ACTS = ("swiglu", "geglu_tanh")
+_SQRT_2_OVER_PI = np.sqrt(2.0 / np.pi)
+_GELU_C = 0.044715
+
+
+def _mm(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """float64 matrix product (library primitive)."""
+    return np.matmul(a, b)
+
+
+# --------------------------------------------------------------------------------
+# Activations -- "Model Patches and Kernels", "Activation functions" table.
+# --------------------------------------------------------------------------------
+
+def sigmoid(g: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-g))
+
+
+def silu(g: np.ndarray) -> np.ndarray:
+    """silu(g) = g * sigmoid(g)  (SwiGLU row of the activation table)."""
+    return g * sigmoid(g)
+
+
+def gelu_tanh(g: np.ndarray) -> np.ndarray:
+    """GELU, tanh approximation (GeGLU Approx row of the activation table)."""
+    return 0.5 * g * (1.0 + np.tanh(_SQRT_2_OVER_PI * (g + _GELU_C * g ** 3)))
+
+
+def act(g: np.ndarray, kind: str) -> np.ndarray:
+    if kind == "swiglu":
+        return silu(g)
+    if kind == "geglu_tanh":
+        return gelu_tanh(g)
+    raise ValueError(f"unknown activation {kind!r}")
+
+
+def act_prime(g: np.ndarray, kind: str) -> np.ndarray:
+    """d act / d g in closed form.
+
+    silu'(g) = sigma(g) (1 + g (1 - sigma(g))).
+    gelu_tanh'(g) = 0.5 (1 + t) + 0.5 g (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 g^2),
+    t = tanh(sqrt(2/pi) (g + 0.044715 g^3)).
+    """
+    if kind == "swiglu":
+        sg = sigmoid(g)
+        return sg * (1.0 + g * (1.0 - sg))
+    if kind == "geglu_tanh":
+        t = np.tanh(_SQRT_2_OVER_PI * (g + _GELU_C * g ** 3))
+        return 0.5 * (1.0 + t) + 0.5 * g * (1.0 - t * t) * _SQRT_2_OVER_PI * (
+            1.0 + 3.0 * _GELU_C * g * g)
+    raise ValueError(f"unknown activation {kind!r}")
+
+
+# --------------------------------------------------------------------------------
+# One LoRA linear -- "Model Patches and Kernels", "Fused LoRA operations",
+# row opake_lora_w:  y = x W^T + s (x A^T) B^T.
+# --------------------------------------------------------------------------------
+
+def linear_t(x: np.ndarray, A: np.ndarray) -> np.ndarray:
+    """The rank-r projection T = x A^T, [M, r]."""
+    return _mm(x, A.T)
+
+
+def lora_linear(x, W, A, B, s):
+    """y = x W^T + s (x A^T) B^T for x [M, in], W [out, in], A [r, in], B [out, r]."""
+    return _mm(x, W.T) + s * _mm(linear_t(x, A), B.T)
+
+
+def lora_linear_grad(x, W, A, B, s, dy):
+    """Gradients of <dy, lora_linear(x, W, A, B, s)> with W frozen.
+
+    U = dy B [M, r];  dx = dy W + s U A;  dA = s U^T x [r, in];
+    dB = s dy^T (x A^T) [out, r].
+    """
+    U = _mm(dy, B)
+    dx = _mm(dy, W) + s * _mm(U, A)
+    dA = s * _mm(U.T, x)
+    dB = s * _mm(dy.T, linear_t(x, A))
+    return dx, dA, dB
+
+
+# --------------------------------------------------------------------------------
+# Gated MLP -- row opake_lora_mlp: gate and up LoRA linears on x, activation of the
+# gate times up, then the down LoRA linear.
+# --------------------------------------------------------------------------------
+
+def mlp_forward(x, Wg, Ag, Bg, Wu, Au, Bu, Wd, Ad, Bd, s, kind):
+    """Returns dict(g, u, h, y) for the LoRA gated MLP."""
+    g = lora_linear(x, Wg, Ag, Bg, s)
+    u = lora_linear(x, Wu, Au, Bu, s)
+    h = act(g, kind) * u
+    y = lora_linear(h, Wd, Ad, Bd, s)
+    return {"g": g, "u": u, "h": h, "y": y}
+
+
+def mlp_backward(x, Wg, Ag, Bg, Wu, Au, Bu, Wd, Ad, Bd, s, kind, dy):
+    """Gradients of <dy, y> for the LoRA gated MLP (frozen W): dx and dA/dB of
+    gate, up and down.  The forward is recomputed in float64."""
+    f = mlp_forward(x, Wg, Ag, Bg, Wu, Au, Bu, Wd, Ad, Bd, s, kind)
+    g, u, h = f["g"], f["u"], f["h"]
+    dh, dAd, dBd = lora_linear_grad(h, Wd, Ad, Bd, s, dy)
+    dg = dh * u * act_prime(g, kind)
+    du = dh * act(g, kind)
+    dxg, dAg, dBg = lora_linear_grad(x, Wg, Ag, Bg, s, dg)
+    dxu, dAu, dBu = lora_linear_grad(x, Wu, Au, Bu, s, du)
+    return {"dx": dxg + dxu, "dA_gate": dAg, "dB_gate": dBg, "dA_up": dAu,
+            "dB_up": dBu, "dA_down": dAd, "dB_down": dBd, "dg": dg, "du": du, "dh": dh}
+
+
+# --------------------------------------------------------------------------------
+# Attention projections -- row opake_lora_qkv (q, k, v share the input x) and the
+# output projection (original_apply_qkv / original_apply_o in the axolotl API).
+# The attention between them is not part of this path; o_in is its output.
+# --------------------------------------------------------------------------------
+
+def qkvo_forward(x, lin_q, lin_k, lin_v, o_in, lin_o, s):
+    """lin_p = (W, A, B).  Returns dict(q, k, v, o)."""
+    out = {}
+    for name, lin in (("q", lin_q), ("k", lin_k), ("v", lin_v)):
+        out[name] = lora_linear(x, *lin, s)
+    out["o"] = lora_linear(o_in, *lin_o, s)
+    return out
+
+
+def qkvo_backward(x, lin_q, lin_k, lin_v, o_in, lin_o, s, dy_q, dy_k, dy_v, dy_o):
+    """Gradients of <dy_q, q> + <dy_k, k> + <dy_v, v> + <dy_o, o>: dx (sum over the
+    three projections), d o_in, and dA/dB of q, k, v and o."""
+    res = {}
+    dx = None
+    for name, lin, d in (("q", lin_q, dy_q), ("k", lin_k, dy_k), ("v", lin_v, dy_v)):
+        dxp, dA, dB = lora_linear_grad(x, *lin, s, d)
+        dx = dxp if dx is None else dx + dxp
+        res[f"dA_{name}"], res[f"dB_{name}"] = dA, dB
+    res["dx"] = dx
+    res["do_in"], res["dA_o"], res["dB_o"] = lora_linear_grad(o_in, *lin_o, s, dy_o)
+    return res
