@@ -1,0 +1,189 @@
+/*
+ * lora_gb300.h -- C ABI of the GB300 (sm_103a) LoRA block-projection library.
+ *
+ * What is computed
+ * ----------------
+ * A LoRA linear with frozen base weight W [out x in] and adapter A [r x in],
+ * B [out x r], scale s:
+ *
+ *     y = x W^T + s (x A^T) B^T                                               (1)
+ *
+ * ("Model Patches and Kernels", opake user guide, section "Fused LoRA operations",
+ * row opake_lora_w: x @ W.T + x @ A @ B * s, written here in the PEFT layout with
+ * A stored [r x in] and B stored [out x r]; s = alpha / r.)
+ *
+ * The gated MLP (same section, row opake_lora_mlp: gate + up + activation + down in
+ * one call; activations from the same page, "Activation functions" table):
+ *
+ *     g = (1) with gate,  u = (1) with up,  h = act(g) * u,  y = (1) of h with down
+ *     act = silu (SwiGLU) or the tanh approximation of GELU (GeGLU)
+ *
+ * The attention projections (row opake_lora_qkv: q, k, v share the input x; the
+ * axolotl "monkeypatch.lora_kernels" reference, original_apply_qkv returning
+ * (query, key, value) and original_apply_o for the output projection): q, k, v and
+ * o are each (1); o's input is the attention output, which this library does not
+ * compute.
+ *
+ * Backward computes the gradient of <dy, y> with respect to x and every A and B.
+ * W is frozen and gets no gradient ("Model Patches and Kernels", section "Fused
+ * linear cross-entropy": a frozen weight's gradient is skipped).  Adapters have no
+ * dropout and no bias (axolotl apply_lora_kernel_patches note; MLP fusion is
+ * bias-free per opake).
+ *
+ * Conventions (all entry points)
+ * ------------------------------
+ * - Tensors are bf16, row-major, dense (row stride = number of columns), in device
+ *   memory, token-major for activations: x [M x in], y [M x out]; M = batch * seq.
+ *   W [out x in], A [r x in], B [out x r], dA [r x in], dB [out x r].
+ * - The caller owns and allocates every buffer, including `saved` and `ws`; the
+ *   library allocates no memory and never synchronises (lora_poll_status aside).
+ *   All work is enqueued on `stream`, in order.
+ * - Gradient outputs (dx, dA, dB) are overwritten, not accumulated.
+ * - Alignment: every pointer 16-byte aligned (`ws` and `saved` 256-byte aligned);
+ *   every feature size (in, out, h, i, n_q, n_kv) a multiple of 8.  A and B need no
+ *   alignment beyond their element size.  Violations return LORA_ERR_ALIGNMENT.
+ * - Rank limits: 1 <= r, and (number of adapters sharing one input) * r <= 256,
+ *   i.e. r <= 128 for the MLP's gate/up pair and r <= 85 for q/k/v; otherwise
+ *   LORA_ERR_UNSUPPORTED.
+ * - Every argument error returns before anything is enqueued.  No entry point
+ *   aborts, throws or prints.
+ * - `ws` must hold lora_*_workspace_bytes(...) bytes; its first 256 bytes hold the
+ *   status word that kernels set asynchronously (zero them before first use;
+ *   lora_poll_status reads and clears it).  `saved` must hold lora_*_saved_bytes(...)
+ *   and is an opaque blob written by forward and read by backward.
+ * - M == 0 is allowed: forward enqueues nothing, backward zero-fills dA and dB.
+ * - Calls that share a `ws` must not overlap on the GPU (same stream is safe).
+ */
+#ifndef LORA_GB300_H
+#define LORA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LORA_ACT_SWIGLU = 0,      /* silu(g) * u */
+  LORA_ACT_GEGLU_TANH = 1   /* gelu_tanh(g) * u, 0.5 g (1 + tanh(sqrt(2/pi)(g + 0.044715 g^3))) */
+} lora_act_t;
+
+typedef enum {
+  LORA_OK = 0,
+  LORA_ERR_INVALID_ARG = 1,   /* NULL pointer, negative size, bad enum, non-finite s */
+  LORA_ERR_ALIGNMENT = 2,     /* pointer or feature size violates the alignment rules */
+  LORA_ERR_UNSUPPORTED = 3,   /* rank beyond the limits above, or a non-NULL bias */
+  LORA_ERR_WORKSPACE = 4,     /* ws_bytes below the workspace query */
+  LORA_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
+  LORA_ERR_TIMEOUT = 6        /* a kernel's bounded wait expired (read by lora_poll_status) */
+} lora_status_t;
+
+/* One frozen base weight and its adapter: device pointers, bf16, row-major.
+ * W [out x in], A [r x in], B [out x r]. */
+typedef struct {
+  const void* W;
+  const void* A;
+  const void* B;
+} lora_linear_t;
+
+/* Gradient outputs of one adapter: dA [r x in], dB [out x r], bf16, overwritten. */
+typedef struct {
+  void* dA;
+  void* dB;
+} lora_grads_t;
+
+/* ---------------------------------------------------------------- single linear
+ * (1) for one projection ("opake_lora_w").  saved holds the rank-r projection x A^T
+ * for backward; pass NULL for inference. */
+size_t lora_linear_saved_bytes(int64_t M, int64_t in, int64_t out, int r);
+size_t lora_linear_workspace_bytes(int64_t M, int64_t in, int64_t out, int r);
+lora_status_t lora_linear_forward(int64_t M, int64_t in, int64_t out, int r, float s,
+                                  const void* x, lora_linear_t lin, void* y, void* saved,
+                                  void* ws, size_t ws_bytes, cudaStream_t stream);
+/* dx [M x in] = dy W + s (dy B) A;  dA = s (dy B)^T x;  dB = s dy^T (x A^T).
+ * x is the forward input again; saved is what forward wrote. */
+lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out, int r, float s,
+                                   const void* x, lora_linear_t lin, const void* saved,
+                                   const void* dy, void* dx, lora_grads_t grads,
+                                   void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- gated MLP
+ * x [M x h] -> y [M x h] through gate/up [i x h] and down [h x i] ("opake_lora_mlp").
+ * saved (NULL for inference) receives g, u, h and the rank-r projections for
+ * backward. */
+size_t lora_mlp_saved_bytes(int64_t M, int64_t h, int64_t i, int r);
+size_t lora_mlp_workspace_bytes(int64_t M, int64_t h, int64_t i, int r);
+lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r, float s, lora_act_t act,
+                               const void* x, lora_linear_t gate, lora_linear_t up,
+                               lora_linear_t down, void* y, void* saved,
+                               void* ws, size_t ws_bytes, cudaStream_t stream);
+/* Gradients of <dy, y>: dx [M x h] and dA/dB of gate, up and down.  Needs the
+ * forward's x and saved blob (the activation and its derivative are recomputed from
+ * the saved g, u). */
+lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int r, float s, lora_act_t act,
+                                const void* x, lora_linear_t gate, lora_linear_t up,
+                                lora_linear_t down, const void* saved, const void* dy,
+                                void* dx, lora_grads_t d_gate, lora_grads_t d_up,
+                                lora_grads_t d_down, void* ws, size_t ws_bytes,
+                                cudaStream_t stream);
+
+/* ---------------------------------------------------------------- Q/K/V + O
+ * q = (1)(x; q) [M x n_q], k, v = (1)(x; k or v) [M x n_kv] ("opake_lora_qkv"), and
+ * yo = (1)(o_in; o) [M x h] with W_o [h x n_q] ("original_apply_o").  Attention runs
+ * between the two halves in a real block, so either half may be skipped: x == NULL
+ * skips q/k/v, o_in == NULL skips O.  bias_qkv must be NULL (frozen biases are not
+ * supported; LORA_ERR_UNSUPPORTED otherwise). */
+size_t lora_qkvo_saved_bytes(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r);
+size_t lora_qkvo_workspace_bytes(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r);
+lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r, float s,
+                                const void* x, lora_linear_t q, lora_linear_t k,
+                                lora_linear_t v, void* yq, void* yk, void* yv,
+                                const void* o_in, lora_linear_t o, void* yo,
+                                const void* bias_qkv, void* saved,
+                                void* ws, size_t ws_bytes, cudaStream_t stream);
+/* Gradients of <dyq, q> + <dyk, k> + <dyv, v> (dx = their sum over the three
+ * projections, and dA/dB of q, k, v) and of <dyo, yo> (do_in and dA/dB of o).
+ * x == NULL skips the q/k/v half, o_in == NULL the O half. */
+lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r, float s,
+                                 const void* x, lora_linear_t q, lora_linear_t k,
+                                 lora_linear_t v, const void* o_in, lora_linear_t o,
+                                 const void* saved, const void* dyq, const void* dyk,
+                                 const void* dyv, void* dx, const void* dyo, void* do_in,
+                                 lora_grads_t d_q, lora_grads_t d_k, lora_grads_t d_v,
+                                 lora_grads_t d_o, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream);
+
+/* ---------------------------------------------------------------- status, counters
+ * lora_poll_status: synchronises `stream`, reads the asynchronous status word in
+ * ws (LORA_OK or LORA_ERR_TIMEOUT), clears it, and returns it (LORA_ERR_CUDA if the
+ * synchronisation itself fails). */
+lora_status_t lora_poll_status(void* ws, cudaStream_t stream);
+const char* lora_status_string(lora_status_t status);
+/* Kernels this library has launched in this process (all entry points). */
+uint64_t lora_launch_count(void);
+
+/* Launch tracing, for measurement.  lora_trace_enable(n) makes every later launch
+ * record a pair of CUDA events around itself on its stream, keeping the first n
+ * launches (0 disables and frees the events).  lora_trace_read synchronises the
+ * recorded events, fills kind[] and ms[] (kernel kinds below) for up to `max`
+ * launches, and restarts the trace; it returns the number filled or -1 on error. */
+enum {
+  LORA_KIND_PACK = 0,        /* adapter packing */
+  LORA_KIND_REDUCE = 1,      /* split-K reduction of the rank-r products */
+  LORA_KIND_RANK_PROJ = 2,   /* token-major rank-r projections (x A^T, dy B, dg B) */
+  LORA_KIND_RANK_GRAD = 3,   /* reductions over tokens (dA, dB) */
+  LORA_KIND_GATE_UP = 4,     /* gate/up GEMM with the activation epilogue */
+  LORA_KIND_PROJ = 5,        /* plain projection GEMM (down, q/k/v, o) */
+  LORA_KIND_ACT_BWD = 6,     /* dh GEMM with the activation-derivative epilogue */
+  LORA_KIND_DGRAD = 7        /* input-gradient GEMM (dx, d o_in) */
+};
+lora_status_t lora_trace_enable(int capacity);
+int lora_trace_read(int* kind, float* ms, int max);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_GB300_H */

@@ -1,0 +1,315 @@
+"""Python binding of ``include/lora_gb300.h`` (ctypes).
+
+Argument marshalling only: tensors are checked for dtype/contiguity/device, their
+pointers and the current CUDA stream are passed to the C ABI, and status codes
+become exceptions.  Every step of the computation runs in the library's kernels;
+there is no fallback, and a missing library raises.
+
+Adapters are passed as ``(W, A, B)`` tuples of bf16 CUDA tensors: W [out, in],
+A [r, in], B [out, r].  Activations are token-major [M, features].
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+ACT = {"swiglu": 0, "geglu_tanh": 1}
+KIND_NAMES = {0: "pack", 1: "reduce", 2: "rank_proj", 3: "rank_grad", 4: "gate_up",
+              5: "proj", 6: "act_bwd", 7: "dgrad"}
+STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported",
+          4: "workspace too small", 5: "CUDA error", 6: "timeout"}
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _LIB.lora_status_string(status).decode() if _LIB is not None else STATUS.get(status, "?")
+        super().__init__(f"{where}: {msg} (status {status})")
+
+
+class LoraLinear(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p)]
+
+
+class LoraGrads(ctypes.Structure):
+    _fields_ = [("dA", ctypes.c_void_p), ("dB", ctypes.c_void_p)]
+
+
+_LIB = None
+_LOCK = threading.Lock()
+_I64, _INT, _F32, _VP, _SZ = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+
+_SIGS = {
+    "lora_linear_saved_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
+    "lora_linear_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
+    "lora_linear_forward": (_INT, [_I64, _I64, _I64, _INT, _F32, _VP, LoraLinear, _VP, _VP, _VP, _SZ, _VP]),
+    "lora_linear_backward": (_INT, [_I64, _I64, _I64, _INT, _F32, _VP, LoraLinear, _VP, _VP, _VP, LoraGrads,
+                                    _VP, _SZ, _VP]),
+    "lora_mlp_saved_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
+    "lora_mlp_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
+    "lora_mlp_forward": (_INT, [_I64, _I64, _I64, _INT, _F32, _INT, _VP, LoraLinear, LoraLinear, LoraLinear,
+                                _VP, _VP, _VP, _SZ, _VP]),
+    "lora_mlp_backward": (_INT, [_I64, _I64, _I64, _INT, _F32, _INT, _VP, LoraLinear, LoraLinear, LoraLinear,
+                                 _VP, _VP, _VP, LoraGrads, LoraGrads, LoraGrads, _VP, _SZ, _VP]),
+    "lora_qkvo_saved_bytes": (_SZ, [_I64, _I64, _I64, _I64, _INT]),
+    "lora_qkvo_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64, _INT]),
+    "lora_qkvo_forward": (_INT, [_I64, _I64, _I64, _I64, _INT, _F32, _VP, LoraLinear, LoraLinear, LoraLinear,
+                                 _VP, _VP, _VP, _VP, LoraLinear, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "lora_qkvo_backward": (_INT, [_I64, _I64, _I64, _I64, _INT, _F32, _VP, LoraLinear, LoraLinear, LoraLinear,
+                                  _VP, LoraLinear, _VP, _VP, _VP, _VP, _VP, _VP, _VP, LoraGrads, LoraGrads,
+                                  LoraGrads, LoraGrads, _VP, _SZ, _VP]),
+    "lora_poll_status": (_INT, [_VP, _VP]),
+    "lora_status_string": (ctypes.c_char_p, [_INT]),
+    "lora_launch_count": (ctypes.c_uint64, []),
+    "lora_trace_enable": (_INT, [_INT]),
+    "lora_trace_read": (_INT, [ctypes.POINTER(_INT), ctypes.POINTER(_F32), _INT]),
+}
+EXPORTS = tuple(_SIGS)
+
+
+def load(path: str | None = None):
+    """Loads the library (built in-tree by ``rank_mlp_gb300.build``); raises if absent."""
+    global _LIB
+    with _LOCK:
+        if _LIB is not None:
+            return _LIB
+        path = path or _build.lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with `python -m rank_mlp_gb300.build` "
+                               "(there is no fallback path)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+        return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise LoraError(status, where)
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor (got {t.dtype}, {t.device})")
+    return t.data_ptr()
+
+
+def _opt(t, name):
+    return None if t is None else _dev(t, name)
+
+
+def _lin(lin, name) -> LoraLinear:
+    W, A, B = lin
+    return LoraLinear(_dev(W, name + ".W"), _dev(A, name + ".A"), _dev(B, name + ".B"))
+
+
+# ------------------------------------------------------------------ workspaces
+
+_WS = {}
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A per-device workspace of at least nbytes (cached, grown on demand, first
+    256 bytes zeroed: they hold the asynchronous status word)."""
+    device = torch.device(device)
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _WS.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _WS[key] = ws
+    return ws
+
+
+def poll_status(ws: torch.Tensor | None = None) -> int:
+    lib = load()
+    if ws is None:
+        ws = workspace(256, torch.cuda.current_device())
+    return lib.lora_poll_status(ctypes.c_void_p(ws.data_ptr()), _stream(ws.device))
+
+
+def launch_count() -> int:
+    return int(load().lora_launch_count())
+
+
+def trace_enable(capacity: int):
+    _check(load().lora_trace_enable(capacity), "lora_trace_enable")
+
+
+def trace_read(max_entries: int = 4096):
+    """[(kind name, ms)] of the launches recorded since the trace was (re)started."""
+    kinds = (_INT * max_entries)()
+    ms = (_F32 * max_entries)()
+    n = load().lora_trace_read(kinds, ms, max_entries)
+    if n < 0:
+        raise LoraError(5, "lora_trace_read")
+    return [(KIND_NAMES.get(kinds[j], str(kinds[j])), float(ms[j])) for j in range(n)]
+
+
+# ------------------------------------------------------------------ single linear
+
+def linear_forward(x, lin, s, *, y=None, saved=None, training=True, ws=None):
+    lib = load()
+    W, A, B = lin
+    M, fin = x.shape
+    fout, r = W.shape[0], A.shape[0]
+    if y is None:
+        y = torch.empty(M, fout, dtype=torch.bfloat16, device=x.device)
+    if saved is None and training:
+        saved = torch.empty(max(lib.lora_linear_saved_bytes(M, fin, fout, r), 256), dtype=torch.uint8,
+                            device=x.device)
+    need = lib.lora_linear_workspace_bytes(M, fin, fout, r)
+    ws = workspace(need, x.device) if ws is None else ws
+    _check(lib.lora_linear_forward(M, fin, fout, r, s, _dev(x, "x"), _lin(lin, "lin"), _dev(y, "y"),
+                                   None if saved is None else saved.data_ptr(), ws.data_ptr(), ws.numel(),
+                                   _stream(x.device)), "lora_linear_forward")
+    return y, saved
+
+
+def linear_backward(x, lin, s, saved, dy, *, dx=None, dA=None, dB=None, ws=None):
+    lib = load()
+    W, A, B = lin
+    M, fin = x.shape
+    fout, r = W.shape[0], A.shape[0]
+    dev = x.device
+    dx = torch.empty(M, fin, dtype=torch.bfloat16, device=dev) if dx is None else dx
+    dA = torch.empty(r, fin, dtype=torch.bfloat16, device=dev) if dA is None else dA
+    dB = torch.empty(fout, r, dtype=torch.bfloat16, device=dev) if dB is None else dB
+    need = lib.lora_linear_workspace_bytes(M, fin, fout, r)
+    ws = workspace(need, dev) if ws is None else ws
+    _check(lib.lora_linear_backward(M, fin, fout, r, s, _dev(x, "x"), _lin(lin, "lin"), saved.data_ptr(),
+                                    _dev(dy, "dy"), _dev(dx, "dx"), LoraGrads(_dev(dA, "dA"), _dev(dB, "dB")),
+                                    ws.data_ptr(), ws.numel(), _stream(dev)), "lora_linear_backward")
+    return dx, dA, dB
+
+
+# ------------------------------------------------------------------ gated MLP
+
+def mlp_sizes(M, h, i, r):
+    lib = load()
+    return lib.lora_mlp_saved_bytes(M, h, i, r), lib.lora_mlp_workspace_bytes(M, h, i, r)
+
+
+def mlp_forward(x, gate, up, down, s, act="swiglu", *, y=None, saved=None, training=True, ws=None):
+    """y = down(act(gate(x)) * up(x)); returns (y, saved)."""
+    lib = load()
+    M, h = x.shape
+    i, r = gate[0].shape[0], gate[1].shape[0]
+    if y is None:
+        y = torch.empty(M, h, dtype=torch.bfloat16, device=x.device)
+    if saved is None and training:
+        saved = torch.empty(max(lib.lora_mlp_saved_bytes(M, h, i, r), 256), dtype=torch.uint8, device=x.device)
+    need = lib.lora_mlp_workspace_bytes(M, h, i, r)
+    ws = workspace(need, x.device) if ws is None else ws
+    _check(lib.lora_mlp_forward(M, h, i, r, s, ACT[act], _dev(x, "x"), _lin(gate, "gate"), _lin(up, "up"),
+                                _lin(down, "down"), _dev(y, "y"), None if saved is None else saved.data_ptr(),
+                                ws.data_ptr(), ws.numel(), _stream(x.device)), "lora_mlp_forward")
+    return y, saved
+
+
+def mlp_backward(x, gate, up, down, s, act, saved, dy, *, dx=None, grads=None, ws=None):
+    """Returns dict(dx, dA_gate, dB_gate, dA_up, dB_up, dA_down, dB_down)."""
+    lib = load()
+    M, h = x.shape
+    i, r = gate[0].shape[0], gate[1].shape[0]
+    dev = x.device
+    e = lambda *sh: torch.empty(*sh, dtype=torch.bfloat16, device=dev)  # noqa: E731
+    out = {"dx": e(M, h) if dx is None else dx}
+    if grads is None:
+        grads = {"dA_gate": e(r, h), "dB_gate": e(i, r), "dA_up": e(r, h), "dB_up": e(i, r),
+                 "dA_down": e(r, i), "dB_down": e(h, r)}
+    out.update(grads)
+    need = lib.lora_mlp_workspace_bytes(M, h, i, r)
+    ws = workspace(need, dev) if ws is None else ws
+    g = lambda n: LoraGrads(_dev(out["dA_" + n], "dA_" + n), _dev(out["dB_" + n], "dB_" + n))  # noqa: E731
+    _check(lib.lora_mlp_backward(M, h, i, r, s, ACT[act], _dev(x, "x"), _lin(gate, "gate"), _lin(up, "up"),
+                                 _lin(down, "down"), saved.data_ptr(), _dev(dy, "dy"), _dev(out["dx"], "dx"),
+                                 g("gate"), g("up"), g("down"), ws.data_ptr(), ws.numel(), _stream(dev)),
+           "lora_mlp_backward")
+    return out
+
+
+# ------------------------------------------------------------------ Q/K/V + O
+
+def qkvo_forward(x, q, k, v, o_in, o, s, *, saved=None, training=True, ws=None, outs=None):
+    """q/k/v from x (skipped if x is None) and the O projection of o_in (skipped if
+    o_in is None).  Returns (dict(q, k, v, o), saved)."""
+    lib = load()
+    ref = x if x is not None else o_in
+    dev = ref.device
+    M = ref.shape[0]
+    h = q[0].shape[1] if x is not None else o[0].shape[0]
+    nq = q[0].shape[0] if x is not None else o[0].shape[1]
+    nkv = k[0].shape[0] if x is not None else 8
+    r = (q if x is not None else o)[1].shape[0]
+    e = lambda *sh: torch.empty(*sh, dtype=torch.bfloat16, device=dev)  # noqa: E731
+    res = dict(outs or {})
+    if x is not None:
+        for n, w in (("q", nq), ("k", nkv), ("v", nkv)):
+            res.setdefault(n, e(M, w))
+    if o_in is not None:
+        res.setdefault("o", e(M, h))
+    if saved is None and training:
+        saved = torch.empty(max(lib.lora_qkvo_saved_bytes(M, h, nq, nkv, r), 256), dtype=torch.uint8,
+                            device=dev)
+    need = lib.lora_qkvo_workspace_bytes(M, h, nq, nkv, r)
+    ws = workspace(need, dev) if ws is None else ws
+    z = LoraLinear(None, None, None)
+    _check(lib.lora_qkvo_forward(
+        M, h, nq, nkv, r, s, _opt(x, "x"),
+        _lin(q, "q") if x is not None else z, _lin(k, "k") if x is not None else z,
+        _lin(v, "v") if x is not None else z,
+        _opt(res.get("q"), "yq"), _opt(res.get("k"), "yk"), _opt(res.get("v"), "yv"),
+        _opt(o_in, "o_in"), _lin(o, "o") if o_in is not None else z, _opt(res.get("o"), "yo"),
+        None, None if saved is None else saved.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)),
+        "lora_qkvo_forward")
+    return res, saved
+
+
+def qkvo_backward(x, q, k, v, o_in, o, s, saved, dyq=None, dyk=None, dyv=None, dyo=None, *, ws=None):
+    """Returns dict(dx, do_in, dA_q, dB_q, ..., dA_o, dB_o) for the halves present."""
+    lib = load()
+    ref = x if x is not None else o_in
+    dev = ref.device
+    M = ref.shape[0]
+    h = q[0].shape[1] if x is not None else o[0].shape[0]
+    nq = q[0].shape[0] if x is not None else o[0].shape[1]
+    nkv = k[0].shape[0] if x is not None else 8
+    r = (q if x is not None else o)[1].shape[0]
+    e = lambda *sh: torch.empty(*sh, dtype=torch.bfloat16, device=dev)  # noqa: E731
+    out = {}
+    z = LoraGrads(None, None)
+    zl = LoraLinear(None, None, None)
+    if x is not None:
+        out["dx"] = e(M, h)
+        for n, w in (("q", nq), ("k", nkv), ("v", nkv)):
+            out["dA_" + n], out["dB_" + n] = e(r, h), e(w, r)
+    if o_in is not None:
+        out["do_in"] = e(M, nq)
+        out["dA_o"], out["dB_o"] = e(r, nq), e(h, r)
+    gr = lambda n: LoraGrads(out["dA_" + n].data_ptr(), out["dB_" + n].data_ptr()) if "dA_" + n in out else z  # noqa: E731,E501
+    need = lib.lora_qkvo_workspace_bytes(M, h, nq, nkv, r)
+    ws = workspace(need, dev) if ws is None else ws
+    _check(lib.lora_qkvo_backward(
+        M, h, nq, nkv, r, s, _opt(x, "x"),
+        _lin(q, "q") if x is not None else zl, _lin(k, "k") if x is not None else zl,
+        _lin(v, "v") if x is not None else zl, _opt(o_in, "o_in"),
+        _lin(o, "o") if o_in is not None else zl, saved.data_ptr(),
+        _opt(dyq, "dyq"), _opt(dyk, "dyk"), _opt(dyv, "dyv"), _opt(out.get("dx"), "dx"),
+        _opt(dyo, "dyo"), _opt(out.get("do_in"), "do_in"), gr("q"), gr("k"), gr("v"), gr("o"),
+        ws.data_ptr(), ws.numel(), _stream(dev)), "lora_qkvo_backward")
+    return out

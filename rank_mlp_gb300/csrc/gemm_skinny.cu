@@ -1,0 +1,41 @@
+// 128 x 64 / 128 x 128 tiles: the rank-r products (token-major projections such as
+// x A^T, and the reductions over tokens that give dA and dB).  HBM-bound; deep rings.
+#include "host.cuh"
+
+namespace lgb {
+
+template <int BN, int STAGES, bool A_MN, bool B_MN>
+static cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
+  auto* k = tc_gemm_kernel<BN, STAGES, A_MN, B_MN>;
+  constexpr int smem = TcCfg<BN, STAGES>::kSmemBytes;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  k<<<grid, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_skinny(int variant, const TcParams& p, int grid, cudaStream_t st) {
+  switch (variant) {
+    case V64_KK: return launch_one<64, 8, false, false>(p, grid, st);
+    case V64_MNMN: return launch_one<64, 8, true, true>(p, grid, st);
+    case V128_KK: return launch_one<128, 6, false, false>(p, grid, st);
+    case V128_MNMN: return launch_one<128, 6, true, true>(p, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+int tc_smem_bytes(int variant) {
+  switch (variant) {
+    case V256_KK:
+    case V256_KMN: return TcCfg<256, 4>::kSmemBytes;
+    case V64_KK:
+    case V64_MNMN: return TcCfg<64, 8>::kSmemBytes;
+    default: return TcCfg<128, 6>::kSmemBytes;
+  }
+}
+
+}  // namespace lgb

@@ -1,0 +1,486 @@
+// Persistent tcgen05 GEMM for sm_103a with the LoRA rank-r term folded in as extra
+// K-segments, and the block's epilogues fused in.
+//
+// C[m, n] = sum over segments s, k in segment:  A_s[m, k] * B_s[n, k]
+//
+// A LoRA linear y = x W^T + s (x A^T) B^T ("Model Patches and Kernels", section
+// "Fused LoRA operations", row opake_lora_w) becomes two segments: [x | T] against
+// [W | s B] with T = x A^T computed first; the gated MLP's gate and up projections
+// (row opake_lora_mlp) share one tile: the B tile's first half holds gate rows,
+// the second half the matching up rows, so the activation epilogue sees both.
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 0     TMA producer (one lane): fills a STAGES-deep ring of A/B tiles.
+//   warp 1     TMEM owner + MMA issuer (one lane): 128 x BN x 16 tcgen05.mma per step
+//              into one of two TMEM accumulators (the epilogue drains the other).
+//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter, fused math, stores.
+//
+// Every wait is bounded in time; on expiry the CTA records a timeout in the status
+// word, lets its own copies and MMAs finish (again bounded), frees TMEM and exits.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace lgb {
+
+constexpr int kBM = 128;       // accumulator rows = TMEM lanes
+constexpr int kBK = 64;        // one 128-byte swizzle row of bf16 per k-block
+constexpr int kThreads = 192;
+constexpr int kMaxMaps = 12;
+constexpr int kMaxGroups = 3;
+constexpr int kMaxSegs = 4;
+constexpr unsigned kStatusTimeout = 1u;
+
+enum EpiKind : int { EPI_STORE = 0, EPI_ACT_FWD = 1, EPI_ACT_BWD = 2, EPI_PARTIAL = 3 };
+enum ActKind : int { ACT_SWIGLU = 0, ACT_GEGLU_TANH = 1 };
+
+struct SegDesc {
+  int a, b0, b1;   // tensor-map indices; b1 >= 0: B tile = BN/2 rows of b0 + BN/2 rows of b1
+  int kblocks;     // number of 64-wide k-blocks in this segment
+  int kvalid;      // K columns that may be non-zero; MMA steps at or past it are skipped
+};
+
+struct GroupDesc {
+  int M, N;                  // logical output extent
+  int tiles_m, tiles_n, splits;
+  int unit_begin;            // first work unit of this group
+  int nseg, kb_total;
+  SegDesc seg[kMaxSegs];
+  int epi;
+  void* out0;
+  void* out1;
+  void* out2;
+  const void* in0;
+  const void* in1;
+  long long ldo, ldi;
+  float* part;               // EPI_PARTIAL: [splits][tiles_m*128][tiles_n*BN] f32
+};
+
+struct TcParams {
+  CUtensorMap maps[kMaxMaps];
+  GroupDesc grp[kMaxGroups];
+  int nmaps;
+  int ngroups;
+  int total_units;
+  int band;                  // raster: n-tiles per band, m fastest inside a band
+  int act;
+  unsigned int* status;
+  unsigned long long timeout_ns;
+};
+
+template <int BN, int STAGES>
+struct TcCfg {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+  static constexpr int kBarBytes = 8 * (2 * STAGES + 5) + 16;
+  static constexpr int kSmemBytes = STAGES * kStageBytes + kBarBytes + 1024;
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+};
+
+struct Unit {
+  int g, tm, tn, split, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
+  int g = 0;
+  while (g + 1 < p.ngroups && u >= p.grp[g + 1].unit_begin) ++g;
+  const GroupDesc& G = p.grp[g];
+  const int local = u - G.unit_begin;
+  const int tiles = G.tiles_m * G.tiles_n;
+  const int split = local / tiles;
+  const int t = local - split * tiles;
+  const int band = p.band;
+  const int b = t / (G.tiles_m * band);
+  const int rem = t - b * G.tiles_m * band;
+  const int nb = min(band, G.tiles_n - b * band);
+  Unit U;
+  U.g = g;
+  U.tm = rem / nb;
+  U.tn = b * band + rem % nb;
+  U.split = split;
+  U.kb0 = static_cast<int>(static_cast<long long>(G.kb_total) * split / G.splits);
+  U.kb1 = static_cast<int>(static_cast<long long>(G.kb_total) * (split + 1) / G.splits);
+  return U;
+}
+
+// Bounded wait: true when the phase completed, false on abort (flag set by another
+// role, or this wait timed out, which sets the flag and the status word).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           const TcParams& p) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > p.timeout_ns) {
+        *abort_flag = 1;
+        if (p.status) atomicOr(p.status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+// Drain wait after an abort: bounded by time only.
+__device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity, const TcParams& p) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > p.timeout_ns) {
+      if (p.status) atomicOr(p.status, kStatusTimeout);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kSqrt2OverPi = 0.7978845608028654f;
+constexpr float kGeluC = 0.044715f;
+
+// act(g): silu or tanh-GELU ("Model Patches and Kernels", activation table).
+__device__ __forceinline__ float act_fwd(float g, int act) {
+  if (act == ACT_SWIGLU) return g / (1.0f + __expf(-g));
+  const float t = tanh_approx(kSqrt2OverPi * (g + kGeluC * g * g * g));
+  return 0.5f * g * (1.0f + t);
+}
+
+// act(g) and act'(g) together.
+__device__ __forceinline__ void act_fwd_bwd(float g, int act, float& a, float& ap) {
+  if (act == ACT_SWIGLU) {
+    const float sg = 1.0f / (1.0f + __expf(-g));
+    a = g * sg;
+    ap = sg * (1.0f + g * (1.0f - sg));
+  } else {
+    const float t = tanh_approx(kSqrt2OverPi * (g + kGeluC * g * g * g));
+    a = 0.5f * g * (1.0f + t);
+    ap = 0.5f * (1.0f + t) + 0.5f * g * (1.0f - t * t) * kSqrt2OverPi * (1.0f + 3.0f * kGeluC * g * g);
+  }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int BN, int STAGES, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  using C = TcCfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane < p.nmaps) tma_prefetch_map(&p.maps[lane]);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[STAGES];
+      for (int s = 0; s < STAGES; ++s) armed[s] = -1;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+        const Unit U = decode_unit(p, u);
+        const GroupDesc& G = p.grp[U.g];
+        int seg = 0, seg_base = 0;
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
+          while (kb >= seg_base + G.seg[seg].kblocks) {
+            seg_base += G.seg[seg].kblocks;
+            ++seg;
+          }
+          const SegDesc& S = G.seg[seg];
+          const int kc = (kb - seg_base) * kBK;
+          if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) { ok = false; break; }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, C::kStageBytes);
+          armed[stage] = static_cast<int>(phase);
+          const uint32_t sa = sbase + stage * C::kStageBytes;
+          const uint32_t sb = sa + C::kABytes;
+          const CUtensorMap* ma = &p.maps[S.a];
+          if (!A_MN) {
+            tma_load_2d(sa, ma, fb, kc, U.tm * kBM);
+          } else {
+            tma_load_2d(sa, ma, fb, U.tm * kBM, kc);
+            tma_load_2d(sa + 8192u, ma, fb, U.tm * kBM + 64, kc);
+          }
+          if (!B_MN) {
+            if (S.b1 >= 0) {
+              tma_load_2d(sb, &p.maps[S.b0], fb, kc, U.tn * (BN / 2));
+              tma_load_2d(sb + (BN / 2) * 128u, &p.maps[S.b1], fb, kc, U.tn * (BN / 2));
+            } else {
+              tma_load_2d(sb, &p.maps[S.b0], fb, kc, U.tn * BN);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              tma_load_2d(sb + c * 8192u, &p.maps[S.b0], fb, U.tn * BN + c * 64, kc);
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // let this CTA's copies land before its shared memory is released
+        for (int s = 0; s < STAGES; ++s)
+          if (armed[s] >= 0) wait_phase_drain(full_bar(s), static_cast<uint32_t>(armed[s]), p);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
+        const Unit U = decode_unit(p, u);
+        const GroupDesc& G = p.grp[U.g];
+        if (!wait_phase(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        uint32_t accumulate = 0;
+        int seg = 0, seg_base = 0;
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
+          while (kb >= seg_base + G.seg[seg].kblocks) {
+            seg_base += G.seg[seg].kblocks;
+            ++seg;
+          }
+          const int kc = (kb - seg_base) * kBK;
+          const int kvalid = G.seg[seg].kvalid;
+          if (!wait_phase(full_bar(stage), phase, abort_flag, p)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t sa = sbase + stage * C::kStageBytes;
+          const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            if (kc + 16 * k < kvalid) {
+              const uint64_t adesc = A_MN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                          : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+              const uint64_t bdesc = B_MN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
+                                          : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
+              tc_mma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
+              accumulate = 1;
+            }
+          }
+          tc_commit(empty_bar(stage));     // frees this smem stage once its MMAs are done
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(acc));         // accumulator ready for the epilogue
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok) {
+        tc_commit(drain_bar);
+        wait_phase_drain(drain_bar, 0, p);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                       // TMEM lane quarter of this warp
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < p.total_units; u += gridDim.x) {
+      const Unit U = decode_unit(p, u);
+      const GroupDesc& G = p.grp[U.g];
+      // tcgen05.ld is warp-collective: the whole warp proceeds or the whole warp stops
+      const bool ready = wait_phase(tfull_bar(acc), acc_phase, abort_flag, p);
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after_sync();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const int row = U.tm * kBM + row_in_tile;
+      const bool row_ok = row < G.M;
+
+      if (G.epi == EPI_STORE) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(G.out0);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld32(tacc + c, v);
+          tmem_ld_wait();
+          const int col0 = U.tn * BN + c;
+          if (row_ok) {
+            __nv_bfloat16* dst = out + static_cast<long long>(row) * G.ldo + col0;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              if (col0 + j + 8 <= G.N) {
+                uint4 w;
+                w.x = pack_bf16x2(__uint_as_float(v[j + 0]), __uint_as_float(v[j + 1]));
+                w.y = pack_bf16x2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                w.z = pack_bf16x2(__uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]));
+                w.w = pack_bf16x2(__uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]));
+                *reinterpret_cast<uint4*>(dst + j) = w;
+              }
+            }
+          }
+        }
+      } else if (G.epi == EPI_ACT_FWD) {
+        // gate in accumulator columns [0, BN/2), up in [BN/2, BN)
+        __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(G.out0);
+        __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(G.out1);
+        __nv_bfloat16* uout = static_cast<__nv_bfloat16*>(G.out2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t vg[32], vu[32];
+          __syncwarp();
+          tmem_ld32(tacc + c, vg);
+          tmem_ld32(tacc + BN / 2 + c, vu);
+          tmem_ld_wait();
+          const int col0 = U.tn * (BN / 2) + c;
+          if (row_ok) {
+            const long long off = static_cast<long long>(row) * G.ldo + col0;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              if (col0 + j + 8 <= G.N) {
+                float hv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  hv[e] = act_fwd(__uint_as_float(vg[j + e]), p.act) * __uint_as_float(vu[j + e]);
+                uint4 w;
+                w.x = pack_bf16x2(hv[0], hv[1]);
+                w.y = pack_bf16x2(hv[2], hv[3]);
+                w.z = pack_bf16x2(hv[4], hv[5]);
+                w.w = pack_bf16x2(hv[6], hv[7]);
+                *reinterpret_cast<uint4*>(hout + off + j) = w;
+                if (gout != nullptr) {
+                  uint4 wg, wu;
+                  wg.x = pack_bf16x2(__uint_as_float(vg[j + 0]), __uint_as_float(vg[j + 1]));
+                  wg.y = pack_bf16x2(__uint_as_float(vg[j + 2]), __uint_as_float(vg[j + 3]));
+                  wg.z = pack_bf16x2(__uint_as_float(vg[j + 4]), __uint_as_float(vg[j + 5]));
+                  wg.w = pack_bf16x2(__uint_as_float(vg[j + 6]), __uint_as_float(vg[j + 7]));
+                  wu.x = pack_bf16x2(__uint_as_float(vu[j + 0]), __uint_as_float(vu[j + 1]));
+                  wu.y = pack_bf16x2(__uint_as_float(vu[j + 2]), __uint_as_float(vu[j + 3]));
+                  wu.z = pack_bf16x2(__uint_as_float(vu[j + 4]), __uint_as_float(vu[j + 5]));
+                  wu.w = pack_bf16x2(__uint_as_float(vu[j + 6]), __uint_as_float(vu[j + 7]));
+                  *reinterpret_cast<uint4*>(gout + off + j) = wg;
+                  *reinterpret_cast<uint4*>(uout + off + j) = wu;
+                }
+              }
+            }
+          }
+        }
+      } else if (G.epi == EPI_ACT_BWD) {
+        // accumulator = dh; saved g, u give dg = dh * u * act'(g), du = dh * act(g)
+        const __nv_bfloat16* gin = static_cast<const __nv_bfloat16*>(G.in0);
+        const __nv_bfloat16* uin = static_cast<const __nv_bfloat16*>(G.in1);
+        __nv_bfloat16* dgo = static_cast<__nv_bfloat16*>(G.out0);
+        __nv_bfloat16* duo = static_cast<__nv_bfloat16*>(G.out1);
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          const int col0 = U.tn * BN + c;
+          uint4 gw[4], uw[4];
+          const long long ioff = static_cast<long long>(row) * G.ldi + col0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (row_ok && col0 + 8 * j + 8 <= G.N) {
+              gw[j] = __ldg(reinterpret_cast<const uint4*>(gin + ioff + 8 * j));
+              uw[j] = __ldg(reinterpret_cast<const uint4*>(uin + ioff + 8 * j));
+            } else {
+              gw[j] = make_uint4(0, 0, 0, 0);
+              uw[j] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld32(tacc + c, v);
+          tmem_ld_wait();
+          if (row_ok) {
+            const long long ooff = static_cast<long long>(row) * G.ldo + col0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (col0 + 8 * j + 8 <= G.N) {
+                const uint32_t gg[4] = {gw[j].x, gw[j].y, gw[j].z, gw[j].w};
+                const uint32_t uu[4] = {uw[j].x, uw[j].y, uw[j].z, uw[j].w};
+                uint32_t og[4], ou[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float a0, ap0, a1, ap1;
+                  const float g0 = bf16_lo(gg[e]), g1 = bf16_hi(gg[e]);
+                  const float u0 = bf16_lo(uu[e]), u1 = bf16_hi(uu[e]);
+                  act_fwd_bwd(g0, p.act, a0, ap0);
+                  act_fwd_bwd(g1, p.act, a1, ap1);
+                  const float d0 = __uint_as_float(v[8 * j + 2 * e]);
+                  const float d1 = __uint_as_float(v[8 * j + 2 * e + 1]);
+                  og[e] = pack_bf16x2(d0 * u0 * ap0, d1 * u1 * ap1);
+                  ou[e] = pack_bf16x2(d0 * a0, d1 * a1);
+                }
+                *reinterpret_cast<uint4*>(dgo + ooff + 8 * j) = make_uint4(og[0], og[1], og[2], og[3]);
+                *reinterpret_cast<uint4*>(duo + ooff + 8 * j) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+              }
+            }
+          }
+        }
+      } else {
+        // EPI_PARTIAL: f32 tile into the split's slab (rows and columns padded)
+        const long long width = static_cast<long long>(G.tiles_n) * BN;
+        float* dst = G.part + (static_cast<long long>(U.split) * G.tiles_m * kBM + row) * width + U.tn * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld32(tacc + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<uint4*>(dst + c + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace lgb

@@ -1,0 +1,166 @@
+// Host-side plumbing shared by the entry points: tensor-map encoding, the GEMM plan
+// builder, workspace carving, launch wrappers (with the launch counter and the
+// optional event trace).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/lora_gb300.h"
+#include "aux_kernels.cuh"
+#include "gemm_tc.cuh"
+
+namespace lgb {
+
+// Kernel variants (tile width BN, operand majors) compiled into the library.
+enum Variant : int {
+  V256_KK = 0,     // big GEMMs, K-major A and B: forward projections
+  V256_KMN = 1,    // big GEMMs, B MN-major: dh and input gradients (W used untransposed)
+  V64_KK = 2,      // token-major rank-r projections, padded rank <= 64
+  V64_MNMN = 3,    // reductions over tokens (dA, dB), padded rank <= 64
+  V128_KK = 4,
+  V128_MNMN = 5,
+  kNumVariants = 6
+};
+
+constexpr int variant_bn(int v) { return (v <= V256_KMN) ? 256 : (v <= V64_MNMN ? 64 : 128); }
+constexpr bool variant_a_mn(int v) { return v == V64_MNMN || v == V128_MNMN; }
+constexpr bool variant_b_mn(int v) { return v == V256_KMN || v == V64_MNMN || v == V128_MNMN; }
+
+// Defined in gemm_big.cu / gemm_skinny.cu.
+cudaError_t launch_tc_big(int variant, const TcParams& p, int grid, cudaStream_t st);
+cudaError_t launch_tc_skinny(int variant, const TcParams& p, int grid, cudaStream_t st);
+int tc_smem_bytes(int variant);
+
+// Defined in lora_api.cu.
+int num_sms();
+bool encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                uint32_t box_inner, uint32_t box_outer);
+lora_status_t launch_gemm(int variant, const TcParams& p, int kind, cudaStream_t st);
+lora_status_t launch_pack(const PackParams& p, cudaStream_t st);
+lora_status_t launch_reduce(const RedParams& p, cudaStream_t st);
+
+constexpr int kTargetUnits = 304;     // work units aimed at for split-K (2 per SM)
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// Padded width of the rank-r operands of `nslots` adapters sharing one input.
+inline int fold_width(int nslots, int r) { return static_cast<int>(round_up(static_cast<int64_t>(nslots) * r, 64)); }
+inline int skinny_bn(int kf) { return kf <= 64 ? 64 : 128; }
+inline int skinny_kk(int kf) { return kf <= 64 ? V64_KK : V128_KK; }
+inline int skinny_mnmn(int kf) { return kf <= 64 ? V64_MNMN : V128_MNMN; }
+
+inline int choose_splits(int64_t tiles, int64_t kb_total) {
+  int64_t s = ceil_div(kTargetUnits, tiles);
+  s = s < 1 ? 1 : s;
+  if (s > 8) s = 8;
+  const int64_t maxs = kb_total / 4 > 0 ? kb_total / 4 : 1;
+  if (s > maxs) s = maxs;
+  return static_cast<int>(s);
+}
+
+// Bump allocator over a caller-provided buffer (256-byte aligned regions).  Used
+// both to size (base == nullptr) and to carve.
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(static_cast<uint8_t*>(b)) {}
+  void* take(size_t bytes) {
+    off = static_cast<size_t>(round_up(static_cast<int64_t>(off), 256));
+    void* p = base ? base + off : nullptr;
+    off += bytes;
+    return p;
+  }
+  template <class T>
+  T* take_n(int64_t n) { return static_cast<T*>(take(static_cast<size_t>(n) * sizeof(T))); }
+  // Offset (from the base) of a region of `bytes`, carved like take().
+  size_t offset_of(size_t bytes) {
+    off = static_cast<size_t>(round_up(static_cast<int64_t>(off), 256));
+    const size_t at = off;
+    off += bytes;
+    return at;
+  }
+};
+
+constexpr size_t kWsHeader = 256;
+
+// Builds the TcParams of one GEMM launch.
+struct GemmPlan {
+  TcParams p;
+  int variant;
+  int bn;
+  bool ok = true;
+
+  explicit GemmPlan(int v) : variant(v), bn(variant_bn(v)) {
+    std::memset(static_cast<void*>(&p), 0, sizeof(p));
+    p.band = 8;
+    p.timeout_ns = kTimeoutNs;
+  }
+
+  int add_map(const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t bi, uint32_t bo) {
+    if (!ok || p.nmaps >= kMaxMaps) { ok = false; return -1; }
+    if (!encode_map(&p.maps[p.nmaps], base, inner, outer, ld, bi, bo)) { ok = false; return -1; }
+    return p.nmaps++;
+  }
+  // A operand, K-major: activation [rows x K] with row stride ld.
+  int a_kmajor(const void* base, int64_t rows, int64_t K, int64_t ld) {
+    return add_map(base, K, rows, ld, 64, kBM);
+  }
+  // A operand, MN-major: source [K x rows] (K = tokens, rows = features contiguous).
+  int a_mnmajor(const void* base, int64_t rows, int64_t K, int64_t ld) {
+    return add_map(base, rows, K, ld, 64, 64);
+  }
+  // B operand, K-major: [N x K]; box_rows = BN, or BN/2 for a split (gate/up) tile.
+  int b_kmajor(const void* base, int64_t N, int64_t K, int64_t ld, int box_rows) {
+    return add_map(base, K, N, ld, 64, box_rows);
+  }
+  // B operand, MN-major: source [K x N] (N contiguous).
+  int b_mnmajor(const void* base, int64_t N, int64_t K, int64_t ld) {
+    return add_map(base, N, K, ld, 64, 64);
+  }
+
+  GroupDesc& group(int M, int N, int epi, bool split_n_tile) {
+    GroupDesc& G = p.grp[p.ngroups++];
+    G.M = M;
+    G.N = N;
+    G.epi = epi;
+    G.tiles_m = static_cast<int>(ceil_div(M, kBM));
+    G.tiles_n = static_cast<int>(ceil_div(N, split_n_tile ? bn / 2 : bn));
+    G.splits = 1;
+    return G;
+  }
+  static void seg(GroupDesc& G, int a, int b0, int b1, int64_t K, int64_t kvalid) {
+    SegDesc& S = G.seg[G.nseg++];
+    S.a = a;
+    S.b0 = b0;
+    S.b1 = b1;
+    S.kblocks = static_cast<int>(ceil_div(K, kBK));
+    S.kvalid = static_cast<int>(kvalid);
+    G.kb_total += S.kblocks;
+  }
+  // Total work units; call after every group and segment is in place.
+  void finish() {
+    int u = 0;
+    for (int g = 0; g < p.ngroups; ++g) {
+      p.grp[g].unit_begin = u;
+      u += p.grp[g].tiles_m * p.grp[g].tiles_n * p.grp[g].splits;
+    }
+    p.total_units = u;
+    int maxtn = 1;
+    for (int g = 0; g < p.ngroups; ++g) maxtn = p.grp[g].tiles_n > maxtn ? p.grp[g].tiles_n : maxtn;
+    p.band = maxtn < 8 ? maxtn : 8;
+  }
+};
+
+// f32 partial slab size of a split-K group: [splits][tiles_m*128][tiles_n*BN].
+inline int64_t partial_elems(int64_t rows, int64_t kf, int bn, int splits) {
+  return static_cast<int64_t>(splits) * round_up(rows, kBM) * round_up(kf, bn);
+}
+
+}  // namespace lgb
