@@ -1,0 +1,429 @@
+#!/usr/bin/env python3
+"""LoRA-MLP forward + backward throughput on one GB300 (or N independent replicas).
+
+One step = lora_mlp_forward + lora_mlp_backward over one batch of the 7B-shaped
+workload (M = 8192 tokens = 4 x 2048, h = 4096, i = 14336, r = 16, alpha = 32,
+SwiGLU, bf16), synthetic seeded inputs resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU with no
+collective on the data path ("replicas only": the block's work has no exchange
+step on one batch); value = tokens of all ranks / the slowest rank's time.
+
+--impl reference times the CPU float64 oracle (the only other implementation of
+this method here) on a bounded sample of the same workload, on the host's cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-MLP fwd+bwd tokens/s and TFLOP/s as % of GB300 dense-BF16 peak"
+WORKLOAD = "llama7b"
+
+
+# ---------------------------------------------------------------------------- ranks
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(backend: str):
+    rank, world, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value over all ranks (the slowest rank's time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_steps(step, steps: int, world: int, device=None, sync=None, timer=None):
+    """Barrier + sync, run `steps` steps inside the timer, sync + barrier; returns the
+    max over ranks of the elapsed seconds.  `timer` is a (start, stop) pair whose
+    stop returns seconds (CUDA events on the GPU, perf_counter on the CPU)."""
+    sync = sync or (lambda: None)
+    barrier(world, device)
+    sync()
+    start, stop = timer
+    start()
+    for _ in range(steps):
+        step()
+    secs = stop()
+    sync()
+    barrier(world, device)
+    return max_over_ranks(secs, world, device)
+
+
+def cuda_timer(torch, stream):
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+
+    def start():
+        e0.record(stream)
+
+    def stop():
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3
+
+    return start, stop
+
+
+# ---------------------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader",
+                                          "-lms", "200", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        return parse_clock_rows(rows)
+
+
+def parse_clock_rows(rows):
+    def num(s):
+        try:
+            return float(s.split()[0])
+        except (ValueError, IndexError):
+            return None
+    sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+    mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+    pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+    if not sm:
+        return None
+    # under load: samples above half of the peak power seen in the region
+    pmax = max(pw) if pw else 0.0
+    loaded = [num(r[1]) for r in rows if pw and num(r[3]) is not None and num(r[3]) >= 0.5 * pmax] or sm
+    reasons = sorted({REASONS[j] for r in rows for j in range(4) if r[5 + j].lower() == "active"})
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx) if mx else None,
+            "reasons": reasons, "samples": len(rows), "power_w_max": pmax}
+
+
+# ---------------------------------------------------------------------------- flops
+
+def kernel_flops(cfg):
+    """Algorithmic FLOPs per launch of each GEMM kind of one MLP step."""
+    M, h, i, r = cfg.M, cfg.h, cfg.i, cfg.r
+    return {"gate_up": 4.0 * M * i * (h + r), "proj": 2.0 * M * h * (i + r),
+            "act_bwd": 2.0 * M * i * (h + r), "dgrad": 4.0 * M * h * (i + r)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from profiles/traffic.md, if that capture
+    was taken on the current kernel source; else None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    src = os.path.join(ROOT, "rank_mlp_gb300", "csrc", "gemm_tc.cuh")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(path):
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) >= 4 and cells[0] == kernel and cells[2] == sha:
+                return float(cells[3])
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------- oracle
+
+def oracle_step_fn(cfg, tokens: int, host):
+    """One oracle fwd+bwd over the first `tokens` rows of the workload."""
+    import oracle
+    v = host
+    x, dy = v["x"][:tokens], v["dy"][:tokens]
+
+    def step():
+        args = (x, v["W_gate"], v["A_gate"], v["B_gate"], v["W_up"], v["A_up"], v["B_up"],
+                v["W_down"], v["A_down"], v["B_down"], cfg.s, cfg.act)
+        oracle.mlp_forward(*args)
+        oracle.mlp_backward(*args, dy)
+    return step
+
+
+def host_inputs(cfg, max_tokens: int):
+    """Float64 copies of the workload's bf16 inputs (tokens truncated)."""
+    import torch
+    import synth
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    c = cfg.replace(M=max_tokens)
+    t = synth.make_mlp_inputs(c, seed=0, device=dev)
+    return {k: synth.bf16_to_f64(x) for k, x in t.items()}
+
+
+def cpu_baseline(cfg, budget_s: float = 15.0):
+    """Times the oracle as it stands on a sample of tokens sized for ~budget_s."""
+    probe = 64
+    host = host_inputs(cfg, 4096)
+    t0 = time.perf_counter()
+    oracle_step_fn(cfg, probe, host)()
+    per_tok = (time.perf_counter() - t0) / probe
+    tokens = int(max(probe, min(4096, budget_s / max(per_tok, 1e-9))))
+    step = oracle_step_fn(cfg, tokens, host)
+    t0 = time.perf_counter()
+    step()
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"fwd+bwd of the first {tokens} of {cfg.M} tokens (all weights full size), "
+                      f"float64 numpy/BLAS, {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import synth
+    cfg = synth.MLP_CONFIGS[args.workload]
+    host = host_inputs(cfg, 4096)
+    probe = 32
+    t0 = time.perf_counter()
+    oracle_step_fn(cfg, probe, host)()
+    per_tok = (time.perf_counter() - t0) / probe
+    budget = 150.0 / max(args.steps + args.warmup, 1)        # whole run within a few minutes
+    tokens = int(max(16, min(4096, budget / max(per_tok, 1e-9))))
+    step = oracle_step_fn(cfg, tokens, host)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = time.perf_counter() - t0
+    value = tokens * args.steps / secs
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator), bounded token sample",
+        "config": {"workload": workload_name(cfg), "sample_tokens": tokens},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"fwd+bwd of {tokens} of {cfg.M} tokens per step, float64 numpy/BLAS"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_name(cfg):
+    return (f"{cfg.name}-shaped LoRA-MLP fwd+bwd: M={cfg.M} tokens ({cfg.batch}x{cfg.seq}), h={cfg.h}, "
+            f"i={cfg.i}, r={cfg.r}, alpha={cfg.alpha:g}, {cfg.act}")
+
+
+def run_ours(args):
+    import torch
+    import synth
+    from rank_mlp_gb300 import binding as lib
+
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist_init("nccl")
+    lib.load()
+    cfg = synth.MLP_CONFIGS[args.workload]
+    M, h, i, r = cfg.M, cfg.h, cfg.i, cfg.r
+    t = synth.make_mlp_inputs(cfg, seed=0, device=device)
+    lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
+    gate, up, down = lin("gate"), lin("up"), lin("down")
+    saved_b, ws_b = lib.mlp_sizes(M, h, i, r)
+    saved = torch.empty(saved_b, dtype=torch.uint8, device=device)
+    ws = torch.zeros(ws_b, dtype=torch.uint8, device=device)
+    y = torch.empty(M, h, dtype=torch.bfloat16, device=device)
+    dx = torch.empty(M, h, dtype=torch.bfloat16, device=device)
+    e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=device)  # noqa: E731
+    grads = {"dA_gate": e(r, h), "dB_gate": e(i, r), "dA_up": e(r, h), "dB_up": e(i, r),
+             "dA_down": e(r, i), "dB_down": e(h, r)}
+    x, dy = t["x"], t["dy"]
+
+    def step():
+        lib.mlp_forward(x, gate, up, down, cfg.s, cfg.act, y=y, saved=saved, ws=ws)
+        lib.mlp_backward(x, gate, up, down, cfg.s, cfg.act, saved, dy, dx=dx, grads=grads, ws=ws)
+
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region, with the per-launch event trace
+    lib.trace_enable(64 * args.steps + 64)
+    n0 = lib.launch_count()
+    clocks = ClockSampler()
+    if rank == 0:
+        clocks.start()
+    secs = timed_steps(step, args.steps, world, device, torch.cuda.synchronize, cuda_timer(torch, stream))
+    clk = clocks.stop() if rank == 0 else None
+    launches = lib.launch_count() - n0
+    trace = lib.trace_read(64 * args.steps + 64)
+    lib.trace_enable(0)
+    status = lib.poll_status(ws)
+    if status != 0:
+        raise RuntimeError(f"kernel status {status} after the timed region")
+
+    per_kind = {}
+    for k, ms in trace:
+        a = per_kind.setdefault(k, [0, 0.0])
+        a[0] += 1
+        a[1] += ms
+    flops = kernel_flops(cfg)
+    dom = max((k for k in per_kind if k in flops), key=lambda k: per_kind[k][1])
+    dom_ms = per_kind[dom][1] / per_kind[dom][0]
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops_sustained"])
+    achieved = flops[dom] / (dom_ms * 1e-3) / 1e12
+    ms_step = secs / args.steps * 1e3
+    tflops = cfg.flops() / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through host buffers: H2D of x, dy; D2H of y, dx and the grads
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        dyh = dy.cpu().pin_memory()
+        yh = torch.empty(M, h, dtype=torch.bfloat16).pin_memory()
+        dxh = torch.empty(M, h, dtype=torch.bfloat16).pin_memory()
+        gh = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in grads.items()}
+        xd, dyd = torch.empty_like(x), torch.empty_like(dy)
+
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            dyd.copy_(dyh, non_blocking=True)
+            lib.mlp_forward(xd, gate, up, down, cfg.s, cfg.act, y=y, saved=saved, ws=ws)
+            lib.mlp_backward(xd, gate, up, down, cfg.s, cfg.act, saved, dyd, dx=dx, grads=grads, ws=ws)
+            yh.copy_(y, non_blocking=True)
+            dxh.copy_(dx, non_blocking=True)
+            for k in grads:
+                gh[k].copy_(grads[k], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        ke = max(1, min(args.steps, 50))
+        esecs = timed_steps(e2e_step, ke, world, device, torch.cuda.synchronize, cuda_timer(torch, stream))
+        h2d = 2 * M * h * 2
+        d2h = 2 * M * h * 2 + sum(v.numel() * 2 for v in grads.values())
+        e2e = {"value": world * M * ke / esecs, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": ke,
+               "path": "pinned host x, dy -> device; lora_mlp_forward + lora_mlp_backward; y, dx, dA, dB -> host"}
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        del t
+        torch.cuda.empty_cache()
+        cpu = cpu_baseline(cfg)
+    traffic = ncu_traffic(dom)
+    line = {
+        "metric": METRIC, "value": world * M * args.steps / secs, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generator: x, dy ~ N(0,1), W ~ N(0,1/fan_in), A ~ U(+-1/sqrt(fan_in)), "
+                "B ~ N(0,0.02))",
+        "config": {"workload": workload_name(cfg), "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (weights 352 MB + activations per step)"},
+        "tflops": tflops, "pct_of_peak": 100.0 * tflops / peak, "peak_tflops": peak,
+        "peak_source": f"{peak_src} bf16_tflops_sustained",
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None if traffic is None else traffic / 1.0,
+                     "launch_ms": dom_ms, "flops_per_launch": flops[dom]},
+        "kernels_ms_per_step": {k: v[1] / args.steps for k, v in sorted(per_kind.items())},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

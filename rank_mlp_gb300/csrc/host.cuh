@@ -57,6 +57,7 @@ inline int skinny_kk(int kf) { return kf <= 64 ? V64_KK : V128_KK; }
 inline int skinny_mnmn(int kf) { return kf <= 64 ? V64_MNMN : V128_MNMN; }
 
 inline int choose_splits(int64_t tiles, int64_t kb_total) {
+  if (tiles <= 0 || kb_total <= 0) return 1;
   int64_t s = ceil_div(kTargetUnits, tiles);
   s = s < 1 ? 1 : s;
   if (s > 8) s = 8;

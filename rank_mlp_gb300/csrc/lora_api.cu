@@ -374,7 +374,9 @@ extern "C" lora_status_t lora_linear_forward(int64_t M, int64_t in, int64_t out,
   check_size(in, st);
   check_size(out, st);
   if (st != LORA_OK) return st;
-  if (x == nullptr || y == nullptr || lin.W == nullptr || lin.A == nullptr || lin.B == nullptr || ws == nullptr)
+  const bool tok = M > 0;   // activations may be NULL when there are no tokens
+  if ((tok && (x == nullptr || y == nullptr)) || lin.W == nullptr || lin.A == nullptr || lin.B == nullptr ||
+      ws == nullptr)
     return LORA_ERR_INVALID_ARG;
   if (r > 256) return LORA_ERR_UNSUPPORTED;
   if (in % 8 || out % 8 || !aligned(x, 16) || !aligned(y, 16) || !aligned(lin.W, 16) || !aligned(lin.A, 2) ||
@@ -421,7 +423,8 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   check_size(in, st);
   check_size(out, st);
   if (st != LORA_OK) return st;
-  if (x == nullptr || dy == nullptr || dx == nullptr || saved == nullptr || lin.W == nullptr ||
+  const bool tok = M > 0;
+  if ((tok && (x == nullptr || dy == nullptr || dx == nullptr)) || saved == nullptr || lin.W == nullptr ||
       lin.A == nullptr || lin.B == nullptr || grads.dA == nullptr || grads.dB == nullptr || ws == nullptr)
     return LORA_ERR_INVALID_ARG;
   if (r > 256) return LORA_ERR_UNSUPPORTED;
@@ -570,7 +573,7 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
                                           lora_linear_t down, void* y, void* saved, void* ws, size_t ws_bytes,
                                           cudaStream_t stream) {
   LGB_TRY(check_mlp(M, h, i, r, s, static_cast<int>(act)));
-  if (!x || !y || !ws || !lin_ok(gate) || !lin_ok(up) || !lin_ok(down)) return LORA_ERR_INVALID_ARG;
+  if ((M > 0 && (!x || !y)) || !ws || !lin_ok(gate) || !lin_ok(up) || !lin_ok(down)) return LORA_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !lin_aligned(gate) || !lin_aligned(up) || !lin_aligned(down) ||
       !aligned(ws, 256) || (saved && !aligned(saved, 256)))
     return LORA_ERR_ALIGNMENT;
@@ -661,7 +664,7 @@ extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int 
                                            lora_grads_t d_gate, lora_grads_t d_up, lora_grads_t d_down, void* ws,
                                            size_t ws_bytes, cudaStream_t stream) {
   LGB_TRY(check_mlp(M, h, i, r, s, static_cast<int>(act)));
-  if (!x || !dy || !dx || !saved || !ws || !lin_ok(gate) || !lin_ok(up) || !lin_ok(down) || !d_gate.dA ||
+  if ((M > 0 && (!x || !dy || !dx)) || !saved || !ws || !lin_ok(gate) || !lin_ok(up) || !lin_ok(down) || !d_gate.dA ||
       !d_gate.dB || !d_up.dA || !d_up.dB || !d_down.dA || !d_down.dB)
     return LORA_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(dy, 16) || !aligned(dx, 16) || !lin_aligned(gate) || !lin_aligned(up) ||
@@ -863,8 +866,8 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
   LGB_TRY(check_qkvo(M, h, n_q, n_kv, r, s));
   if (bias_qkv != nullptr) return LORA_ERR_UNSUPPORTED;
   if (!ws || (!x && !o_in)) return LORA_ERR_INVALID_ARG;
-  if (x && (!yq || !yk || !yv || !lin_ok(q) || !lin_ok(k) || !lin_ok(v))) return LORA_ERR_INVALID_ARG;
-  if (o_in && (!yo || !lin_ok(o))) return LORA_ERR_INVALID_ARG;
+  if (x && ((M > 0 && (!yq || !yk || !yv)) || !lin_ok(q) || !lin_ok(k) || !lin_ok(v))) return LORA_ERR_INVALID_ARG;
+  if (o_in && ((M > 0 && !yo) || !lin_ok(o))) return LORA_ERR_INVALID_ARG;
   if (!aligned(ws, 256) || (saved && !aligned(saved, 256))) return LORA_ERR_ALIGNMENT;
   if (x && (!aligned(x, 16) || !aligned(yq, 16) || !aligned(yk, 16) || !aligned(yv, 16) || !lin_aligned(q) ||
             !lin_aligned(k) || !lin_aligned(v)))
@@ -957,10 +960,10 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
                                             cudaStream_t stream) {
   LGB_TRY(check_qkvo(M, h, n_q, n_kv, r, s));
   if (!ws || !saved || (!x && !o_in)) return LORA_ERR_INVALID_ARG;
-  if (x && (!dyq || !dyk || !dyv || !dx || !lin_ok(q) || !lin_ok(k) || !lin_ok(v) || !d_q.dA || !d_q.dB ||
+  if (x && ((M > 0 && (!dyq || !dyk || !dyv || !dx)) || !lin_ok(q) || !lin_ok(k) || !lin_ok(v) || !d_q.dA || !d_q.dB ||
             !d_k.dA || !d_k.dB || !d_v.dA || !d_v.dB))
     return LORA_ERR_INVALID_ARG;
-  if (o_in && (!dyo || !do_in || !lin_ok(o) || !d_o.dA || !d_o.dB)) return LORA_ERR_INVALID_ARG;
+  if (o_in && ((M > 0 && (!dyo || !do_in)) || !lin_ok(o) || !d_o.dA || !d_o.dB)) return LORA_ERR_INVALID_ARG;
   if (!aligned(ws, 256) || !aligned(saved, 256)) return LORA_ERR_ALIGNMENT;
   if (x && (!aligned(x, 16) || !aligned(dyq, 16) || !aligned(dyk, 16) || !aligned(dyv, 16) || !aligned(dx, 16) ||
             !lin_aligned(q) || !lin_aligned(k) || !lin_aligned(v) || !aligned(d_q.dA, 2) || !aligned(d_q.dB, 2) ||

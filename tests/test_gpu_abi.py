@@ -1,0 +1,116 @@
+"""The C ABI on the GPU: writes stay inside the buffers the caller passed (guard
+bands around every output, the saved blob and the workspace), M = 0 backward
+zero-fills the adapter gradients, errors launch nothing, the launch counter and
+the event trace account for every kernel, and the status word reads OK."""
+
+import pytest
+import torch
+
+import synth
+from helpers import MLP_GRADS, f64, mlp_oracle, parity, to_f64_dict
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+GUARD = 4096          # bytes of canary on each side
+CANARY = 0x5A
+
+
+class Guarded:
+    """Contiguous bf16 views carved out of one byte buffer with canaries around each."""
+
+    def __init__(self):
+        self.parts = []
+
+    def bf16(self, *shape):
+        n = 2 * int(torch.tensor(shape).prod())
+        buf = torch.full((n + 2 * GUARD,), CANARY, dtype=torch.uint8, device=DEV)
+        self.parts.append(buf)
+        return buf[GUARD:GUARD + n].view(torch.bfloat16).view(*shape)
+
+    def raw(self, nbytes):
+        buf = torch.full((nbytes + 2 * GUARD,), CANARY, dtype=torch.uint8, device=DEV)
+        self.parts.append(buf)
+        return buf[GUARD:GUARD + nbytes]
+
+    def check(self):
+        torch.cuda.synchronize()
+        for b in self.parts:
+            assert torch.all(b[:GUARD] == CANARY) and torch.all(b[-GUARD:] == CANARY), "guard band overwritten"
+
+
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("qwen05b", {"M": 333, "i": 4856})])
+def test_mlp_writes_stay_in_bounds(lib, name, over):
+    cfg = synth.MLP_CONFIGS[name].replace(**over)
+    ins = synth.make_mlp_inputs(cfg, seed=1)
+    t = {k: x.to(DEV) for k, x in ins.items()}
+    M, h, i, r = cfg.M, cfg.h, cfg.i, cfg.r
+    saved_b, ws_b = lib.mlp_sizes(M, h, i, r)
+    G = Guarded()
+    y = G.bf16(M, h)
+    saved = G.raw(saved_b)
+    ws = G.raw(ws_b)
+    ws[:256].zero_()
+    grads = {"dA_gate": G.bf16(r, h), "dB_gate": G.bf16(i, r), "dA_up": G.bf16(r, h),
+             "dB_up": G.bf16(i, r), "dA_down": G.bf16(r, i), "dB_down": G.bf16(h, r)}
+    dx = G.bf16(M, h)
+    lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
+    lib.mlp_forward(t["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, y=y, saved=saved, ws=ws)
+    g = lib.mlp_backward(t["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, saved, t["dy"],
+                         dx=dx, grads=grads, ws=ws)
+    G.check()
+    assert lib.poll_status(ws) == 0
+    f, b = mlp_oracle(to_f64_dict(ins), cfg)
+    parity("y", y, f["y"])
+    for k in MLP_GRADS:
+        parity(k, g[k], b[k])
+
+
+def test_zero_tokens(lib):
+    cfg = synth.MLP_CONFIGS["tiny"]
+    ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg).items()}
+    x0 = torch.empty(0, cfg.h, dtype=torch.bfloat16, device=DEV)
+    lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
+    before = lib.launch_count()
+    y, saved = lib.mlp_forward(x0, lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act)
+    g = lib.mlp_backward(x0, lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, saved, x0)
+    torch.cuda.synchronize()
+    assert lib.launch_count() == before
+    assert y.shape == (0, cfg.h) and g["dx"].shape == (0, cfg.h)
+    for k in ("dA_gate", "dB_gate", "dA_up", "dB_up", "dA_down", "dB_down"):
+        assert torch.count_nonzero(g[k]).item() == 0
+
+
+def test_errors_launch_nothing(lib):
+    from rank_mlp_gb300.binding import LoraError
+    cfg = synth.MLP_CONFIGS["tiny"]
+    ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg).items()}
+    lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
+    before = lib.launch_count()
+    small = torch.zeros(512, dtype=torch.uint8, device=DEV)
+    with pytest.raises(LoraError) as e:
+        lib.mlp_forward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, ws=small)
+    assert e.value.status == 4
+    with pytest.raises(LoraError) as e:
+        lib.mlp_forward(ins["x"], lin("gate"), lin("up"), lin("down"), float("nan"), cfg.act)
+    with pytest.raises(ValueError):
+        lib.mlp_forward(ins["x"].float(), lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act)
+    torch.cuda.synchronize()
+    assert lib.launch_count() == before
+
+
+def test_launch_count_and_trace(lib):
+    cfg = synth.MLP_CONFIGS["tiny"].replace(M=512)
+    ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg).items()}
+    lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
+    lib.trace_enable(256)
+    before = lib.launch_count()
+    y, saved = lib.mlp_forward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act)
+    lib.mlp_backward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, saved, ins["dy"])
+    n = lib.launch_count() - before
+    tr = lib.trace_read()
+    lib.trace_enable(0)
+    assert len(tr) == n > 0
+    kinds = {k for k, _ in tr}
+    assert {"gate_up", "proj", "act_bwd", "dgrad", "pack", "rank_proj", "rank_grad"} <= kinds
+    assert all(ms > 0 for _, ms in tr)
+    assert lib.poll_status() == 0

@@ -1,0 +1,159 @@
+"""GPU path vs the CPU float64 oracle on small and ragged problems (seconds each).
+
+Sizes span several 128 x 256 tiles with ragged tails in M, N and K, ranks that
+pad the folded K-segment (r = 1, 5, 8) and ranks that fill it (r = 64), both
+activations, and the degenerate cases: one token, zero tokens, B = 0 (the base
+projections alone, adapter gradients exactly zero) and s = 0.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import MLP_GRADS, f64, mlp_gpu, mlp_oracle, parity, qkvo_gpu, qkvo_oracle, to_f64_dict
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _randn(shape, scale, seed):
+    g = torch.Generator().manual_seed(seed)
+    return synth.f64_to_bf16((torch.randn(*shape, generator=g, dtype=torch.float64) * scale))
+
+
+def _linear(M, fin, fout, r, seed):
+    x = _randn((M, fin), 1.0, seed)
+    W = _randn((fout, fin), fin ** -0.5, seed + 1)
+    A = _randn((r, fin), fin ** -0.5, seed + 2)
+    B = _randn((fout, r), 0.02 ** 0.5, seed + 3)
+    dy = _randn((M, fout), 1.0, seed + 4)
+    return x, W, A, B, dy
+
+
+@pytest.mark.parametrize("M,fin,fout,r", [
+    (256, 256, 512, 8),      # whole tiles
+    (300, 192, 328, 5),      # ragged M, K and N; r pads the fold
+    (1, 64, 64, 1),          # one token, rank 1
+    (129, 4096, 1024, 64),   # one row past a tile, full fold width
+    (127, 520, 136, 16),     # K not a multiple of 64, N < one tile
+])
+def test_linear_forward_backward(lib, M, fin, fout, r):
+    s = 2.0
+    x, W, A, B, dy = _linear(M, fin, fout, r, seed=M + fin)
+    d = lambda t: t.to(DEV)  # noqa: E731
+    y, saved = lib.linear_forward(d(x), (d(W), d(A), d(B)), s)
+    dx, dA, dB = lib.linear_backward(d(x), (d(W), d(A), d(B)), s, saved, d(dy))
+    torch.cuda.synchronize()
+    assert lib.poll_status() == 0
+    v = [f64(t) for t in (x, W, A, B, dy)]
+    parity("y", y, oracle.lora_linear(v[0], v[1], v[2], v[3], s))
+    rdx, rdA, rdB = oracle.lora_linear_grad(v[0], v[1], v[2], v[3], s, v[4])
+    parity("dx", dx, rdx)
+    parity("dA", dA, rdA)
+    parity("dB", dB, rdB)
+
+
+def _mlp_inputs(cfg, seed=0, **zero):
+    ins = synth.make_mlp_inputs(cfg, seed=seed)
+    for k in zero:
+        ins[k] = torch.zeros_like(ins[k])
+    return {k: t.to(DEV) for k, t in ins.items()}, to_f64_dict(ins)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "geglu_tanh"])
+@pytest.mark.parametrize("M", [64, 1, 127, 129])
+def test_mlp_tiny(lib, act, M):
+    cfg = synth.MLP_CONFIGS["tiny"].replace(act=act, M=M)
+    t, v = _mlp_inputs(cfg)
+    y, g = mlp_gpu(lib, t, cfg)
+    f, b = mlp_oracle(v, cfg)
+    parity("y", y, f["y"])
+    for k in MLP_GRADS:
+        parity(k, g[k], b[k])
+
+
+@pytest.mark.parametrize("r", [1, 8, 64, 128])
+def test_mlp_ranks(lib, r):
+    cfg = synth.MLP_CONFIGS["tiny"].replace(M=200, h=256, i=520, r=r, alpha=2 * r)
+    t, v = _mlp_inputs(cfg, seed=r)
+    y, g = mlp_gpu(lib, t, cfg)
+    f, b = mlp_oracle(v, cfg)
+    parity("y", y, f["y"])
+    for k in MLP_GRADS:
+        parity(k, g[k], b[k])
+
+
+def test_mlp_zero_b_is_the_base_mlp(lib):
+    """B = 0: the adapters contribute nothing and every dA is exactly zero."""
+    cfg = synth.MLP_CONFIGS["tiny"].replace(M=300)
+    t, v = _mlp_inputs(cfg, B_gate=1, B_up=1, B_down=1)
+    y, g = mlp_gpu(lib, t, cfg)
+    f, b = mlp_oracle(v, cfg)
+    parity("y", y, f["y"])
+    for k in MLP_GRADS:
+        parity(k, g[k], b[k])
+    for k in ("dA_gate", "dA_up", "dA_down"):
+        assert torch.count_nonzero(g[k]).item() == 0
+
+
+def test_mlp_zero_scale_and_adapter_term(lib):
+    """s = 0 gives the base MLP; the adapter's share of y, y(s) - y(0), matches the
+    oracle's on its own (it is a fraction of |y|)."""
+    cfg = synth.MLP_CONFIGS["tiny"].replace(M=256)
+    t, v = _mlp_inputs(cfg)
+    y0, g0 = mlp_gpu(lib, t, cfg, s=0.0)
+    y1, _ = mlp_gpu(lib, t, cfg)
+    f0, b0 = mlp_oracle(v, cfg, s=0.0)
+    f1, _ = mlp_oracle(v, cfg)
+    parity("y(s=0)", y0, f0["y"])
+    for k in ("dA_gate", "dA_up", "dA_down", "dB_gate", "dB_up", "dB_down"):
+        assert torch.count_nonzero(g0[k]).item() == 0
+    delta = f64(y1) - f64(y0)
+    parity("y(s)-y(0)", torch.from_numpy(delta), f1["y"] - f0["y"], fro_tol=2e-2, max_tol=5e-2)
+
+
+def test_qkvo_small(lib):
+    cfg = synth.QKVO_CONFIGS["gqa7b"].replace(M=200, h=256, heads_q=4, heads_kv=2, head_dim=64)
+    ins = synth.make_qkvo_inputs(cfg)
+    t = {k: x.to(DEV) for k, x in ins.items()}
+    out, g = qkvo_gpu(lib, t, cfg)
+    f, b = qkvo_oracle(to_f64_dict(ins), cfg)
+    for k in ("q", "k", "v", "o"):
+        parity(k, out[k], f[k])
+    for k in b:
+        parity(k, g[k], b[k])
+
+
+def test_qkvo_halves_independent(lib):
+    """Either half can run alone (attention sits between them in a real block)."""
+    cfg = synth.QKVO_CONFIGS["gqa7b"].replace(M=130, h=256, heads_q=4, heads_kv=2, head_dim=64, r=16)
+    ins = synth.make_qkvo_inputs(cfg, seed=3)
+    t = {k: x.to(DEV) for k, x in ins.items()}
+    lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
+    f, b = qkvo_oracle(to_f64_dict(ins), cfg)
+    out, saved = lib.qkvo_forward(t["x"], lin("q"), lin("k"), lin("v"), None, None, cfg.s)
+    g = lib.qkvo_backward(t["x"], lin("q"), lin("k"), lin("v"), None, None, cfg.s, saved,
+                          t["dy_q"], t["dy_k"], t["dy_v"], None)
+    for k in ("q", "k", "v"):
+        parity(k, out[k], f[k])
+    for k in ("dx", "dA_q", "dB_q", "dA_k", "dB_k", "dA_v", "dB_v"):
+        parity(k, g[k], b[k])
+    out, saved = lib.qkvo_forward(None, None, None, None, t["o_in"], lin("o"), cfg.s)
+    g = lib.qkvo_backward(None, None, None, None, t["o_in"], lin("o"), cfg.s, saved, dyo=t["dy_o"])
+    torch.cuda.synchronize()
+    parity("o", out["o"], f["o"])
+    for k in ("do_in", "dA_o", "dB_o"):
+        parity(k, g[k], b[k])
+
+
+def test_deterministic(lib):
+    """Split-K reductions run in a fixed order: repeated calls give identical bits."""
+    cfg = synth.MLP_CONFIGS["qwen05b"].replace(M=1000)
+    t, _ = _mlp_inputs(cfg)
+    y1, g1 = mlp_gpu(lib, t, cfg)
+    y2, g2 = mlp_gpu(lib, t, cfg)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    for k in MLP_GRADS:
+        assert torch.equal(g1[k].view(torch.int16), g2[k].view(torch.int16)), k
