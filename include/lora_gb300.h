@@ -109,6 +109,25 @@ lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out, int r, fl
                                    const void* dy, void* dx, lora_grads_t grads,
                                    void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Forward of the single linear (inference: nothing is saved) that allocates nothing
+ * and takes no workspace.  The pages have no counterpart; it exists for callers that
+ * cannot allocate device memory where they run this projection -- a plugin inside a
+ * host framework that owns all device memory and passes the plugin only its input and
+ * output buffers, or a latency-critical loop that must never call cudaMalloc (which
+ * can synchronise the device).  Scratch comes from a fixed 32 MiB array inside the
+ * library, which every GPU that loads the library holds until the process exits.
+ * - Problems with lora_linear_workspace_bytes(M, in, out, r) > 32 MiB are rejected with
+ *   LORA_ERR_WORKSPACE before anything is enqueued; other argument rules and results
+ *   are those of lora_linear_forward with saved == NULL.
+ * - The first call on a device looks up the array's device address (a one-time set-up
+ *   per device); make that first call before any stream capture.
+ * - Every call on a device shares the one array and leaves its contents behind; calls
+ *   whose GPU work overlaps (other streams, other threads) race and corrupt each
+ *   other's results.  Calls in order on one stream are safe. */
+lora_status_t lora_linear_forward_noalloc(int64_t M, int64_t in, int64_t out, int r, float s,
+                                          const void* x, lora_linear_t lin, void* y,
+                                          cudaStream_t stream);
+
 /* ---------------------------------------------------------------- gated MLP
  * x [M x h] -> y [M x h] through gate/up [i x h] and down [h x i] ("opake_lora_mlp").
  * saved (NULL for inference) receives g, u, h and the rank-r projections for

@@ -51,6 +51,7 @@ _SIGS = {
     "lora_linear_forward": (_INT, [_I64, _I64, _I64, _INT, _F32, _VP, LoraLinear, _VP, _VP, _VP, _SZ, _VP]),
     "lora_linear_backward": (_INT, [_I64, _I64, _I64, _INT, _F32, _VP, LoraLinear, _VP, _VP, _VP, LoraGrads,
                                     _VP, _SZ, _VP]),
+    "lora_linear_forward_noalloc": (_INT, [_I64, _I64, _I64, _INT, _F32, _VP, LoraLinear, _VP, _VP]),
     "lora_mlp_saved_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
     "lora_mlp_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
     "lora_mlp_forward": (_INT, [_I64, _I64, _I64, _INT, _F32, _INT, _VP, LoraLinear, LoraLinear, LoraLinear,
@@ -178,6 +179,20 @@ def linear_forward(x, lin, s, *, y=None, saved=None, training=True, ws=None):
                                    None if saved is None else saved.data_ptr(), ws.data_ptr(), ws.numel(),
                                    _stream(x.device)), "lora_linear_forward")
     return y, saved
+
+
+def linear_forward_noalloc(x, lin, s, *, y=None):
+    """Inference forward through lora_linear_forward_noalloc: the library allocates
+    nothing and the caller passes no workspace (the library's fixed scratch is used)."""
+    lib = load()
+    W, A, B = lin
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty(M, W.shape[0], dtype=torch.bfloat16, device=x.device)
+    _check(lib.lora_linear_forward_noalloc(M, x.shape[1], W.shape[0], A.shape[0], s, _dev(x, "x"),
+                                           _lin(lin, "lin"), _dev(y, "y"), _stream(x.device)),
+           "lora_linear_forward_noalloc")
+    return y
 
 
 def linear_backward(x, lin, s, saved, dy, *, dx=None, dA=None, dB=None, ws=None):
