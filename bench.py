@@ -181,14 +181,22 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def kernel_source_sha() -> str:
+    """sha256[:16] over the GEMM kernels' sources (ptx.cuh, gemm_tc.cuh, gemm_pair.cuh)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("ptx.cuh", "gemm_tc.cuh", "gemm_pair.cuh"):
+        with open(os.path.join(ROOT, "rank_mlp_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def ncu_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from profiles/traffic.md, if that capture
     was taken on the current kernel source; else None."""
-    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.md")
-    src = os.path.join(ROOT, "rank_mlp_gb300", "csrc", "gemm_tc.cuh")
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        sha = kernel_source_sha()
         for line in open(path):
             cells = [c.strip() for c in line.strip().strip("|").split("|")]
             if len(cells) >= 4 and cells[0] == kernel and cells[2] == sha:

@@ -1,0 +1,219 @@
+// The projection GEMM on a CTA pair (cluster of 2, tcgen05 cta_group::2): one
+// 256 x 256 output tile per pair and step.  Each CTA loads its own 128 rows of A and
+// one half (128 rows) of the B tile; the even CTA issues 256 x 256 x 16 MMAs that read
+// A from both CTAs and B from both halves, so each SM's shared memory moves half of B
+// instead of all of it.  Each CTA's TMEM holds its 128 accumulator rows (two
+// 256-column buffers) and its own epilogue warps drain them.
+//
+// Barriers: the even CTA's `full` barrier counts the bytes of both CTAs' copies (it
+// alone arms it); the MMA's commits arrive on `empty` and `tfull` of both CTAs
+// (multicast); both CTAs' epilogue warps arrive on the even CTA's `tempty`.
+// Gate/up tiles put the gate rows in the even CTA's half and the matching up rows in
+// the odd CTA's half, so accumulator columns 0-127 are g and 128-255 are u.
+#pragma once
+
+#include "gemm_tc.cuh"
+
+namespace lgb {
+
+template <int STAGES>
+struct PairCfg {
+  static constexpr int BN = 256;                       // accumulator columns per tile
+  static constexpr int kBLocal = BN / 2;               // B rows held by each CTA
+  static constexpr int kABytes = kBM * kBK * 2;        // this CTA's 128 rows of A
+  static constexpr int kBBytes = kBLocal * kBK * 2;    // this CTA's half of B
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTxBytes = 2 * kStageBytes;     // both CTAs, counted on the even CTA
+  static constexpr int kTmemCols = 512;
+  static constexpr int kBarBytes = 8 * (2 * STAGES + 5) + 16;
+  static constexpr int kSmemBytes = STAGES * kStageBytes + kBarBytes + 1024;
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+};
+
+template <int STAGES, bool B_MN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
+  using C = PairCfg<STAGES>;
+  constexpr int BN = C::BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int npairs = static_cast<int>(gridDim.x >> 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 8);        // 4 epilogue warps x 2 CTAs (used on the even CTA)
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane < p.nmaps) tma_prefetch_map(&p.maps[lane]);
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync_all();                     // both CTAs' barriers exist before any remote arrive
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int armed[STAGES];
+      for (int s = 0; s < STAGES; ++s) armed[s] = -1;
+      bool ok = true;
+      for (int u = pair; u < p.total_units && ok; u += npairs) {
+        const Unit U = decode_unit(p, u);
+        const GroupDesc& G = p.grp[U.g];
+        int seg = 0, seg_base = 0;
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
+          while (kb >= seg_base + G.seg[seg].kblocks) {
+            seg_base += G.seg[seg].kblocks;
+            ++seg;
+          }
+          const SegDesc& S = G.seg[seg];
+          const int kc = (kb - seg_base) * kBK;
+          if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) { ok = false; break; }
+          const uint32_t fb = full_bar(stage);
+          if (leader) {
+            mbar_arrive_expect_tx(fb, C::kTxBytes);
+            armed[stage] = static_cast<int>(phase);
+          }
+          const uint32_t fb_even = mapa_shared(fb, 0);
+          const uint32_t sa = sbase + stage * C::kStageBytes;
+          const uint32_t sb = sa + C::kABytes;
+          tma_load_2d_pair(sa, &p.maps[S.a], fb_even, kc, U.tm * (2 * kBM) + static_cast<int>(rank) * kBM);
+          if (!B_MN) {
+            if (S.b1 >= 0) {
+              tma_load_2d_pair(sb, &p.maps[rank ? S.b1 : S.b0], fb_even, kc, U.tn * C::kBLocal);
+            } else {
+              tma_load_2d_pair(sb, &p.maps[S.b0], fb_even, kc, U.tn * BN + static_cast<int>(rank) * C::kBLocal);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < C::kBLocal / 64; ++c)
+              tma_load_2d_pair(sb + c * 8192u, &p.maps[S.b0], fb_even,
+                               U.tn * BN + static_cast<int>(rank) * C::kBLocal + c * 64, kc);
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok && leader) {
+        for (int s = 0; s < STAGES; ++s)
+          if (armed[s] >= 0) wait_phase_drain(full_bar(s), static_cast<uint32_t>(armed[s]), p);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, BN, 0, B_MN ? 1 : 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = pair; u < p.total_units && ok; u += npairs) {
+        const Unit U = decode_unit(p, u);
+        const GroupDesc& G = p.grp[U.g];
+        if (!wait_phase(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        uint32_t accumulate = 0;
+        int seg = 0, seg_base = 0;
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
+          while (kb >= seg_base + G.seg[seg].kblocks) {
+            seg_base += G.seg[seg].kblocks;
+            ++seg;
+          }
+          const int kc = (kb - seg_base) * kBK;
+          const int kvalid = G.seg[seg].kvalid;
+          if (!wait_phase(full_bar(stage), phase, abort_flag, p)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t sa = sbase + stage * C::kStageBytes;
+          const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            if (kc + 16 * k < kvalid) {
+              const uint64_t adesc = smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+              const uint64_t bdesc = B_MN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
+                                          : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
+              tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
+              accumulate = 1;
+            }
+          }
+          tc_commit_pair_multicast(empty_bar(stage), 0x3);   // frees this stage in both CTAs
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast(tfull_bar(acc), 0x3);       // both halves of the tile ready
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok) {
+        tc_commit_pair_multicast(drain_bar, 0x1);
+        wait_phase_drain(drain_bar, 0, p);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t tempty_even[2] = {mapa_shared(tempty_bar(0), 0), mapa_shared(tempty_bar(1), 0)};
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = pair; u < p.total_units; u += npairs) {
+      const Unit U = decode_unit(p, u);
+      const GroupDesc& G = p.grp[U.g];
+      const bool ready = wait_phase(tfull_bar(acc), acc_phase, abort_flag, p);
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after_sync();
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      epilogue_tile<BN>(p, G, U, tacc, U.tm * (2 * kBM) + static_cast<int>(rank) * kBM + row_in_tile);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_even[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  if (*abort_flag) {
+    // after an abort, give copies still in flight time to land before shared memory goes
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+  }
+  __syncwarp();
+  tc_fence_before_sync();
+  cluster_sync_all();                     // no remote arrive or MMA read of either CTA is pending
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace lgb

@@ -1,5 +1,6 @@
 // 128 x 64 / 128 x 128 tiles: the rank-r products (token-major projections such as
 // x A^T, and the reductions over tokens that give dA and dB).  HBM-bound; deep rings.
+#include "gemm_pair.cuh"
 #include "host.cuh"
 
 namespace lgb {
@@ -30,8 +31,8 @@ cudaError_t launch_tc_skinny(int variant, const TcParams& p, int grid, cudaStrea
 
 int tc_smem_bytes(int variant) {
   switch (variant) {
-    case V256_KK:
-    case V256_KMN: return TcCfg<256, 4>::kSmemBytes;
+    case VP_KK:
+    case VP_KMN: return PairCfg<6>::kSmemBytes;
     case V64_KK:
     case V64_MNMN: return TcCfg<64, 8>::kSmemBytes;
     default: return TcCfg<128, 6>::kSmemBytes;

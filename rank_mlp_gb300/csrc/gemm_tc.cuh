@@ -168,6 +168,150 @@ __device__ __forceinline__ void act_fwd_bwd(float g, int act, float& a, float& a
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Epilogue of one accumulator tile.  The calling thread owns output row `row` and
+// reads its TMEM lane at `tacc` (columns = the tile's N).  Warp-collective: every
+// lane of the warp calls it (tcgen05.ld), rows past M are computed and dropped.
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc& G, const Unit& U,
+                                              uint32_t tacc, int row) {
+  const bool row_ok = row < G.M;
+  if (G.epi == EPI_STORE) {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(G.out0);
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t v[32];
+      __syncwarp();
+      tmem_ld32(tacc + c, v);
+      tmem_ld_wait();
+      const int col0 = U.tn * BN + c;
+      if (row_ok) {
+        __nv_bfloat16* dst = out + static_cast<long long>(row) * G.ldo + col0;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          if (col0 + j + 8 <= G.N) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[j + 0]), __uint_as_float(v[j + 1]));
+            w.y = pack_bf16x2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+            w.z = pack_bf16x2(__uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]));
+            w.w = pack_bf16x2(__uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]));
+            *reinterpret_cast<uint4*>(dst + j) = w;
+          }
+        }
+      }
+    }
+  } else if (G.epi == EPI_ACT_FWD) {
+    // gate in accumulator columns [0, BN/2), up in [BN/2, BN)
+    __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(G.out0);
+    __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(G.out1);
+    __nv_bfloat16* uout = static_cast<__nv_bfloat16*>(G.out2);
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 32) {
+      uint32_t vg[32], vu[32];
+      __syncwarp();
+      tmem_ld32(tacc + c, vg);
+      tmem_ld32(tacc + BN / 2 + c, vu);
+      tmem_ld_wait();
+      const int col0 = U.tn * (BN / 2) + c;
+      if (row_ok) {
+        const long long off = static_cast<long long>(row) * G.ldo + col0;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          if (col0 + j + 8 <= G.N) {
+            float hv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              hv[e] = act_fwd(__uint_as_float(vg[j + e]), p.act) * __uint_as_float(vu[j + e]);
+            uint4 w;
+            w.x = pack_bf16x2(hv[0], hv[1]);
+            w.y = pack_bf16x2(hv[2], hv[3]);
+            w.z = pack_bf16x2(hv[4], hv[5]);
+            w.w = pack_bf16x2(hv[6], hv[7]);
+            *reinterpret_cast<uint4*>(hout + off + j) = w;
+            if (gout != nullptr) {
+              uint4 wg, wu;
+              wg.x = pack_bf16x2(__uint_as_float(vg[j + 0]), __uint_as_float(vg[j + 1]));
+              wg.y = pack_bf16x2(__uint_as_float(vg[j + 2]), __uint_as_float(vg[j + 3]));
+              wg.z = pack_bf16x2(__uint_as_float(vg[j + 4]), __uint_as_float(vg[j + 5]));
+              wg.w = pack_bf16x2(__uint_as_float(vg[j + 6]), __uint_as_float(vg[j + 7]));
+              wu.x = pack_bf16x2(__uint_as_float(vu[j + 0]), __uint_as_float(vu[j + 1]));
+              wu.y = pack_bf16x2(__uint_as_float(vu[j + 2]), __uint_as_float(vu[j + 3]));
+              wu.z = pack_bf16x2(__uint_as_float(vu[j + 4]), __uint_as_float(vu[j + 5]));
+              wu.w = pack_bf16x2(__uint_as_float(vu[j + 6]), __uint_as_float(vu[j + 7]));
+              *reinterpret_cast<uint4*>(gout + off + j) = wg;
+              *reinterpret_cast<uint4*>(uout + off + j) = wu;
+            }
+          }
+        }
+      }
+    }
+  } else if (G.epi == EPI_ACT_BWD) {
+    // accumulator = dh; saved g, u give dg = dh * u * act'(g), du = dh * act(g)
+    const __nv_bfloat16* gin = static_cast<const __nv_bfloat16*>(G.in0);
+    const __nv_bfloat16* uin = static_cast<const __nv_bfloat16*>(G.in1);
+    __nv_bfloat16* dgo = static_cast<__nv_bfloat16*>(G.out0);
+    __nv_bfloat16* duo = static_cast<__nv_bfloat16*>(G.out1);
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      const int col0 = U.tn * BN + c;
+      uint4 gw[4], uw[4];
+      const long long ioff = static_cast<long long>(row) * G.ldi + col0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (row_ok && col0 + 8 * j + 8 <= G.N) {
+          gw[j] = __ldg(reinterpret_cast<const uint4*>(gin + ioff + 8 * j));
+          uw[j] = __ldg(reinterpret_cast<const uint4*>(uin + ioff + 8 * j));
+        } else {
+          gw[j] = make_uint4(0, 0, 0, 0);
+          uw[j] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      uint32_t v[32];
+      __syncwarp();
+      tmem_ld32(tacc + c, v);
+      tmem_ld_wait();
+      if (row_ok) {
+        const long long ooff = static_cast<long long>(row) * G.ldo + col0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (col0 + 8 * j + 8 <= G.N) {
+            const uint32_t gg[4] = {gw[j].x, gw[j].y, gw[j].z, gw[j].w};
+            const uint32_t uu[4] = {uw[j].x, uw[j].y, uw[j].z, uw[j].w};
+            uint32_t og[4], ou[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float a0, ap0, a1, ap1;
+              const float g0 = bf16_lo(gg[e]), g1 = bf16_hi(gg[e]);
+              const float u0 = bf16_lo(uu[e]), u1 = bf16_hi(uu[e]);
+              act_fwd_bwd(g0, p.act, a0, ap0);
+              act_fwd_bwd(g1, p.act, a1, ap1);
+              const float d0 = __uint_as_float(v[8 * j + 2 * e]);
+              const float d1 = __uint_as_float(v[8 * j + 2 * e + 1]);
+              og[e] = pack_bf16x2(d0 * u0 * ap0, d1 * u1 * ap1);
+              ou[e] = pack_bf16x2(d0 * a0, d1 * a1);
+            }
+            *reinterpret_cast<uint4*>(dgo + ooff + 8 * j) = make_uint4(og[0], og[1], og[2], og[3]);
+            *reinterpret_cast<uint4*>(duo + ooff + 8 * j) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+          }
+        }
+      }
+    }
+  } else {
+    // EPI_PARTIAL: f32 tile into the split's slab (rows and columns padded)
+    const long long width = static_cast<long long>(G.tiles_n) * BN;
+    float* dst = G.part + (static_cast<long long>(U.split) * G.tiles_m * kBM + row) * width + U.tn * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t v[32];
+      __syncwarp();
+      tmem_ld32(tacc + c, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<uint4*>(dst + c + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    }
+  }
+}
+
 template <int BN, int STAGES, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<BN, STAGES>;
@@ -329,144 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after_sync();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      const int row = U.tm * kBM + row_in_tile;
-      const bool row_ok = row < G.M;
-
-      if (G.epi == EPI_STORE) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(G.out0);
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          __syncwarp();
-          tmem_ld32(tacc + c, v);
-          tmem_ld_wait();
-          const int col0 = U.tn * BN + c;
-          if (row_ok) {
-            __nv_bfloat16* dst = out + static_cast<long long>(row) * G.ldo + col0;
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              if (col0 + j + 8 <= G.N) {
-                uint4 w;
-                w.x = pack_bf16x2(__uint_as_float(v[j + 0]), __uint_as_float(v[j + 1]));
-                w.y = pack_bf16x2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-                w.z = pack_bf16x2(__uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]));
-                w.w = pack_bf16x2(__uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]));
-                *reinterpret_cast<uint4*>(dst + j) = w;
-              }
-            }
-          }
-        }
-      } else if (G.epi == EPI_ACT_FWD) {
-        // gate in accumulator columns [0, BN/2), up in [BN/2, BN)
-        __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(G.out0);
-        __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(G.out1);
-        __nv_bfloat16* uout = static_cast<__nv_bfloat16*>(G.out2);
-#pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
-          uint32_t vg[32], vu[32];
-          __syncwarp();
-          tmem_ld32(tacc + c, vg);
-          tmem_ld32(tacc + BN / 2 + c, vu);
-          tmem_ld_wait();
-          const int col0 = U.tn * (BN / 2) + c;
-          if (row_ok) {
-            const long long off = static_cast<long long>(row) * G.ldo + col0;
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              if (col0 + j + 8 <= G.N) {
-                float hv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  hv[e] = act_fwd(__uint_as_float(vg[j + e]), p.act) * __uint_as_float(vu[j + e]);
-                uint4 w;
-                w.x = pack_bf16x2(hv[0], hv[1]);
-                w.y = pack_bf16x2(hv[2], hv[3]);
-                w.z = pack_bf16x2(hv[4], hv[5]);
-                w.w = pack_bf16x2(hv[6], hv[7]);
-                *reinterpret_cast<uint4*>(hout + off + j) = w;
-                if (gout != nullptr) {
-                  uint4 wg, wu;
-                  wg.x = pack_bf16x2(__uint_as_float(vg[j + 0]), __uint_as_float(vg[j + 1]));
-                  wg.y = pack_bf16x2(__uint_as_float(vg[j + 2]), __uint_as_float(vg[j + 3]));
-                  wg.z = pack_bf16x2(__uint_as_float(vg[j + 4]), __uint_as_float(vg[j + 5]));
-                  wg.w = pack_bf16x2(__uint_as_float(vg[j + 6]), __uint_as_float(vg[j + 7]));
-                  wu.x = pack_bf16x2(__uint_as_float(vu[j + 0]), __uint_as_float(vu[j + 1]));
-                  wu.y = pack_bf16x2(__uint_as_float(vu[j + 2]), __uint_as_float(vu[j + 3]));
-                  wu.z = pack_bf16x2(__uint_as_float(vu[j + 4]), __uint_as_float(vu[j + 5]));
-                  wu.w = pack_bf16x2(__uint_as_float(vu[j + 6]), __uint_as_float(vu[j + 7]));
-                  *reinterpret_cast<uint4*>(gout + off + j) = wg;
-                  *reinterpret_cast<uint4*>(uout + off + j) = wu;
-                }
-              }
-            }
-          }
-        }
-      } else if (G.epi == EPI_ACT_BWD) {
-        // accumulator = dh; saved g, u give dg = dh * u * act'(g), du = dh * act(g)
-        const __nv_bfloat16* gin = static_cast<const __nv_bfloat16*>(G.in0);
-        const __nv_bfloat16* uin = static_cast<const __nv_bfloat16*>(G.in1);
-        __nv_bfloat16* dgo = static_cast<__nv_bfloat16*>(G.out0);
-        __nv_bfloat16* duo = static_cast<__nv_bfloat16*>(G.out1);
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          const int col0 = U.tn * BN + c;
-          uint4 gw[4], uw[4];
-          const long long ioff = static_cast<long long>(row) * G.ldi + col0;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (row_ok && col0 + 8 * j + 8 <= G.N) {
-              gw[j] = __ldg(reinterpret_cast<const uint4*>(gin + ioff + 8 * j));
-              uw[j] = __ldg(reinterpret_cast<const uint4*>(uin + ioff + 8 * j));
-            } else {
-              gw[j] = make_uint4(0, 0, 0, 0);
-              uw[j] = make_uint4(0, 0, 0, 0);
-            }
-          }
-          uint32_t v[32];
-          __syncwarp();
-          tmem_ld32(tacc + c, v);
-          tmem_ld_wait();
-          if (row_ok) {
-            const long long ooff = static_cast<long long>(row) * G.ldo + col0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (col0 + 8 * j + 8 <= G.N) {
-                const uint32_t gg[4] = {gw[j].x, gw[j].y, gw[j].z, gw[j].w};
-                const uint32_t uu[4] = {uw[j].x, uw[j].y, uw[j].z, uw[j].w};
-                uint32_t og[4], ou[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  float a0, ap0, a1, ap1;
-                  const float g0 = bf16_lo(gg[e]), g1 = bf16_hi(gg[e]);
-                  const float u0 = bf16_lo(uu[e]), u1 = bf16_hi(uu[e]);
-                  act_fwd_bwd(g0, p.act, a0, ap0);
-                  act_fwd_bwd(g1, p.act, a1, ap1);
-                  const float d0 = __uint_as_float(v[8 * j + 2 * e]);
-                  const float d1 = __uint_as_float(v[8 * j + 2 * e + 1]);
-                  og[e] = pack_bf16x2(d0 * u0 * ap0, d1 * u1 * ap1);
-                  ou[e] = pack_bf16x2(d0 * a0, d1 * a1);
-                }
-                *reinterpret_cast<uint4*>(dgo + ooff + 8 * j) = make_uint4(og[0], og[1], og[2], og[3]);
-                *reinterpret_cast<uint4*>(duo + ooff + 8 * j) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
-              }
-            }
-          }
-        }
-      } else {
-        // EPI_PARTIAL: f32 tile into the split's slab (rows and columns padded)
-        const long long width = static_cast<long long>(G.tiles_n) * BN;
-        float* dst = G.part + (static_cast<long long>(U.split) * G.tiles_m * kBM + row) * width + U.tn * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          __syncwarp();
-          tmem_ld32(tacc + c, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<uint4*>(dst + c + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-        }
-      }
+      epilogue_tile<BN>(p, G, U, tacc, U.tm * kBM + row_in_tile);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));

@@ -10,7 +10,7 @@
 #include <cstdint>
 #include <cstring>
 
-#include "../../include/lora_gb300.h"
+#include "lora_gb300.h"
 #include "aux_kernels.cuh"
 #include "gemm_tc.cuh"
 
@@ -18,8 +18,8 @@ namespace lgb {
 
 // Kernel variants (tile width BN, operand majors) compiled into the library.
 enum Variant : int {
-  V256_KK = 0,     // big GEMMs, K-major A and B: forward projections
-  V256_KMN = 1,    // big GEMMs, B MN-major: dh and input gradients (W used untransposed)
+  VP_KK = 0,       // projections on a CTA pair, 256 x 256 tiles, K-major B (forward)
+  VP_KMN = 1,      // projections on a CTA pair, MN-major B (backward: W read untransposed)
   V64_KK = 2,      // token-major rank-r projections, padded rank <= 64
   V64_MNMN = 3,    // reductions over tokens (dA, dB), padded rank <= 64
   V128_KK = 4,
@@ -27,9 +27,14 @@ enum Variant : int {
   kNumVariants = 6
 };
 
-constexpr int variant_bn(int v) { return (v <= V256_KMN) ? 256 : (v <= V64_MNMN ? 64 : 128); }
+constexpr bool variant_pair(int v) { return v == VP_KK || v == VP_KMN; }
+constexpr int variant_bn(int v) { return variant_pair(v) ? 256 : (v <= V64_MNMN ? 64 : 128); }
 constexpr bool variant_a_mn(int v) { return v == V64_MNMN || v == V128_MNMN; }
-constexpr bool variant_b_mn(int v) { return v == V256_KMN || v == V64_MNMN || v == V128_MNMN; }
+constexpr bool variant_b_mn(int v) { return v == VP_KMN || v == V64_MNMN || v == V128_MNMN; }
+
+// The big projection GEMMs run on CTA pairs (256 x 256 tiles).
+constexpr int kBigKK = VP_KK;
+constexpr int kBigKMN = VP_KMN;
 
 // Defined in gemm_big.cu / gemm_skinny.cu.
 cudaError_t launch_tc_big(int variant, const TcParams& p, int grid, cudaStream_t st);
@@ -44,7 +49,7 @@ lora_status_t launch_gemm(int variant, const TcParams& p, int kind, cudaStream_t
 lora_status_t launch_pack(const PackParams& p, cudaStream_t st);
 lora_status_t launch_reduce(const RedParams& p, cudaStream_t st);
 
-constexpr int kTargetUnits = 304;     // work units aimed at for split-K (2 per SM)
+constexpr int kMaxSplits = 16;        // split-K factors of the rank-r products
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -56,14 +61,30 @@ inline int skinny_bn(int kf) { return kf <= 64 ? 64 : 128; }
 inline int skinny_kk(int kf) { return kf <= 64 ? V64_KK : V128_KK; }
 inline int skinny_mnmn(int kf) { return kf <= 64 ? V64_MNMN : V128_MNMN; }
 
-inline int choose_splits(int64_t tiles, int64_t kb_total) {
-  if (tiles <= 0 || kb_total <= 0) return 1;
-  int64_t s = ceil_div(kTargetUnits, tiles);
-  s = s < 1 ? 1 : s;
-  if (s > 8) s = 8;
-  const int64_t maxs = kb_total / 4 > 0 ? kb_total / 4 : 1;
-  if (s > maxs) s = maxs;
+// Largest split-K factor for a K of kb_total k-blocks (at least 4 k-blocks per split);
+// workspaces are sized for it, so they do not depend on the device.
+inline int max_splits(int64_t kb_total) {
+  int64_t s = kb_total / 4;
+  s = s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
   return static_cast<int>(s);
+}
+
+// Split-K factor for `tiles` output tiles on `sms` SMs: the one (<= max_splits) that
+// minimises waves per split, ceil(tiles * s / sms) / s, i.e. the busy time of the
+// slowest SM; ties go to fewer splits (less partial traffic).
+inline int choose_splits(int64_t tiles, int64_t kb_total, int sms) {
+  if (tiles <= 0 || kb_total <= 0 || sms <= 0) return 1;
+  const int smax = max_splits(kb_total);
+  int best = 1;
+  double best_cost = 1e30;
+  for (int s = 1; s <= smax; ++s) {
+    const double cost = static_cast<double>(ceil_div(tiles * s, sms)) / s;
+    if (cost < best_cost * (1.0 - 1e-9)) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
 }
 
 // Bump allocator over a caller-provided buffer (256-byte aligned regions).  Used
@@ -96,9 +117,10 @@ struct GemmPlan {
   TcParams p;
   int variant;
   int bn;
+  bool pair;
   bool ok = true;
 
-  explicit GemmPlan(int v) : variant(v), bn(variant_bn(v)) {
+  explicit GemmPlan(int v) : variant(v), bn(variant_bn(v)), pair(variant_pair(v)) {
     std::memset(static_cast<void*>(&p), 0, sizeof(p));
     p.band = 8;
     p.timeout_ns = kTimeoutNs;
@@ -117,7 +139,9 @@ struct GemmPlan {
   int a_mnmajor(const void* base, int64_t rows, int64_t K, int64_t ld) {
     return add_map(base, rows, K, ld, 64, 64);
   }
-  // B operand, K-major: [N x K]; box_rows = BN, or BN/2 for a split (gate/up) tile.
+  // Rows of a whole (not split) K-major B tile held by one CTA.
+  int b_rows_full() const { return pair ? bn / 2 : bn; }
+  // B operand, K-major: [N x K]; box_rows = b_rows_full(), or BN/2 for a split (gate/up) tile.
   int b_kmajor(const void* base, int64_t N, int64_t K, int64_t ld, int box_rows) {
     return add_map(base, K, N, ld, 64, box_rows);
   }
@@ -131,7 +155,7 @@ struct GemmPlan {
     G.M = M;
     G.N = N;
     G.epi = epi;
-    G.tiles_m = static_cast<int>(ceil_div(M, kBM));
+    G.tiles_m = static_cast<int>(ceil_div(M, pair ? 2 * kBM : kBM));
     G.tiles_n = static_cast<int>(ceil_div(N, split_n_tile ? bn / 2 : bn));
     G.splits = 1;
     return G;

@@ -80,10 +80,15 @@ static void trace_end(int slot, cudaStream_t st) {
 
 lora_status_t launch_gemm(int variant, const TcParams& p, int kind, cudaStream_t st) {
   if (p.total_units <= 0) return LORA_OK;
-  const int grid = p.total_units < num_sms() ? p.total_units : num_sms();
+  int grid;
+  if (variant_pair(variant)) {
+    const int pairs = num_sms() / 2;
+    grid = 2 * (p.total_units < pairs ? p.total_units : pairs);
+  } else {
+    grid = p.total_units < num_sms() ? p.total_units : num_sms();
+  }
   const int slot = trace_begin(kind, st);
-  cudaError_t e = (variant <= V256_KMN) ? launch_tc_big(variant, p, grid, st)
-                                        : launch_tc_skinny(variant, p, grid, st);
+  cudaError_t e = variant_pair(variant) ? launch_tc_big(variant, p, grid, st) : launch_tc_skinny(variant, p, grid, st);
   trace_end(slot, st);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -174,7 +179,7 @@ static lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int
   int64_t kb = 0;
   for (int s = 0; s < nseg; ++s) kb += ceil_div(segs[s].K, kBK);
   const int64_t tiles = ceil_div(M, kBM) * ceil_div(kf, g.bn);
-  const int splits = choose_splits(tiles, kb);
+  const int splits = choose_splits(tiles, kb, num_sms());
   GroupDesc& G = g.group(static_cast<int>(M), kf, splits > 1 ? EPI_PARTIAL : EPI_STORE, false);
   G.splits = splits;
   for (int s = 0; s < nseg; ++s) {
@@ -213,9 +218,8 @@ static lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int
   return LORA_OK;
 }
 static int64_t rank_projection_part(int64_t M, int kf, int64_t ktotal_blocks) {
-  const int bn = skinny_bn(kf);
-  const int splits = choose_splits(ceil_div(M, kBM) * ceil_div(kf, bn), ktotal_blocks);
-  return splits > 1 ? partial_elems(M, kf, bn, splits) : 0;
+  const int splits = max_splits(ktotal_blocks);
+  return splits > 1 ? partial_elems(M, kf, skinny_bn(kf), splits) : 0;
 }
 
 // Reductions over tokens: for each job j, D_j[f x kf] = Q_j[tokens x f]^T * T[tokens x kf],
@@ -230,10 +234,7 @@ struct GradJob {
 static int64_t token_grad_part(int64_t M, int kf, const int64_t* fs, int n) {
   const int bn = skinny_bn(kf);
   int64_t tot = 0;
-  for (int j = 0; j < n; ++j) {
-    const int splits = choose_splits(ceil_div(fs[j], kBM) * ceil_div(kf, bn), ceil_div(M, kBK));
-    tot += round_up(partial_elems(fs[j], kf, bn, splits), 64);
-  }
+  for (int j = 0; j < n; ++j) tot += round_up(partial_elems(fs[j], kf, bn, max_splits(ceil_div(M, kBK))), 64);
   return tot;
 }
 // Jobs with the same Q share one slab (several rank slots out of one product).
@@ -254,14 +255,14 @@ static lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* 
       gi = nq++;
       qs[gi] = jobs[j].Q;
       const int64_t tiles = ceil_div(jobs[j].f, kBM) * ceil_div(kf, g.bn);
-      const int splits = choose_splits(tiles, ceil_div(M, kBK));
+      const int splits = choose_splits(tiles, ceil_div(M, kBK), num_sms());
       GroupDesc& G = g.group(static_cast<int>(jobs[j].f), kf, EPI_PARTIAL, false);
       G.splits = splits;
       const int a = g.a_mnmajor(jobs[j].Q, jobs[j].f, M, jobs[j].f);
       GemmPlan::seg(G, a, tmap, -1, M, M);
       G.part = cur;
       parts[gi] = cur;
-      cur += round_up(partial_elems(jobs[j].f, kf, g.bn, splits), 64);
+      cur += round_up(partial_elems(jobs[j].f, kf, g.bn, max_splits(ceil_div(M, kBK))), 64);
     }
     group_of[j] = gi;
   }
@@ -403,16 +404,16 @@ extern "C" lora_status_t lora_linear_forward(int64_t M, int64_t in, int64_t out,
   const ProjSeg ps = {x, acat, in};
   LGB_TRY(rank_projection(M, kf, &ps, 1, T, part, status, stream));
 
-  GemmPlan g(V256_KK);
+  GemmPlan g(kBigKK);
   GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(out), EPI_STORE, false);
-  GemmPlan::seg(G, g.a_kmajor(x, M, in, in), g.b_kmajor(lin.W, out, in, in, 256), -1, in, in);
-  GemmPlan::seg(G, g.a_kmajor(T, M, kf, kf), g.b_kmajor(bf, out, kf, kf, 256), -1, kf, r);
+  GemmPlan::seg(G, g.a_kmajor(x, M, in, in), g.b_kmajor(lin.W, out, in, in, g.b_rows_full()), -1, in, in);
+  GemmPlan::seg(G, g.a_kmajor(T, M, kf, kf), g.b_kmajor(bf, out, kf, kf, g.b_rows_full()), -1, kf, r);
   G.out0 = y;
   G.ldo = out;
   g.p.status = status;
   g.finish();
   if (!g.ok) return LORA_ERR_CUDA;
-  return launch_gemm(V256_KK, g.p, LORA_KIND_PROJ, stream);
+  return launch_gemm(kBigKK, g.p, LORA_KIND_PROJ, stream);
 }
 
 extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out, int r, float s, const void* x,
@@ -460,7 +461,7 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   const GradJob jb = {dy, out, 0, grads.dB, 0};
   LGB_TRY(token_grads(M, r, kf, s, T, &jb, 1, part, status, stream));
 
-  GemmPlan g(V256_KMN);
+  GemmPlan g(kBigKMN);
   GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(in), EPI_STORE, false);
   GemmPlan::seg(G, g.a_kmajor(dy, M, out, out), g.b_mnmajor(lin.W, in, out, in), -1, out, out);
   GemmPlan::seg(G, g.a_kmajor(U, M, kf, kf), g.b_mnmajor(af, in, kf, in), -1, kf, r);
@@ -469,7 +470,7 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   g.p.status = status;
   g.finish();
   if (!g.ok) return LORA_ERR_CUDA;
-  LGB_TRY(launch_gemm(V256_KMN, g.p, LORA_KIND_DGRAD, stream));
+  LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
 
   const GradJob ja = {x, in, 0, grads.dA, 1};
   return token_grads(M, r, kf, s, U, &ja, 1, part, status, stream);
@@ -624,7 +625,7 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
 
   // [g | u] = [x | T_gu] [W_g | s B_g ; W_u | s B_u]^T, gate and up halves per tile; h = act(g) u
   {
-    GemmPlan g(V256_KK);
+    GemmPlan g(kBigKK);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(i), EPI_ACT_FWD, true);
     GemmPlan::seg(G, g.a_kmajor(x, M, h, h), g.b_kmajor(gate.W, i, h, h, 128), g.b_kmajor(up.W, i, h, h, 128), h,
                   h);
@@ -638,7 +639,7 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
     g.p.status = status;
     g.finish();
     if (!g.ok) return LORA_ERR_CUDA;
-    LGB_TRY(launch_gemm(V256_KK, g.p, LORA_KIND_GATE_UP, stream));
+    LGB_TRY(launch_gemm(kBigKK, g.p, LORA_KIND_GATE_UP, stream));
   }
 
   // T_d = h A_d^T
@@ -646,16 +647,16 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
   LGB_TRY(rank_projection(M, kfd, &p2, 1, td, part, status, stream));
 
   // y = [h | T_d] [W_d | s B_d]^T
-  GemmPlan g(V256_KK);
+  GemmPlan g(kBigKK);
   GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(h), EPI_STORE, false);
-  GemmPlan::seg(G, g.a_kmajor(hbuf, M, i, i), g.b_kmajor(down.W, h, i, i, 256), -1, i, i);
-  GemmPlan::seg(G, g.a_kmajor(td, M, kfd, kfd), g.b_kmajor(bf_d, h, kfd, kfd, 256), -1, kfd, r);
+  GemmPlan::seg(G, g.a_kmajor(hbuf, M, i, i), g.b_kmajor(down.W, h, i, i, g.b_rows_full()), -1, i, i);
+  GemmPlan::seg(G, g.a_kmajor(td, M, kfd, kfd), g.b_kmajor(bf_d, h, kfd, kfd, g.b_rows_full()), -1, kfd, r);
   G.out0 = y;
   G.ldo = h;
   g.p.status = status;
   g.finish();
   if (!g.ok) return LORA_ERR_CUDA;
-  return launch_gemm(V256_KK, g.p, LORA_KIND_PROJ, stream);
+  return launch_gemm(kBigKK, g.p, LORA_KIND_PROJ, stream);
 }
 
 extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int r, float s, lora_act_t act,
@@ -724,7 +725,7 @@ extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int 
 
   // dh = [dy | U_d] [W_d ; s A_d];  dg = dh u act'(g), du = dh act(g)
   {
-    GemmPlan g(V256_KMN);
+    GemmPlan g(kBigKMN);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(i), EPI_ACT_BWD, false);
     GemmPlan::seg(G, g.a_kmajor(dy, M, h, h), g.b_mnmajor(down.W, i, h, i), -1, h, h);
     GemmPlan::seg(G, g.a_kmajor(ud, M, kfd, kfd), g.b_mnmajor(af_d, i, kfd, i), -1, kfd, r);
@@ -738,7 +739,7 @@ extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int 
     g.p.status = status;
     g.finish();
     if (!g.ok) return LORA_ERR_CUDA;
-    LGB_TRY(launch_gemm(V256_KMN, g.p, LORA_KIND_ACT_BWD, stream));
+    LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_ACT_BWD, stream));
   }
 
   // dA_d = s U_d^T h
@@ -755,7 +756,7 @@ extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int 
 
   // dx = [dg | du | V] [W_g ; W_u ; s A_g ; s A_u]
   {
-    GemmPlan g(V256_KMN);
+    GemmPlan g(kBigKMN);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(h), EPI_STORE, false);
     GemmPlan::seg(G, g.a_kmajor(dg, M, i, i), g.b_mnmajor(gate.W, h, i, h), -1, i, i);
     GemmPlan::seg(G, g.a_kmajor(du, M, i, i), g.b_mnmajor(up.W, h, i, h), -1, i, i);
@@ -765,7 +766,7 @@ extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int 
     g.p.status = status;
     g.finish();
     if (!g.ok) return LORA_ERR_CUDA;
-    LGB_TRY(launch_gemm(V256_KMN, g.p, LORA_KIND_DGRAD, stream));
+    LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
   }
 
   // dA_g = s V_g^T x,  dA_u = s V_u^T x
@@ -915,7 +916,7 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
   if (x) {
     const ProjSeg p1 = {x, acat, h};
     LGB_TRY(rank_projection(M, kfq, &p1, 1, tqkv, part, status, stream));
-    GemmPlan g(V256_KK);
+    GemmPlan g(kBigKK);
     const int ax = g.a_kmajor(x, M, h, h);
     const int at = g.a_kmajor(tqkv, M, kfq, kfq);
     const lora_linear_t* lins[3] = {&q, &k, &v};
@@ -924,29 +925,29 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
     const int64_t ns[3] = {n_q, n_kv, n_kv};
     for (int p = 0; p < 3; ++p) {
       GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(ns[p]), EPI_STORE, false);
-      GemmPlan::seg(G, ax, g.b_kmajor(lins[p]->W, ns[p], h, h, 256), -1, h, h);
-      GemmPlan::seg(G, at, g.b_kmajor(bfs[p], ns[p], kfq, kfq, 256), -1, kfq, (p + 1) * r);
+      GemmPlan::seg(G, ax, g.b_kmajor(lins[p]->W, ns[p], h, h, g.b_rows_full()), -1, h, h);
+      GemmPlan::seg(G, at, g.b_kmajor(bfs[p], ns[p], kfq, kfq, g.b_rows_full()), -1, kfq, (p + 1) * r);
       G.out0 = ys[p];
       G.ldo = ns[p];
     }
     g.p.status = status;
     g.finish();
     if (!g.ok) return LORA_ERR_CUDA;
-    LGB_TRY(launch_gemm(V256_KK, g.p, LORA_KIND_PROJ, stream));
+    LGB_TRY(launch_gemm(kBigKK, g.p, LORA_KIND_PROJ, stream));
   }
   if (o_in) {
     const ProjSeg p2 = {o_in, acat_o, n_q};
     LGB_TRY(rank_projection(M, kfo, &p2, 1, to, part, status, stream));
-    GemmPlan g(V256_KK);
+    GemmPlan g(kBigKK);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(h), EPI_STORE, false);
-    GemmPlan::seg(G, g.a_kmajor(o_in, M, n_q, n_q), g.b_kmajor(o.W, h, n_q, n_q, 256), -1, n_q, n_q);
-    GemmPlan::seg(G, g.a_kmajor(to, M, kfo, kfo), g.b_kmajor(bf_o, h, kfo, kfo, 256), -1, kfo, r);
+    GemmPlan::seg(G, g.a_kmajor(o_in, M, n_q, n_q), g.b_kmajor(o.W, h, n_q, n_q, g.b_rows_full()), -1, n_q, n_q);
+    GemmPlan::seg(G, g.a_kmajor(to, M, kfo, kfo), g.b_kmajor(bf_o, h, kfo, kfo, g.b_rows_full()), -1, kfo, r);
     G.out0 = yo;
     G.ldo = h;
     g.p.status = status;
     g.finish();
     if (!g.ok) return LORA_ERR_CUDA;
-    LGB_TRY(launch_gemm(V256_KK, g.p, LORA_KIND_PROJ, stream));
+    LGB_TRY(launch_gemm(kBigKK, g.p, LORA_KIND_PROJ, stream));
   }
   return LORA_OK;
 }
@@ -1027,7 +1028,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     LGB_TRY(rank_projection(M, kfo, &p1, 1, uo, part, status, stream));
     const GradJob j1 = {dyo, h, 0, d_o.dB, 0};
     LGB_TRY(token_grads(M, r, kfo, s, to, &j1, 1, part, status, stream));
-    GemmPlan g(V256_KMN);
+    GemmPlan g(kBigKMN);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(n_q), EPI_STORE, false);
     GemmPlan::seg(G, g.a_kmajor(dyo, M, h, h), g.b_mnmajor(o.W, n_q, h, n_q), -1, h, h);
     GemmPlan::seg(G, g.a_kmajor(uo, M, kfo, kfo), g.b_mnmajor(af_o, n_q, kfo, n_q), -1, kfo, r);
@@ -1036,7 +1037,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     g.p.status = status;
     g.finish();
     if (!g.ok) return LORA_ERR_CUDA;
-    LGB_TRY(launch_gemm(V256_KMN, g.p, LORA_KIND_DGRAD, stream));
+    LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
     const GradJob j2 = {o_in, n_q, 0, d_o.dA, 1};
     LGB_TRY(token_grads(M, r, kfo, s, uo, &j2, 1, part, status, stream));
   }
@@ -1045,7 +1046,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     LGB_TRY(rank_projection(M, kfq, p3, 3, V, part, status, stream));
     const GradJob j3[3] = {{dyq, n_q, 0, d_q.dB, 0}, {dyk, n_kv, r, d_k.dB, 0}, {dyv, n_kv, 2 * r, d_v.dB, 0}};
     LGB_TRY(token_grads(M, r, kfq, s, tqkv, j3, 3, part, status, stream));
-    GemmPlan g(V256_KMN);
+    GemmPlan g(kBigKMN);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(h), EPI_STORE, false);
     GemmPlan::seg(G, g.a_kmajor(dyq, M, n_q, n_q), g.b_mnmajor(q.W, h, n_q, h), -1, n_q, n_q);
     GemmPlan::seg(G, g.a_kmajor(dyk, M, n_kv, n_kv), g.b_mnmajor(k.W, h, n_kv, h), -1, n_kv, n_kv);
@@ -1056,7 +1057,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     g.p.status = status;
     g.finish();
     if (!g.ok) return LORA_ERR_CUDA;
-    LGB_TRY(launch_gemm(V256_KMN, g.p, LORA_KIND_DGRAD, stream));
+    LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
     const GradJob j4[3] = {{x, h, 0, d_q.dA, 1}, {x, h, r, d_k.dA, 1}, {x, h, 2 * r, d_v.dA, 1}};
     LGB_TRY(token_grads(M, r, kfq, s, V, j4, 3, part, status, stream));
   }
