@@ -5,9 +5,9 @@
 
 namespace lgb {
 
-template <int STAGES, bool B_MN>
+template <int STAGES, bool B_MN, int EPIW>
 static cudaError_t launch_pair(const TcParams& p, int grid, cudaStream_t st) {
-  auto* k = tc_gemm_pair_kernel<STAGES, B_MN>;
+  auto* k = tc_gemm_pair_kernel<STAGES, B_MN, EPIW>;
   constexpr int smem = PairCfg<STAGES>::kSmemBytes;
   static bool configured = false;
   if (!configured) {
@@ -15,14 +15,15 @@ static cudaError_t launch_pair(const TcParams& p, int grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k<<<grid, kThreads, smem, st>>>(p);     // grid is a multiple of the cluster size (2)
+  k<<<grid, pair_threads(EPIW), smem, st>>>(p);  // grid is a multiple of the cluster size (2)
   return cudaGetLastError();
 }
 
 cudaError_t launch_tc_big(int variant, const TcParams& p, int grid, cudaStream_t st) {
   switch (variant) {
-    case VP_KK: return launch_pair<6, false>(p, grid, st);
-    case VP_KMN: return launch_pair<6, true>(p, grid, st);
+    // forward (gate/up activation, down): 4 epilogue warps; backward (act', dx): 8
+    case VP_KK: return launch_pair<6, false, 4>(p, grid, st);
+    case VP_KMN: return launch_pair<6, true, 8>(p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -16,6 +16,9 @@
 
 namespace lgb {
 
+// Threads of a pair-kernel CTA: producer warp, MMA warp and EPIW epilogue warps.
+constexpr int pair_threads(int epiw) { return 64 + 32 * epiw; }
+
 template <int STAGES>
 struct PairCfg {
   static constexpr int BN = 256;                       // accumulator columns per tile
@@ -30,9 +33,14 @@ struct PairCfg {
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
 
-template <int STAGES, bool B_MN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// EPIW = 4 or 8 epilogue warps: with 8, two warps share each TMEM lane quarter and
+// take half of the tile's columns each (more loads in flight for epilogues that read
+// saved tensors); with 4, fewer warps compete for issue slots with the producer and
+// MMA lanes (better for arithmetic-heavy epilogues).
+template <int STAGES, bool B_MN, int EPIW>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
+  static_assert(EPIW == 4 || EPIW == 8, "epilogue warps");
   using C = PairCfg<STAGES>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
@@ -63,7 +71,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 8);        // 4 epilogue warps x 2 CTAs (used on the even CTA)
+      mbar_init(tempty_bar(a), 2 * EPIW);  // every epilogue warp of both CTAs (even CTA's)
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -90,37 +98,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int u = pair; u < p.total_units && ok; u += npairs) {
         const Unit U = decode_unit(p, u);
         const GroupDesc& G = p.grp[U.g];
-        int seg = 0, seg_base = 0;
-        for (int kb = U.kb0; kb < U.kb1; ++kb) {
-          while (kb >= seg_base + G.seg[seg].kblocks) {
-            seg_base += G.seg[seg].kblocks;
-            ++seg;
-          }
-          const SegDesc& S = G.seg[seg];
-          const int kc = (kb - seg_base) * kBK;
-          if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) { ok = false; break; }
-          const uint32_t fb = full_bar(stage);
-          if (leader) {
-            mbar_arrive_expect_tx(fb, C::kTxBytes);
-            armed[stage] = static_cast<int>(phase);
-          }
-          const uint32_t fb_even = mapa_shared(fb, 0);
-          const uint32_t sa = sbase + stage * C::kStageBytes;
-          const uint32_t sb = sa + C::kABytes;
-          tma_load_2d_pair(sa, &p.maps[S.a], fb_even, kc, U.tm * (2 * kBM) + static_cast<int>(rank) * kBM);
-          if (!B_MN) {
-            if (S.b1 >= 0) {
-              tma_load_2d_pair(sb, &p.maps[rank ? S.b1 : S.b0], fb_even, kc, U.tn * C::kBLocal);
-            } else {
-              tma_load_2d_pair(sb, &p.maps[S.b0], fb_even, kc, U.tn * BN + static_cast<int>(rank) * C::kBLocal);
+        // walk the unit's k-range segment by segment; a segment's fields live in registers
+        const int nseg = G.nseg;
+        int seg_base = 0;
+        for (int sg = 0; sg < nseg && ok; ++sg) {
+          const int nkb = G.seg[sg].kblocks;
+          const int j0 = max(U.kb0 - seg_base, 0), j1 = min(U.kb1 - seg_base, nkb);
+          const CUtensorMap* ma = &p.maps[G.seg[sg].a];
+          const int b0 = G.seg[sg].b0, b1 = G.seg[sg].b1;
+          const CUtensorMap* mb = &p.maps[(rank && b1 >= 0) ? b1 : b0];
+          const int a_row = U.tm * (2 * kBM) + static_cast<int>(rank) * kBM;
+          const int b_row = (b1 >= 0) ? U.tn * C::kBLocal : U.tn * BN + static_cast<int>(rank) * C::kBLocal;
+          seg_base += nkb;
+          for (int j = j0; j < j1; ++j) {
+            const int kc = j * kBK;
+            if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) { ok = false; break; }
+            const uint32_t fb = full_bar(stage);
+            if (leader) {
+              mbar_arrive_expect_tx(fb, C::kTxBytes);
+              armed[stage] = static_cast<int>(phase);
             }
-          } else {
+            const uint32_t fb_even = mapa_shared(fb, 0);
+            const uint32_t sa = sbase + stage * C::kStageBytes;
+            const uint32_t sb = sa + C::kABytes;
+            tma_load_2d_pair(sa, ma, fb_even, kc, a_row);
+            if (!B_MN) {
+              tma_load_2d_pair(sb, mb, fb_even, kc, b_row);
+            } else {
 #pragma unroll
-            for (int c = 0; c < C::kBLocal / 64; ++c)
-              tma_load_2d_pair(sb + c * 8192u, &p.maps[S.b0], fb_even,
-                               U.tn * BN + static_cast<int>(rank) * C::kBLocal + c * 64, kc);
+              for (int c = 0; c < C::kBLocal / 64; ++c) tma_load_2d_pair(sb + c * 8192u, mb, fb_even, b_row + c * 64, kc);
+            }
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
       if (!ok && leader) {
@@ -144,30 +153,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         uint32_t accumulate = 0;
-        int seg = 0, seg_base = 0;
-        for (int kb = U.kb0; kb < U.kb1; ++kb) {
-          while (kb >= seg_base + G.seg[seg].kblocks) {
-            seg_base += G.seg[seg].kblocks;
-            ++seg;
-          }
-          const int kc = (kb - seg_base) * kBK;
-          const int kvalid = G.seg[seg].kvalid;
-          if (!wait_phase(full_bar(stage), phase, abort_flag, p)) { ok = false; break; }
-          tc_fence_after_sync();
-          const uint32_t sa = sbase + stage * C::kStageBytes;
-          const uint32_t sb = sa + C::kABytes;
+        const int nseg = G.nseg;
+        int seg_base = 0;
+        for (int sg = 0; sg < nseg && ok; ++sg) {
+          const int nkb = G.seg[sg].kblocks, kvalid = G.seg[sg].kvalid;
+          const int j0 = max(U.kb0 - seg_base, 0), j1 = min(U.kb1 - seg_base, nkb);
+          seg_base += nkb;
+          for (int j = j0; j < j1; ++j) {
+            const int kc = j * kBK;
+            if (!wait_phase(full_bar(stage), phase, abort_flag, p)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint32_t sa = sbase + stage * C::kStageBytes;
+            const uint32_t sb = sa + C::kABytes;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            if (kc + 16 * k < kvalid) {
-              const uint64_t adesc = smem_desc_sw128(sa + 32u * k, 16u, 1024u);
-              const uint64_t bdesc = B_MN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
-                                          : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
-              tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
-              accumulate = 1;
+            for (int k = 0; k < kBK / 16; ++k) {
+              if (kc + 16 * k < kvalid) {
+                const uint64_t adesc = smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+                const uint64_t bdesc = B_MN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
+                                            : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
+                tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
+                accumulate = 1;
+              }
             }
+            tc_commit_pair_multicast(empty_bar(stage), 0x3);   // frees this stage in both CTAs
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
-          tc_commit_pair_multicast(empty_bar(stage), 0x3);   // frees this stage in both CTAs
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         tc_commit_pair_multicast(tfull_bar(acc), 0x3);       // both halves of the tile ready
@@ -180,7 +190,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
+    // EPIW / 4 warps per TMEM lane quarter, each taking a share of the tile's columns
     const int q = warp & 3;
+    const int part = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
     const uint32_t tempty_even[2] = {mapa_shared(tempty_bar(0), 0), mapa_shared(tempty_bar(1), 0)};
     int acc = 0;
@@ -192,7 +204,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after_sync();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<BN>(p, G, U, tacc, U.tm * (2 * kBM) + static_cast<int>(rank) * kBM + row_in_tile);
+      epilogue_tile<BN>(p, G, U, tacc, U.tm * (2 * kBM) + static_cast<int>(rank) * kBM + row_in_tile, part, EPIW / 4);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_even[acc]);

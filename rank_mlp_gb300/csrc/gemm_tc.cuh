@@ -106,17 +106,23 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   return U;
 }
 
+// Wait limit in SM cycles: timeout_ns at up to 2.5 GHz (longer at lower clocks).
+// The SM cycle counter is a register read; the global nanosecond timer is not.
+__device__ __forceinline__ long long timeout_cycles(const TcParams& p) {
+  return static_cast<long long>(p.timeout_ns) * 5 / 2;
+}
+
 // Bounded wait: true when the phase completed, false on abort (flag set by another
 // role, or this wait timed out, which sets the flag and the status word).
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            const TcParams& p) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 15u) == 0) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > p.timeout_ns) {
+      if (clock64() - t0 > timeout_cycles(p)) {
         *abort_flag = 1;
         if (p.status) atomicOr(p.status, kStatusTimeout);
         return false;
@@ -127,9 +133,9 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 
 // Drain wait after an abort: bounded by time only.
 __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity, const TcParams& p) {
-  const uint64_t t0 = global_timer_ns();
+  const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > p.timeout_ns) {
+    if (clock64() - t0 > timeout_cycles(p)) {
       if (p.status) atomicOr(p.status, kStatusTimeout);
       return;
     }
@@ -147,7 +153,7 @@ constexpr float kGeluC = 0.044715f;
 
 // act(g): silu or tanh-GELU ("Model Patches and Kernels", activation table).
 __device__ __forceinline__ float act_fwd(float g, int act) {
-  if (act == ACT_SWIGLU) return g / (1.0f + __expf(-g));
+  if (act == ACT_SWIGLU) return __fdividef(g, 1.0f + __expf(-g));
   const float t = tanh_approx(kSqrt2OverPi * (g + kGeluC * g * g * g));
   return 0.5f * g * (1.0f + t);
 }
@@ -155,7 +161,7 @@ __device__ __forceinline__ float act_fwd(float g, int act) {
 // act(g) and act'(g) together.
 __device__ __forceinline__ void act_fwd_bwd(float g, int act, float& a, float& ap) {
   if (act == ACT_SWIGLU) {
-    const float sg = 1.0f / (1.0f + __expf(-g));
+    const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
     a = g * sg;
     ap = sg * (1.0f + g * (1.0f - sg));
   } else {
@@ -168,17 +174,19 @@ __device__ __forceinline__ void act_fwd_bwd(float g, int act, float& a, float& a
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Epilogue of one accumulator tile.  The calling thread owns output row `row` and
-// reads its TMEM lane at `tacc` (columns = the tile's N).  Warp-collective: every
-// lane of the warp calls it (tcgen05.ld), rows past M are computed and dropped.
+// Epilogue of one accumulator tile, columns split into `nparts` equal parts of which
+// this warp takes part `part`.  The calling thread owns output row `row` and reads its
+// TMEM lane at `tacc`.  Warp-collective: every lane of the warp calls it (tcgen05.ld);
+// rows past M are computed and dropped.
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc& G, const Unit& U,
-                                              uint32_t tacc, int row) {
+                                              uint32_t tacc, int row, int part, int nparts) {
   const bool row_ok = row < G.M;
   if (G.epi == EPI_STORE) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(G.out0);
+    const int span = BN / nparts, c_lo = part * span;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = c_lo; c < c_lo + span; c += 32) {
       uint32_t v[32];
       __syncwarp();
       tmem_ld32(tacc + c, v);
@@ -204,8 +212,9 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
     __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(G.out0);
     __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(G.out1);
     __nv_bfloat16* uout = static_cast<__nv_bfloat16*>(G.out2);
+    const int span = (BN / 2) / nparts, c_lo = part * span;
 #pragma unroll 1
-    for (int c = 0; c < BN / 2; c += 32) {
+    for (int c = c_lo; c < c_lo + span; c += 32) {
       uint32_t vg[32], vu[32];
       __syncwarp();
       tmem_ld32(tacc + c, vg);
@@ -245,26 +254,34 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
       }
     }
   } else if (G.epi == EPI_ACT_BWD) {
-    // accumulator = dh; saved g, u give dg = dh * u * act'(g), du = dh * act(g)
+    // accumulator = dh; saved g, u give dg = dh * u * act'(g), du = dh * act(g).  The
+    // g, u loads of the next 32-column chunk are in flight while this one is computed.
     const __nv_bfloat16* gin = static_cast<const __nv_bfloat16*>(G.in0);
     const __nv_bfloat16* uin = static_cast<const __nv_bfloat16*>(G.in1);
     __nv_bfloat16* dgo = static_cast<__nv_bfloat16*>(G.out0);
     __nv_bfloat16* duo = static_cast<__nv_bfloat16*>(G.out1);
-#pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    const int span = BN / nparts, c_lo = part * span, c_hi = c_lo + span;
+    const long long rbase = static_cast<long long>(row) * G.ldi + U.tn * BN;
+    auto load_chunk = [&](int c, uint4 (&gw)[4], uint4 (&uw)[4]) {
       const int col0 = U.tn * BN + c;
-      uint4 gw[4], uw[4];
-      const long long ioff = static_cast<long long>(row) * G.ldi + col0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (row_ok && col0 + 8 * j + 8 <= G.N) {
-          gw[j] = __ldg(reinterpret_cast<const uint4*>(gin + ioff + 8 * j));
-          uw[j] = __ldg(reinterpret_cast<const uint4*>(uin + ioff + 8 * j));
+          gw[j] = __ldg(reinterpret_cast<const uint4*>(gin + rbase + c + 8 * j));
+          uw[j] = __ldg(reinterpret_cast<const uint4*>(uin + rbase + c + 8 * j));
         } else {
           gw[j] = make_uint4(0, 0, 0, 0);
           uw[j] = make_uint4(0, 0, 0, 0);
         }
       }
+    };
+    uint4 gw[4], uw[4];
+    load_chunk(c_lo, gw, uw);
+#pragma unroll 1
+    for (int c = c_lo; c < c_hi; c += 32) {
+      uint4 gn[4], un[4];
+      if (c + 32 < c_hi) load_chunk(c + 32, gn, un);
+      const int col0 = U.tn * BN + c;
       uint32_t v[32];
       __syncwarp();
       tmem_ld32(tacc + c, v);
@@ -294,13 +311,21 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
           }
         }
       }
+      if (c + 32 < c_hi) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          gw[j] = gn[j];
+          uw[j] = un[j];
+        }
+      }
     }
   } else {
     // EPI_PARTIAL: f32 tile into the split's slab (rows and columns padded)
     const long long width = static_cast<long long>(G.tiles_n) * BN;
     float* dst = G.part + (static_cast<long long>(U.split) * G.tiles_m * kBM + row) * width + U.tn * BN;
+    const int span = BN / nparts, c_lo = part * span;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
+    for (int c = c_lo; c < c_lo + span; c += 32) {
       uint32_t v[32];
       __syncwarp();
       tmem_ld32(tacc + c, v);
@@ -366,40 +391,44 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
         const Unit U = decode_unit(p, u);
         const GroupDesc& G = p.grp[U.g];
-        int seg = 0, seg_base = 0;
-        for (int kb = U.kb0; kb < U.kb1; ++kb) {
-          while (kb >= seg_base + G.seg[seg].kblocks) {
-            seg_base += G.seg[seg].kblocks;
-            ++seg;
-          }
-          const SegDesc& S = G.seg[seg];
-          const int kc = (kb - seg_base) * kBK;
-          if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) { ok = false; break; }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, C::kStageBytes);
-          armed[stage] = static_cast<int>(phase);
-          const uint32_t sa = sbase + stage * C::kStageBytes;
-          const uint32_t sb = sa + C::kABytes;
-          const CUtensorMap* ma = &p.maps[S.a];
-          if (!A_MN) {
-            tma_load_2d(sa, ma, fb, kc, U.tm * kBM);
-          } else {
-            tma_load_2d(sa, ma, fb, U.tm * kBM, kc);
-            tma_load_2d(sa + 8192u, ma, fb, U.tm * kBM + 64, kc);
-          }
-          if (!B_MN) {
-            if (S.b1 >= 0) {
-              tma_load_2d(sb, &p.maps[S.b0], fb, kc, U.tn * (BN / 2));
-              tma_load_2d(sb + (BN / 2) * 128u, &p.maps[S.b1], fb, kc, U.tn * (BN / 2));
+        // walk the unit's k-range segment by segment; a segment's fields live in registers
+        const int nseg = G.nseg;
+        int seg_base = 0;
+        for (int sg = 0; sg < nseg && ok; ++sg) {
+          const int nkb = G.seg[sg].kblocks;
+          const int j0 = max(U.kb0 - seg_base, 0), j1 = min(U.kb1 - seg_base, nkb);
+          const CUtensorMap* ma = &p.maps[G.seg[sg].a];
+          const CUtensorMap* mb0 = &p.maps[G.seg[sg].b0];
+          const int b1 = G.seg[sg].b1;
+          const CUtensorMap* mb1 = &p.maps[b1 >= 0 ? b1 : G.seg[sg].b0];
+          seg_base += nkb;
+          for (int j = j0; j < j1; ++j) {
+            const int kc = j * kBK;
+            if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) { ok = false; break; }
+            const uint32_t fb = full_bar(stage);
+            mbar_arrive_expect_tx(fb, C::kStageBytes);
+            armed[stage] = static_cast<int>(phase);
+            const uint32_t sa = sbase + stage * C::kStageBytes;
+            const uint32_t sb = sa + C::kABytes;
+            if (!A_MN) {
+              tma_load_2d(sa, ma, fb, kc, U.tm * kBM);
             } else {
-              tma_load_2d(sb, &p.maps[S.b0], fb, kc, U.tn * BN);
+              tma_load_2d(sa, ma, fb, U.tm * kBM, kc);
+              tma_load_2d(sa + 8192u, ma, fb, U.tm * kBM + 64, kc);
             }
-          } else {
+            if (!B_MN) {
+              if (b1 >= 0) {
+                tma_load_2d(sb, mb0, fb, kc, U.tn * (BN / 2));
+                tma_load_2d(sb + (BN / 2) * 128u, mb1, fb, kc, U.tn * (BN / 2));
+              } else {
+                tma_load_2d(sb, mb0, fb, kc, U.tn * BN);
+              }
+            } else {
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              tma_load_2d(sb + c * 8192u, &p.maps[S.b0], fb, U.tn * BN + c * 64, kc);
+              for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * 8192u, mb0, fb, U.tn * BN + c * 64, kc);
+            }
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
       if (!ok) {
@@ -424,31 +453,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         uint32_t accumulate = 0;
-        int seg = 0, seg_base = 0;
-        for (int kb = U.kb0; kb < U.kb1; ++kb) {
-          while (kb >= seg_base + G.seg[seg].kblocks) {
-            seg_base += G.seg[seg].kblocks;
-            ++seg;
-          }
-          const int kc = (kb - seg_base) * kBK;
-          const int kvalid = G.seg[seg].kvalid;
-          if (!wait_phase(full_bar(stage), phase, abort_flag, p)) { ok = false; break; }
-          tc_fence_after_sync();
-          const uint32_t sa = sbase + stage * C::kStageBytes;
-          const uint32_t sb = sa + C::kABytes;
+        const int nseg = G.nseg;
+        int seg_base = 0;
+        for (int sg = 0; sg < nseg && ok; ++sg) {
+          const int nkb = G.seg[sg].kblocks, kvalid = G.seg[sg].kvalid;
+          const int j0 = max(U.kb0 - seg_base, 0), j1 = min(U.kb1 - seg_base, nkb);
+          seg_base += nkb;
+          for (int j = j0; j < j1; ++j) {
+            const int kc = j * kBK;
+            if (!wait_phase(full_bar(stage), phase, abort_flag, p)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint32_t sa = sbase + stage * C::kStageBytes;
+            const uint32_t sb = sa + C::kABytes;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            if (kc + 16 * k < kvalid) {
-              const uint64_t adesc = A_MN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
-                                          : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
-              const uint64_t bdesc = B_MN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
-                                          : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
-              tc_mma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
-              accumulate = 1;
+            for (int k = 0; k < kBK / 16; ++k) {
+              if (kc + 16 * k < kvalid) {
+                const uint64_t adesc = A_MN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
+                                            : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
+                const uint64_t bdesc = B_MN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
+                                            : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
+                tc_mma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
+                accumulate = 1;
+              }
             }
+            tc_commit(empty_bar(stage));     // frees this smem stage once its MMAs are done
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
-          tc_commit(empty_bar(stage));     // frees this smem stage once its MMAs are done
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         tc_commit(tfull_bar(acc));         // accumulator ready for the epilogue
@@ -473,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after_sync();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<BN>(p, G, U, tacc, U.tm * kBM + row_in_tile);
+      epilogue_tile<BN>(p, G, U, tacc, U.tm * kBM + row_in_tile, 0, 1);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));

@@ -179,7 +179,7 @@ struct GemmPlan {
     p.total_units = u;
     int maxtn = 1;
     for (int g = 0; g < p.ngroups; ++g) maxtn = p.grp[g].tiles_n > maxtn ? p.grp[g].tiles_n : maxtn;
-    p.band = maxtn < 8 ? maxtn : 8;
+    p.band = maxtn < 16 ? maxtn : 16;
   }
 };
 
