@@ -174,6 +174,26 @@ __device__ __forceinline__ void act_fwd_bwd(float g, int act, float& a, float& a
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Writes 32 bf16 values (w: 16 packed pairs) of one row at dst, columns col0 ..
+// col0+31, keeping the columns below N.  v8 (row start and stride 32-byte aligned):
+// two whole-sector stores; otherwise 16-byte pieces.
+__device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint32_t (&w)[16], int col0, int N,
+                                                 bool v8) {
+  if (v8 && col0 + 32 <= N) {
+    st_global_v8(dst, w);
+    st_global_v8(dst + 16, w + 8);
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (col0 + 8 * j + 8 <= N)
+      *reinterpret_cast<uint4*>(dst + 8 * j) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+}
+
+__device__ __forceinline__ bool rows_v8_aligned(const void* base, long long ld) {
+  return (ld % 16) == 0 && (reinterpret_cast<uintptr_t>(base) & 31) == 0;
+}
+
 // Epilogue of one accumulator tile, columns split into `nparts` equal parts of which
 // this warp takes part `part`.  The calling thread owns output row `row` and reads its
 // TMEM lane at `tacc`.  Warp-collective: every lane of the warp calls it (tcgen05.ld);
@@ -184,6 +204,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
   const bool row_ok = row < G.M;
   if (G.epi == EPI_STORE) {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(G.out0);
+    const bool v8 = rows_v8_aligned(out, G.ldo);
     const int span = BN / nparts, c_lo = part * span;
 #pragma unroll 1
     for (int c = c_lo; c < c_lo + span; c += 32) {
@@ -193,18 +214,10 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
       tmem_ld_wait();
       const int col0 = U.tn * BN + c;
       if (row_ok) {
-        __nv_bfloat16* dst = out + static_cast<long long>(row) * G.ldo + col0;
+        uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          if (col0 + j + 8 <= G.N) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[j + 0]), __uint_as_float(v[j + 1]));
-            w.y = pack_bf16x2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-            w.z = pack_bf16x2(__uint_as_float(v[j + 4]), __uint_as_float(v[j + 5]));
-            w.w = pack_bf16x2(__uint_as_float(v[j + 6]), __uint_as_float(v[j + 7]));
-            *reinterpret_cast<uint4*>(dst + j) = w;
-          }
-        }
+        for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+        store_row32_bf16(out + static_cast<long long>(row) * G.ldo + col0, w, col0, G.N, v8);
       }
     }
   } else if (G.epi == EPI_ACT_FWD) {
@@ -212,6 +225,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
     __nv_bfloat16* hout = static_cast<__nv_bfloat16*>(G.out0);
     __nv_bfloat16* gout = static_cast<__nv_bfloat16*>(G.out1);
     __nv_bfloat16* uout = static_cast<__nv_bfloat16*>(G.out2);
+    const bool v8 = rows_v8_aligned(hout, G.ldo) && (gout == nullptr || (rows_v8_aligned(gout, G.ldo) &&
+                                                                         rows_v8_aligned(uout, G.ldo)));
     const int span = (BN / 2) / nparts, c_lo = part * span;
 #pragma unroll 1
     for (int c = c_lo; c < c_lo + span; c += 32) {
@@ -223,33 +238,21 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
       const int col0 = U.tn * (BN / 2) + c;
       if (row_ok) {
         const long long off = static_cast<long long>(row) * G.ldo + col0;
+        uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          if (col0 + j + 8 <= G.N) {
-            float hv[8];
+        for (int e = 0; e < 16; ++e) {
+          const float h0 = act_fwd(__uint_as_float(vg[2 * e]), p.act) * __uint_as_float(vu[2 * e]);
+          const float h1 = act_fwd(__uint_as_float(vg[2 * e + 1]), p.act) * __uint_as_float(vu[2 * e + 1]);
+          w[e] = pack_bf16x2(h0, h1);
+        }
+        store_row32_bf16(hout + off, w, col0, G.N, v8);
+        if (gout != nullptr) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              hv[e] = act_fwd(__uint_as_float(vg[j + e]), p.act) * __uint_as_float(vu[j + e]);
-            uint4 w;
-            w.x = pack_bf16x2(hv[0], hv[1]);
-            w.y = pack_bf16x2(hv[2], hv[3]);
-            w.z = pack_bf16x2(hv[4], hv[5]);
-            w.w = pack_bf16x2(hv[6], hv[7]);
-            *reinterpret_cast<uint4*>(hout + off + j) = w;
-            if (gout != nullptr) {
-              uint4 wg, wu;
-              wg.x = pack_bf16x2(__uint_as_float(vg[j + 0]), __uint_as_float(vg[j + 1]));
-              wg.y = pack_bf16x2(__uint_as_float(vg[j + 2]), __uint_as_float(vg[j + 3]));
-              wg.z = pack_bf16x2(__uint_as_float(vg[j + 4]), __uint_as_float(vg[j + 5]));
-              wg.w = pack_bf16x2(__uint_as_float(vg[j + 6]), __uint_as_float(vg[j + 7]));
-              wu.x = pack_bf16x2(__uint_as_float(vu[j + 0]), __uint_as_float(vu[j + 1]));
-              wu.y = pack_bf16x2(__uint_as_float(vu[j + 2]), __uint_as_float(vu[j + 3]));
-              wu.z = pack_bf16x2(__uint_as_float(vu[j + 4]), __uint_as_float(vu[j + 5]));
-              wu.w = pack_bf16x2(__uint_as_float(vu[j + 6]), __uint_as_float(vu[j + 7]));
-              *reinterpret_cast<uint4*>(gout + off + j) = wg;
-              *reinterpret_cast<uint4*>(uout + off + j) = wu;
-            }
-          }
+          for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(vg[2 * e]), __uint_as_float(vg[2 * e + 1]));
+          store_row32_bf16(gout + off, w, col0, G.N, v8);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(vu[2 * e]), __uint_as_float(vu[2 * e + 1]));
+          store_row32_bf16(uout + off, w, col0, G.N, v8);
         }
       }
     }
@@ -260,6 +263,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
     const __nv_bfloat16* uin = static_cast<const __nv_bfloat16*>(G.in1);
     __nv_bfloat16* dgo = static_cast<__nv_bfloat16*>(G.out0);
     __nv_bfloat16* duo = static_cast<__nv_bfloat16*>(G.out1);
+    const bool v8 = rows_v8_aligned(dgo, G.ldo) && rows_v8_aligned(duo, G.ldo);
     const int span = BN / nparts, c_lo = part * span, c_hi = c_lo + span;
     const long long rbase = static_cast<long long>(row) * G.ldi + U.tn * BN;
     auto load_chunk = [&](int c, uint4 (&gw)[4], uint4 (&uw)[4]) {
@@ -288,28 +292,26 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
       tmem_ld_wait();
       if (row_ok) {
         const long long ooff = static_cast<long long>(row) * G.ldo + col0;
+        uint32_t og[16], ou[16];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (col0 + 8 * j + 8 <= G.N) {
-            const uint32_t gg[4] = {gw[j].x, gw[j].y, gw[j].z, gw[j].w};
-            const uint32_t uu[4] = {uw[j].x, uw[j].y, uw[j].z, uw[j].w};
-            uint32_t og[4], ou[4];
+          const uint32_t gg[4] = {gw[j].x, gw[j].y, gw[j].z, gw[j].w};
+          const uint32_t uu[4] = {uw[j].x, uw[j].y, uw[j].z, uw[j].w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float a0, ap0, a1, ap1;
-              const float g0 = bf16_lo(gg[e]), g1 = bf16_hi(gg[e]);
-              const float u0 = bf16_lo(uu[e]), u1 = bf16_hi(uu[e]);
-              act_fwd_bwd(g0, p.act, a0, ap0);
-              act_fwd_bwd(g1, p.act, a1, ap1);
-              const float d0 = __uint_as_float(v[8 * j + 2 * e]);
-              const float d1 = __uint_as_float(v[8 * j + 2 * e + 1]);
-              og[e] = pack_bf16x2(d0 * u0 * ap0, d1 * u1 * ap1);
-              ou[e] = pack_bf16x2(d0 * a0, d1 * a1);
-            }
-            *reinterpret_cast<uint4*>(dgo + ooff + 8 * j) = make_uint4(og[0], og[1], og[2], og[3]);
-            *reinterpret_cast<uint4*>(duo + ooff + 8 * j) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+          for (int e = 0; e < 4; ++e) {
+            float a0, ap0, a1, ap1;
+            const float g0 = bf16_lo(gg[e]), g1 = bf16_hi(gg[e]);
+            const float u0 = bf16_lo(uu[e]), u1 = bf16_hi(uu[e]);
+            act_fwd_bwd(g0, p.act, a0, ap0);
+            act_fwd_bwd(g1, p.act, a1, ap1);
+            const float d0 = __uint_as_float(v[8 * j + 2 * e]);
+            const float d1 = __uint_as_float(v[8 * j + 2 * e + 1]);
+            og[4 * j + e] = pack_bf16x2(d0 * u0 * ap0, d1 * u1 * ap1);
+            ou[4 * j + e] = pack_bf16x2(d0 * a0, d1 * a1);
           }
         }
+        store_row32_bf16(dgo + ooff, og, col0, G.N, v8);
+        store_row32_bf16(duo + ooff, ou, col0, G.N, v8);
       }
       if (c + 32 < c_hi) {
 #pragma unroll
@@ -320,7 +322,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
       }
     }
   } else {
-    // EPI_PARTIAL: f32 tile into the split's slab (rows and columns padded)
+    // EPI_PARTIAL: f32 tile into the split's slab (rows and columns padded, 32-byte
+    // aligned: the slab starts 256-byte aligned and its width is a multiple of 64)
     const long long width = static_cast<long long>(G.tiles_n) * BN;
     float* dst = G.part + (static_cast<long long>(U.split) * G.tiles_m * kBM + row) * width + U.tn * BN;
     const int span = BN / nparts, c_lo = part * span;
@@ -331,8 +334,7 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
       tmem_ld32(tacc + c, v);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<uint4*>(dst + c + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      for (int j = 0; j < 32; j += 8) st_global_v8(dst + c + j, v + j);
     }
   }
 }
