@@ -16,7 +16,7 @@
  * one call; activations from the same page, "Activation functions" table):
  *
  *     g = (1) with gate,  u = (1) with up,  h = act(g) * u,  y = (1) of h with down
- *     act = silu (SwiGLU) or the tanh approximation of GELU (GeGLU)
+ *     act = silu (SwiGLU), or GELU (GeGLU): exact (erf) or its tanh approximation
  *
  * The attention projections (row opake_lora_qkv: q, k, v share the input x; the
  * axolotl "monkeypatch.lora_kernels" reference, original_apply_qkv returning
@@ -67,14 +67,15 @@ extern "C" {
 
 typedef enum {
   LORA_ACT_SWIGLU = 0,      /* silu(g) * u */
-  LORA_ACT_GEGLU_TANH = 1   /* gelu_tanh(g) * u, 0.5 g (1 + tanh(sqrt(2/pi)(g + 0.044715 g^3))) */
+  LORA_ACT_GEGLU_TANH = 1,  /* gelu_tanh(g) * u, 0.5 g (1 + tanh(sqrt(2/pi)(g + 0.044715 g^3))) */
+  LORA_ACT_GEGLU_ERF = 2    /* gelu(g) * u, 0.5 g (1 + erf(g / sqrt 2)) */
 } lora_act_t;
 
 typedef enum {
   LORA_OK = 0,
   LORA_ERR_INVALID_ARG = 1,   /* NULL pointer, negative size, bad enum, non-finite s */
   LORA_ERR_ALIGNMENT = 2,     /* pointer or feature size violates the alignment rules */
-  LORA_ERR_UNSUPPORTED = 3,   /* rank beyond the limits above, or a non-NULL bias */
+  LORA_ERR_UNSUPPORTED = 3,   /* rank beyond the limits above */
   LORA_ERR_WORKSPACE = 4,     /* ws_bytes below the workspace query */
   LORA_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
   LORA_ERR_TIMEOUT = 6        /* a kernel's bounded wait expired (read by lora_poll_status) */
@@ -152,8 +153,11 @@ lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int r, float s,
  * q = (1)(x; q) [M x n_q], k, v = (1)(x; k or v) [M x n_kv] ("opake_lora_qkv"), and
  * yo = (1)(o_in; o) [M x h] with W_o [h x n_q] ("original_apply_o").  Attention runs
  * between the two halves in a real block, so either half may be skipped: x == NULL
- * skips q/k/v, o_in == NULL skips O.  bias_qkv must be NULL (frozen biases are not
- * supported; LORA_ERR_UNSUPPORTED otherwise). */
+ * skips q/k/v, o_in == NULL skips O.  bias_qkv is NULL or the frozen base-layer
+ * biases of q, k and v, bf16 [n_q + 2 n_kv] (q's, then k's, then v's), 16-byte
+ * aligned, added to q, k, v ("Fused LoRA operations": QKV fusion supports optional
+ * frozen base-layer biases); a frozen bias gets no gradient, so backward does not
+ * take it. */
 size_t lora_qkvo_saved_bytes(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r);
 size_t lora_qkvo_workspace_bytes(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r);
 lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r, float s,

@@ -12,7 +12,8 @@ Sources (web pages; each function names the passage it follows):
   gate + up + activation + down in one call (row ``opake_lora_mlp``); MLP fusion
   is bias-free.
 * same page, section "Triton kernels", "Activation functions" table:
-  SwiGLU ``silu(gate) * up`` and GeGLU Approx ``gelu_tanh(gate) * up``.
+  SwiGLU ``silu(gate) * up``, GeGLU Exact ``gelu(gate) * up`` (erf-based) and GeGLU
+  Approx ``gelu_tanh(gate) * up``.
 * same page, section "Fused linear cross-entropy", "Key design decisions": a frozen
   weight gets no gradient.  Base weights W are frozen here, so backward returns
   dX and the adapter gradients dA, dB only.
@@ -44,7 +45,7 @@ from __future__ import annotations
 
 import numpy as np
 
-ACTS = ("swiglu", "geglu_tanh")
+ACTS = ("swiglu", "geglu_tanh", "geglu_erf")
 _SQRT_2_OVER_PI = np.sqrt(2.0 / np.pi)
 _GELU_C = 0.044715
 
@@ -73,11 +74,19 @@ def gelu_tanh(g: np.ndarray) -> np.ndarray:
     return 0.5 * g * (1.0 + np.tanh(_SQRT_2_OVER_PI * (g + _GELU_C * g ** 3)))
 
 
+def gelu_erf(g: np.ndarray) -> np.ndarray:
+    """Exact GELU, g * Phi(g) with Phi the standard normal CDF (GeGLU Exact row)."""
+    from scipy.special import erf
+    return 0.5 * g * (1.0 + erf(g / np.sqrt(2.0)))
+
+
 def act(g: np.ndarray, kind: str) -> np.ndarray:
     if kind == "swiglu":
         return silu(g)
     if kind == "geglu_tanh":
         return gelu_tanh(g)
+    if kind == "geglu_erf":
+        return gelu_erf(g)
     raise ValueError(f"unknown activation {kind!r}")
 
 
@@ -87,6 +96,7 @@ def act_prime(g: np.ndarray, kind: str) -> np.ndarray:
     silu'(g) = sigma(g) (1 + g (1 - sigma(g))).
     gelu_tanh'(g) = 0.5 (1 + t) + 0.5 g (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 g^2),
     t = tanh(sqrt(2/pi) (g + 0.044715 g^3)).
+    gelu_erf'(g) = Phi(g) + g phi(g), phi the standard normal density.
     """
     if kind == "swiglu":
         sg = sigmoid(g)
@@ -95,6 +105,9 @@ def act_prime(g: np.ndarray, kind: str) -> np.ndarray:
         t = np.tanh(_SQRT_2_OVER_PI * (g + _GELU_C * g ** 3))
         return 0.5 * (1.0 + t) + 0.5 * g * (1.0 - t * t) * _SQRT_2_OVER_PI * (
             1.0 + 3.0 * _GELU_C * g * g)
+    if kind == "geglu_erf":
+        from scipy.special import erf
+        return 0.5 * (1.0 + erf(g / np.sqrt(2.0))) + g * np.exp(-0.5 * g * g) / np.sqrt(2.0 * np.pi)
     raise ValueError(f"unknown activation {kind!r}")
 
 
@@ -160,11 +173,17 @@ def mlp_backward(x, Wg, Ag, Bg, Wu, Au, Bu, Wd, Ad, Bd, s, kind, dy):
 # The attention between them is not part of this path; o_in is its output.
 # --------------------------------------------------------------------------------
 
-def qkvo_forward(x, lin_q, lin_k, lin_v, o_in, lin_o, s):
-    """lin_p = (W, A, B).  Returns dict(q, k, v, o)."""
+def qkvo_forward(x, lin_q, lin_k, lin_v, o_in, lin_o, s, bias=None):
+    """lin_p = (W, A, B).  Returns dict(q, k, v, o).
+
+    bias: optional frozen base-layer biases (b_q, b_k, b_v) added to q, k, v
+    ("Fused LoRA operations": QKV fusion supports optional frozen base-layer biases).
+    A frozen bias gets no gradient and does not change the backward."""
     out = {}
-    for name, lin in (("q", lin_q), ("k", lin_k), ("v", lin_v)):
+    for j, (name, lin) in enumerate((("q", lin_q), ("k", lin_k), ("v", lin_v))):
         out[name] = lora_linear(x, *lin, s)
+        if bias is not None:
+            out[name] = out[name] + bias[j][None, :]
     out["o"] = lora_linear(o_in, *lin_o, s)
     return out
 

@@ -19,7 +19,7 @@ import torch
 
 from . import build as _build
 
-ACT = {"swiglu": 0, "geglu_tanh": 1}
+ACT = {"swiglu": 0, "geglu_tanh": 1, "geglu_erf": 2}
 KIND_NAMES = {0: "pack", 1: "reduce", 2: "rank_proj", 3: "rank_grad", 4: "gate_up",
               5: "proj", 6: "act_bwd", 7: "dgrad"}
 STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported",
@@ -260,9 +260,10 @@ def mlp_backward(x, gate, up, down, s, act, saved, dy, *, dx=None, grads=None, w
 
 # ------------------------------------------------------------------ Q/K/V + O
 
-def qkvo_forward(x, q, k, v, o_in, o, s, *, saved=None, training=True, ws=None, outs=None):
+def qkvo_forward(x, q, k, v, o_in, o, s, *, bias=None, saved=None, training=True, ws=None, outs=None):
     """q/k/v from x (skipped if x is None) and the O projection of o_in (skipped if
-    o_in is None).  Returns (dict(q, k, v, o), saved)."""
+    o_in is None).  bias: None or the frozen q/k/v biases, one bf16 tensor
+    [n_q + 2 n_kv].  Returns (dict(q, k, v, o), saved)."""
     lib = load()
     ref = x if x is not None else o_in
     dev = ref.device
@@ -290,7 +291,7 @@ def qkvo_forward(x, q, k, v, o_in, o, s, *, saved=None, training=True, ws=None, 
         _lin(v, "v") if x is not None else z,
         _opt(res.get("q"), "yq"), _opt(res.get("k"), "yk"), _opt(res.get("v"), "yv"),
         _opt(o_in, "o_in"), _lin(o, "o") if o_in is not None else z, _opt(res.get("o"), "yo"),
-        None, None if saved is None else saved.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)),
+        _opt(bias, "bias"), None if saved is None else saved.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)),
         "lora_qkvo_forward")
     return res, saved
 

@@ -32,7 +32,7 @@ constexpr int kMaxSegs = 4;
 constexpr unsigned kStatusTimeout = 1u;
 
 enum EpiKind : int { EPI_STORE = 0, EPI_ACT_FWD = 1, EPI_ACT_BWD = 2, EPI_PARTIAL = 3 };
-enum ActKind : int { ACT_SWIGLU = 0, ACT_GEGLU_TANH = 1 };
+enum ActKind : int { ACT_SWIGLU = 0, ACT_GEGLU_TANH = 1, ACT_GEGLU_ERF = 2 };
 
 struct SegDesc {
   int a, b0, b1;   // tensor-map indices; b1 >= 0: B tile = BN/2 rows of b0 + BN/2 rows of b1
@@ -151,9 +151,13 @@ __device__ __forceinline__ float tanh_approx(float x) {
 constexpr float kSqrt2OverPi = 0.7978845608028654f;
 constexpr float kGeluC = 0.044715f;
 
-// act(g): silu or tanh-GELU ("Model Patches and Kernels", activation table).
+constexpr float kSqrtHalf = 0.7071067811865476f;
+constexpr float kInvSqrt2Pi = 0.3989422804014327f;
+
+// act(g): silu, tanh-GELU or exact GELU ("Model Patches and Kernels", activation table).
 __device__ __forceinline__ float act_fwd(float g, int act) {
   if (act == ACT_SWIGLU) return __fdividef(g, 1.0f + __expf(-g));
+  if (act == ACT_GEGLU_ERF) return 0.5f * g * (1.0f + erff(g * kSqrtHalf));
   const float t = tanh_approx(kSqrt2OverPi * (g + kGeluC * g * g * g));
   return 0.5f * g * (1.0f + t);
 }
@@ -164,6 +168,10 @@ __device__ __forceinline__ void act_fwd_bwd(float g, int act, float& a, float& a
     const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
     a = g * sg;
     ap = sg * (1.0f + g * (1.0f - sg));
+  } else if (act == ACT_GEGLU_ERF) {
+    const float cdf = 0.5f * (1.0f + erff(g * kSqrtHalf));
+    a = g * cdf;
+    ap = cdf + g * kInvSqrt2Pi * __expf(-0.5f * g * g);
   } else {
     const float t = tanh_approx(kSqrt2OverPi * (g + kGeluC * g * g * g));
     a = 0.5f * g * (1.0f + t);
@@ -203,7 +211,9 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
                                               uint32_t tacc, int row, int part, int nparts) {
   const bool row_ok = row < G.M;
   if (G.epi == EPI_STORE) {
+    // optional frozen per-column bias (in0, bf16 [N]) added before rounding
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(G.out0);
+    const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(G.in0);
     const bool v8 = rows_v8_aligned(out, G.ldo);
     const int span = BN / nparts, c_lo = part * span;
 #pragma unroll 1
@@ -215,8 +225,21 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
       const int col0 = U.tn * BN + c;
       if (row_ok) {
         uint32_t w[16];
+        if (bias != nullptr) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+          for (int j = 0; j < 4; ++j) {
+            const uint4 b = (col0 + 8 * j + 8 <= G.N) ? __ldg(reinterpret_cast<const uint4*>(bias + col0 + 8 * j))
+                                                      : make_uint4(0, 0, 0, 0);
+            const uint32_t bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[4 * j + e] = pack_bf16x2(__uint_as_float(v[8 * j + 2 * e]) + bf16_lo(bb[e]),
+                                         __uint_as_float(v[8 * j + 2 * e + 1]) + bf16_hi(bb[e]));
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+        }
         store_row32_bf16(out + static_cast<long long>(row) * G.ldo + col0, w, col0, G.N, v8);
       }
     }

@@ -548,7 +548,7 @@ lora_status_t check_mlp(int64_t M, int64_t h, int64_t i, int r, float s, int act
   check_size(h, st);
   check_size(i, st);
   if (st != LORA_OK) return st;
-  if (act != LORA_ACT_SWIGLU && act != LORA_ACT_GEGLU_TANH) return LORA_ERR_INVALID_ARG;
+  if (act != LORA_ACT_SWIGLU && act != LORA_ACT_GEGLU_TANH && act != LORA_ACT_GEGLU_ERF) return LORA_ERR_INVALID_ARG;
   if (2 * r > 256) return LORA_ERR_UNSUPPORTED;
   if (h % 8 || i % 8) return LORA_ERR_ALIGNMENT;
   return LORA_OK;
@@ -865,8 +865,8 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
                                            void* yo, const void* bias_qkv, void* saved, void* ws,
                                            size_t ws_bytes, cudaStream_t stream) {
   LGB_TRY(check_qkvo(M, h, n_q, n_kv, r, s));
-  if (bias_qkv != nullptr) return LORA_ERR_UNSUPPORTED;
   if (!ws || (!x && !o_in)) return LORA_ERR_INVALID_ARG;
+  if (bias_qkv != nullptr && !aligned(bias_qkv, 16)) return LORA_ERR_ALIGNMENT;
   if (x && ((M > 0 && (!yq || !yk || !yv)) || !lin_ok(q) || !lin_ok(k) || !lin_ok(v))) return LORA_ERR_INVALID_ARG;
   if (o_in && ((M > 0 && !yo) || !lin_ok(o))) return LORA_ERR_INVALID_ARG;
   if (!aligned(ws, 256) || (saved && !aligned(saved, 256))) return LORA_ERR_ALIGNMENT;
@@ -929,6 +929,7 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
       GemmPlan::seg(G, at, g.b_kmajor(bfs[p], ns[p], kfq, kfq, g.b_rows_full()), -1, kfq, (p + 1) * r);
       G.out0 = ys[p];
       G.ldo = ns[p];
+      if (bias_qkv != nullptr) G.in0 = static_cast<const bf16*>(bias_qkv) + (p == 0 ? 0 : n_q + (p - 1) * n_kv);
     }
     g.p.status = status;
     g.finish();
@@ -1084,7 +1085,7 @@ extern "C" const char* lora_status_string(lora_status_t status) {
     case LORA_OK: return "ok";
     case LORA_ERR_INVALID_ARG: return "invalid argument";
     case LORA_ERR_ALIGNMENT: return "alignment: pointers 16-byte (ws/saved 256-byte), feature sizes multiples of 8";
-    case LORA_ERR_UNSUPPORTED: return "unsupported: rank too large for the fold, or a bias was given";
+    case LORA_ERR_UNSUPPORTED: return "unsupported: rank too large for the fold";
     case LORA_ERR_WORKSPACE: return "workspace smaller than the size query";
     case LORA_ERR_CUDA: return "CUDA runtime or launch failure";
     case LORA_ERR_TIMEOUT: return "a kernel's bounded wait expired";

@@ -86,6 +86,7 @@ def _mlp_fwd(L, M=64, h=128, i=344, r=8, s=2.0, act=0, x=ALIGNED, y=ALIGNED, ws=
     (dict(s=float("nan")), 1),             # non-finite scale
     (dict(s=float("inf")), 1),
     (dict(act=7), 1),                      # unknown activation
+    (dict(act=3), 1),
     (dict(h=130), 2),                      # feature size not a multiple of 8
     (dict(x=ALIGNED + 2), 2),              # misaligned activation
     (dict(ws=ALIGNED + 16), 2),            # workspace not 256-byte aligned
@@ -104,12 +105,12 @@ def test_mlp_forward_zero_tokens_is_a_no_op(L):
     assert L.lora_launch_count() == before
 
 
-def test_qkvo_rejects_bias_and_large_rank(L):
+def test_qkvo_rejects_misaligned_bias_and_large_rank(L):
     lin = _lin(L)
     ws = L.lora_qkvo_workspace_bytes(64, 256, 256, 128, 8)
     args = lambda r, bias: (64, 256, 256, 128, r, 2.0, ALIGNED, lin, lin, lin, ALIGNED, ALIGNED, ALIGNED,  # noqa
                             None, lin, None, bias, None, ALIGNED, ws, None)
-    assert L.lora_qkvo_forward(*args(8, ALIGNED)) == 3
+    assert L.lora_qkvo_forward(*args(8, ALIGNED + 2)) == 2
     assert L.lora_qkvo_forward(*args(86, None)) == 3
     # both halves skipped: nothing to do is an argument error
     assert L.lora_qkvo_forward(64, 256, 256, 128, 8, 2.0, None, lin, lin, lin, None, None, None,

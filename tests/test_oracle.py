@@ -38,12 +38,24 @@ def test_gelu_tanh_matches_torch_library():
     np.testing.assert_allclose(oracle.gelu_tanh(GRID), ref, rtol=1e-13, atol=1e-14)
 
 
+def test_gelu_erf_matches_torch_library():
+    ref = F.gelu(torch.from_numpy(GRID), approximate="none").numpy()
+    np.testing.assert_allclose(oracle.gelu_erf(GRID), ref, rtol=1e-13, atol=1e-14)
+
+
+def test_gelu_erf_closed_values():
+    # Phi(1) = (1 + erf(1/sqrt 2)) / 2; gelu(1) = Phi(1)
+    assert math.isclose(oracle.gelu_erf(np.array([1.0]))[0], 0.5 * (1.0 + math.erf(1.0 / math.sqrt(2.0))),
+                        rel_tol=1e-15)
+    assert oracle.gelu_erf(np.array([0.0]))[0] == 0.0
+
+
 def test_activation_closed_values_and_asymptotes():
     assert oracle.silu(np.array([0.0]))[0] == 0.0
     assert oracle.gelu_tanh(np.array([0.0]))[0] == 0.0
     assert math.isclose(oracle.silu(np.array([1.0]))[0], 1.0 / (1.0 + math.exp(-1.0)), rel_tol=1e-15)
     # silu(g) -> g for g -> +inf, -> 0 for g -> -inf; the same for gelu
-    for f in (oracle.silu, oracle.gelu_tanh):
+    for f in (oracle.silu, oracle.gelu_tanh, oracle.gelu_erf):
         big = np.array([40.0])
         assert abs(f(big)[0] - 40.0) < 1e-12
         assert abs(f(-big)[0]) < 1e-12
@@ -211,7 +223,10 @@ def base_mlp_error(kind, mod=olora):
     t = {k: torch.from_numpy(v) for k, v in p.items()}
     x = t["x"].clone().requires_grad_(True)
     gate = x @ t["Wg"].T
-    a = F.silu(gate) if kind == "swiglu" else F.gelu(gate, approximate="tanh")
+    if kind == "swiglu":
+        a = F.silu(gate)
+    else:
+        a = F.gelu(gate, approximate="tanh" if kind == "geglu_tanh" else "none")
     y = (a * (x @ t["Wu"].T)) @ t["Wd"].T
     (y * torch.from_numpy(dy)).sum().backward()
     b = mod.mlp_backward(*args, dy)
@@ -316,3 +331,16 @@ def test_planted_forward_mistakes_are_caught(mutant, kind):
     m = _Mutant(**mutant)
     err, _ = base_mlp_error(kind, mod=m)
     assert err > 1e-4
+
+
+def test_frozen_bias_adds_a_row_vector_and_leaves_grads():
+    """A frozen Q/K/V bias shifts each output row by exactly the bias and changes no
+    gradient."""
+    p, dys = _qkvo_params()
+    rng = np.random.default_rng(5)
+    bias = (rng.standard_normal(8), rng.standard_normal(4), rng.standard_normal(4))
+    a = oracle.qkvo_forward(p["x"], p["q"], p["k"], p["v"], p["o_in"], p["o"], 2.0)
+    b = oracle.qkvo_forward(p["x"], p["q"], p["k"], p["v"], p["o_in"], p["o"], 2.0, bias=bias)
+    for j, n in enumerate(("q", "k", "v")):
+        np.testing.assert_allclose(b[n] - a[n], np.broadcast_to(bias[j], a[n].shape), rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(a["o"], b["o"])

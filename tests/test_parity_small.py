@@ -1,9 +1,10 @@
 """GPU path vs the CPU float64 oracle on small and ragged problems (seconds each).
 
 Sizes span several 128 x 256 tiles with ragged tails in M, N and K, ranks that
-pad the folded K-segment (r = 1, 5, 8) and ranks that fill it (r = 64), both
-activations, and the degenerate cases: one token, zero tokens, B = 0 (the base
-projections alone, adapter gradients exactly zero) and s = 0.
+pad the folded K-segment (r = 1, 5, 8) and ranks that fill it (r = 64, 128), the
+three activations (SwiGLU, tanh-GeGLU, exact GeGLU), frozen Q/K/V biases, and the
+degenerate cases: one token, B = 0 (the base projections alone, adapter gradients
+exactly zero) and s = 0.
 """
 
 import numpy as np
@@ -62,7 +63,7 @@ def _mlp_inputs(cfg, seed=0, **zero):
     return {k: t.to(DEV) for k, t in ins.items()}, to_f64_dict(ins)
 
 
-@pytest.mark.parametrize("act", ["swiglu", "geglu_tanh"])
+@pytest.mark.parametrize("act", ["swiglu", "geglu_tanh", "geglu_erf"])
 @pytest.mark.parametrize("M", [64, 1, 127, 129])
 def test_mlp_tiny(lib, act, M):
     cfg = synth.MLP_CONFIGS["tiny"].replace(act=act, M=M)
@@ -157,3 +158,41 @@ def test_deterministic(lib):
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
     for k in MLP_GRADS:
         assert torch.equal(g1[k].view(torch.int16), g2[k].view(torch.int16)), k
+
+
+def test_mlp_geglu_erf_gemma_like(lib):
+    """Exact-erf GeGLU (the Gemma row of the activation table) at a Gemma-like width."""
+    cfg = synth.MLP_CONFIGS["gemma7b"].replace(M=512, h=768, i=3072, act="geglu_erf")
+    t, v = _mlp_inputs(cfg, seed=4)
+    y, g = mlp_gpu(lib, t, cfg)
+    f, b = mlp_oracle(v, cfg)
+    parity("y", y, f["y"])
+    for k in MLP_GRADS:
+        parity(k, g[k], b[k])
+
+
+def test_qkvo_frozen_bias(lib):
+    """Frozen base-layer q/k/v biases are added in the projection epilogue; the
+    backward is unchanged."""
+    cfg = synth.QKVO_CONFIGS["gqa7b"].replace(M=300, h=256, heads_q=4, heads_kv=2, head_dim=64)
+    ins = synth.make_qkvo_inputs(cfg, seed=6)
+    t = {k: x.to(DEV) for k, x in ins.items()}
+    nb = cfg.n_q + 2 * cfg.n_kv
+    bias = _randn((nb,), 1.0, 99).to(DEV)
+    lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
+    out, saved = lib.qkvo_forward(t["x"], lin("q"), lin("k"), lin("v"), t["o_in"], lin("o"), cfg.s, bias=bias)
+    g = lib.qkvo_backward(t["x"], lin("q"), lin("k"), lin("v"), t["o_in"], lin("o"), cfg.s, saved,
+                          t["dy_q"], t["dy_k"], t["dy_v"], t["dy_o"])
+    torch.cuda.synchronize()
+    assert lib.poll_status() == 0
+    v = to_f64_dict(ins)
+    bv = f64(bias)
+    bsplit = (bv[:cfg.n_q], bv[cfg.n_q:cfg.n_q + cfg.n_kv], bv[cfg.n_q + cfg.n_kv:])
+    L = lambda n: (v["W_" + n], v["A_" + n], v["B_" + n])  # noqa: E731
+    f = oracle.qkvo_forward(v["x"], L("q"), L("k"), L("v"), v["o_in"], L("o"), cfg.s, bias=bsplit)
+    b = oracle.qkvo_backward(v["x"], L("q"), L("k"), L("v"), v["o_in"], L("o"), cfg.s,
+                             v["dy_q"], v["dy_k"], v["dy_v"], v["dy_o"])
+    for k in ("q", "k", "v", "o"):
+        parity(k, out[k], f[k])
+    for k in b:
+        parity(k, g[k], b[k])
