@@ -303,6 +303,8 @@ def run_ours(args):
     dist_init("nccl")
     lib.load()
     cfg = synth.MLP_CONFIGS[args.workload]
+    if args.act:
+        cfg = cfg.replace(act=args.act)
     M, h, i, r = cfg.M, cfg.h, cfg.i, cfg.r
     t = synth.make_mlp_inputs(cfg, seed=0, device=device)
     lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
@@ -317,9 +319,17 @@ def run_ours(args):
              "dA_down": e(r, i), "dB_down": e(h, r)}
     x, dy = t["x"], t["dy"]
 
+    n_ex = args.per_example
+    if n_ex:
+        ws = torch.zeros(max(ws_b, lib.load().lora_mlp_per_example_workspace_bytes(M, h, i, r, n_ex)),
+                         dtype=torch.uint8, device=device)
+
     def step():
         lib.mlp_forward(x, gate, up, down, cfg.s, cfg.act, y=y, saved=saved, ws=ws)
-        lib.mlp_backward(x, gate, up, down, cfg.s, cfg.act, saved, dy, dx=dx, grads=grads, ws=ws)
+        if n_ex:
+            lib.mlp_backward_per_example(x, gate, up, down, cfg.s, cfg.act, saved, dy, n_ex, ws=ws)
+        else:
+            lib.mlp_backward(x, gate, up, down, cfg.s, cfg.act, saved, dy, dx=dx, grads=grads, ws=ws)
 
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
@@ -357,7 +367,7 @@ def run_ours(args):
 
     # ---- end to end through host buffers: H2D of x, dy; D2H of y, dx and the grads
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not n_ex:
         xh = x.cpu().pin_memory()
         dyh = dy.cpu().pin_memory()
         yh = torch.empty(M, h, dtype=torch.bfloat16).pin_memory()
@@ -399,7 +409,9 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded generator: x, dy ~ N(0,1), W ~ N(0,1/fan_in), A ~ U(+-1/sqrt(fan_in)), "
                 "B ~ N(0,0.02))",
-        "config": {"workload": workload_name(cfg), "parallelism": "replicas" if world > 1 else "single GPU",
+        "config": {"workload": workload_name(cfg) + (f", per-example adapter gradients of {n_ex} examples"
+                                                      if n_ex else ""),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (weights 352 MB + activations per step)"},
         "tflops": tflops, "pct_of_peak": 100.0 * tflops / peak, "peak_tflops": peak,
         "peak_source": f"{peak_src} bf16_tflops_sustained",
@@ -423,6 +435,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--act", choices=("swiglu", "geglu_tanh", "geglu_erf"), default=None,
+                    help="override the workload's activation")
+    ap.add_argument("--per-example", type=int, default=0, metavar="N",
+                    help="backward with per-example adapter gradients of N examples (DP-SGD)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -149,6 +149,23 @@ lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int r, float s,
                                 lora_grads_t d_down, void* ws, size_t ws_bytes,
                                 cudaStream_t stream);
 
+/* Per-example adapter gradients, for DP-SGD (the opake use case: per-example
+ * gradients by vmap(grad) before clipping; "Model Patches and Kernels").  The M tokens
+ * are n_examples examples of seq = M / n_examples consecutive tokens (M must be a
+ * multiple of n_examples; token t belongs to example t / seq).  Writes dx as
+ * lora_mlp_backward does, and for each adapter the gradient of every example on its
+ * own: d_*.dA [n_examples x r x in], d_*.dB [n_examples x out x r] (bf16, example-major).
+ * sq_norms (NULL or float [n_examples]) receives each example's squared L2 norm over
+ * all six adapter gradients, summed from the bf16 results in a fixed order.  ws must
+ * hold lora_mlp_per_example_workspace_bytes(M, h, i, r, n_examples). */
+size_t lora_mlp_per_example_workspace_bytes(int64_t M, int64_t h, int64_t i, int r, int64_t n_examples);
+lora_status_t lora_mlp_backward_per_example(int64_t M, int64_t h, int64_t i, int r, float s, lora_act_t act,
+                                            int64_t n_examples, const void* x, lora_linear_t gate,
+                                            lora_linear_t up, lora_linear_t down, const void* saved,
+                                            const void* dy, void* dx, lora_grads_t d_gate,
+                                            lora_grads_t d_up, lora_grads_t d_down, float* sq_norms,
+                                            void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- Q/K/V + O
  * q = (1)(x; q) [M x n_q], k, v = (1)(x; k or v) [M x n_kv] ("opake_lora_qkv"), and
  * yo = (1)(o_in; o) [M x h] with W_o [h x n_q] ("original_apply_o").  Attention runs

@@ -167,6 +167,29 @@ def mlp_backward(x, Wg, Ag, Bg, Wu, Au, Bu, Wd, Ad, Bd, s, kind, dy):
             "dB_up": dBu, "dA_down": dAd, "dB_down": dBd, "dg": dg, "du": du, "dh": dh}
 
 
+def mlp_backward_per_example(x, Wg, Ag, Bg, Wu, Au, Bu, Wd, Ad, Bd, s, kind, dy, n_examples):
+    """Per-example adapter gradients for DP-SGD ("Model Patches and Kernels": per-example
+    gradients by vmap(grad) over the examples of a batch).  The block acts on each
+    token independently, so example e's gradient is the backward over its own
+    tokens [e seq, (e+1) seq) alone.  Returns dict(dx, dA_* [n, r, in], dB_* [n, out, r],
+    sq_norms [n]); sq_norms[e] = sum of squares of example e's six adapter gradients."""
+    M = x.shape[0]
+    seq = M // n_examples
+    keys = ("dA_gate", "dB_gate", "dA_up", "dB_up", "dA_down", "dB_down")
+    res = {k: [] for k in keys}
+    dx = []
+    for e in range(n_examples):
+        sl = slice(e * seq, (e + 1) * seq)
+        b = mlp_backward(x[sl], Wg, Ag, Bg, Wu, Au, Bu, Wd, Ad, Bd, s, kind, dy[sl])
+        dx.append(b["dx"])
+        for k in keys:
+            res[k].append(b[k])
+    out = {k: np.stack(v) for k, v in res.items()}
+    out["dx"] = np.concatenate(dx, axis=0)
+    out["sq_norms"] = sum(np.sum(out[k] ** 2, axis=tuple(range(1, out[k].ndim))) for k in keys)
+    return out
+
+
 # --------------------------------------------------------------------------------
 # Attention projections -- row opake_lora_qkv (q, k, v share the input x) and the
 # output projection (original_apply_qkv / original_apply_o in the axolotl API).

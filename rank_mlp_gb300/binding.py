@@ -58,6 +58,10 @@ _SIGS = {
                                 _VP, _VP, _VP, _SZ, _VP]),
     "lora_mlp_backward": (_INT, [_I64, _I64, _I64, _INT, _F32, _INT, _VP, LoraLinear, LoraLinear, LoraLinear,
                                  _VP, _VP, _VP, LoraGrads, LoraGrads, LoraGrads, _VP, _SZ, _VP]),
+    "lora_mlp_per_example_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT, _I64]),
+    "lora_mlp_backward_per_example": (_INT, [_I64, _I64, _I64, _INT, _F32, _INT, _I64, _VP, LoraLinear, LoraLinear,
+                                             LoraLinear, _VP, _VP, _VP, LoraGrads, LoraGrads, LoraGrads, _VP, _VP,
+                                             _SZ, _VP]),
     "lora_qkvo_saved_bytes": (_SZ, [_I64, _I64, _I64, _I64, _INT]),
     "lora_qkvo_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64, _INT]),
     "lora_qkvo_forward": (_INT, [_I64, _I64, _I64, _I64, _INT, _F32, _VP, LoraLinear, LoraLinear, LoraLinear,
@@ -255,6 +259,29 @@ def mlp_backward(x, gate, up, down, s, act, saved, dy, *, dx=None, grads=None, w
                                  _lin(down, "down"), saved.data_ptr(), _dev(dy, "dy"), _dev(out["dx"], "dx"),
                                  g("gate"), g("up"), g("down"), ws.data_ptr(), ws.numel(), _stream(dev)),
            "lora_mlp_backward")
+    return out
+
+
+def mlp_backward_per_example(x, gate, up, down, s, act, saved, dy, n_examples, *, norms=True, ws=None):
+    """Per-example adapter gradients (DP-SGD): dict(dx, dA_gate [n, r, h], dB_gate
+    [n, i, r], ..., sq_norms [n] float32 or None)."""
+    lib = load()
+    M, h = x.shape
+    i, r = gate[0].shape[0], gate[1].shape[0]
+    n = int(n_examples)
+    dev = x.device
+    e = lambda *sh: torch.empty(*sh, dtype=torch.bfloat16, device=dev)  # noqa: E731
+    out = {"dx": e(M, h), "dA_gate": e(n, r, h), "dB_gate": e(n, i, r), "dA_up": e(n, r, h), "dB_up": e(n, i, r),
+           "dA_down": e(n, r, i), "dB_down": e(n, h, r),
+           "sq_norms": torch.empty(n, dtype=torch.float32, device=dev) if norms else None}
+    need = lib.lora_mlp_per_example_workspace_bytes(M, h, i, r, n)
+    ws = workspace(need, dev) if ws is None else ws
+    g = lambda k: LoraGrads(_dev(out["dA_" + k], "dA_" + k), _dev(out["dB_" + k], "dB_" + k))  # noqa: E731
+    _check(lib.lora_mlp_backward_per_example(
+        M, h, i, r, s, ACT[act], n, _dev(x, "x"), _lin(gate, "gate"), _lin(up, "up"), _lin(down, "down"),
+        saved.data_ptr(), _dev(dy, "dy"), _dev(out["dx"], "dx"), g("gate"), g("up"), g("down"),
+        None if out["sq_norms"] is None else out["sq_norms"].data_ptr(), ws.data_ptr(), ws.numel(),
+        _stream(dev)), "lora_mlp_backward_per_example")
     return out
 
 

@@ -46,13 +46,26 @@ struct RedOut {
   int col0, ncols;    // columns [col0, col0 + ncols) of the slab
   long long ld;
   int trans;          // 0: dst[m * ld + c];  1: dst[c * ld + m]
+  long long split_stride;  // per-split outputs: elements between consecutive splits' results
 };
 
 struct RedParams {
   int splits;
   float scale;
+  int per_split;      // 0: out = scale * sum over splits; 1: split k -> dst + k * split_stride
   int nout;
   RedOut out[kMaxRedOuts];
+};
+
+// Per-example squared norms: for each example e (one block each), the sum of squares
+// of its slice of every listed tensor.  Fixed summation order (deterministic).
+constexpr int kMaxNormTensors = 8;
+
+struct NormParams {
+  const __nv_bfloat16* src[kMaxNormTensors];
+  long long count[kMaxNormTensors];     // elements per example
+  int ntensors;
+  float* out;                           // [examples]
 };
 
 }  // namespace lgb

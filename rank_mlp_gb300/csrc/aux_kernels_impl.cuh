@@ -40,11 +40,35 @@ __global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ Red
       c = static_cast<int>(idx - static_cast<long long>(m) * O.ncols);
     }
     const float* src = O.part + static_cast<long long>(m) * O.width + O.col0 + c;
-    float s = 0.0f;
-    for (int k = 0; k < p.splits; ++k) s += src[k * slab];
     const long long d = O.trans ? static_cast<long long>(c) * O.ld + m : static_cast<long long>(m) * O.ld + c;
-    O.dst[d] = __float2bfloat16_rn(p.scale * s);
+    if (p.per_split) {
+      for (int k = 0; k < p.splits; ++k) O.dst[k * O.split_stride + d] = __float2bfloat16_rn(p.scale * src[k * slab]);
+    } else {
+      float s = 0.0f;
+      for (int k = 0; k < p.splits; ++k) s += src[k * slab];
+      O.dst[d] = __float2bfloat16_rn(p.scale * s);
+    }
   }
+}
+
+__global__ void __launch_bounds__(256) norms_kernel(const __grid_constant__ NormParams p) {
+  const int e = blockIdx.x;
+  float acc = 0.0f;
+  for (int t = 0; t < p.ntensors; ++t) {
+    const __nv_bfloat16* src = p.src[t] + static_cast<long long>(e) * p.count[t];
+    for (long long j = threadIdx.x; j < p.count[t]; j += 256) {
+      const float v = __bfloat162float(src[j]);
+      acc += v * v;
+    }
+  }
+  __shared__ float red[256];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.out[e] = red[0];
 }
 
 }  // namespace lgb

@@ -43,6 +43,8 @@ struct SegDesc {
 struct GroupDesc {
   int M, N;                  // logical output extent
   int tiles_m, tiles_n, splits;
+  int per_plane;             // 0: the splits share K out (split-K); 1: split s owns plane s of
+                             // 3-D maps {x, k, plane} and runs the whole K of that plane
   int unit_begin;            // first work unit of this group
   int nseg, kb_total;
   SegDesc seg[kMaxSegs];
@@ -101,8 +103,13 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   U.tm = rem / nb;
   U.tn = b * band + rem % nb;
   U.split = split;
-  U.kb0 = static_cast<int>(static_cast<long long>(G.kb_total) * split / G.splits);
-  U.kb1 = static_cast<int>(static_cast<long long>(G.kb_total) * (split + 1) / G.splits);
+  if (G.per_plane) {
+    U.kb0 = 0;
+    U.kb1 = G.kb_total;
+  } else {
+    U.kb0 = static_cast<int>(static_cast<long long>(G.kb_total) * split / G.splits);
+    U.kb1 = static_cast<int>(static_cast<long long>(G.kb_total) * (split + 1) / G.splits);
+  }
   return U;
 }
 
@@ -435,22 +442,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             armed[stage] = static_cast<int>(phase);
             const uint32_t sa = sbase + stage * C::kStageBytes;
             const uint32_t sb = sa + C::kABytes;
-            if (!A_MN) {
-              tma_load_2d(sa, ma, fb, kc, U.tm * kBM);
-            } else {
-              tma_load_2d(sa, ma, fb, U.tm * kBM, kc);
-              tma_load_2d(sa + 8192u, ma, fb, U.tm * kBM + 64, kc);
-            }
-            if (!B_MN) {
-              if (b1 >= 0) {
-                tma_load_2d(sb, mb0, fb, kc, U.tn * (BN / 2));
-                tma_load_2d(sb + (BN / 2) * 128u, mb1, fb, kc, U.tn * (BN / 2));
-              } else {
-                tma_load_2d(sb, mb0, fb, kc, U.tn * BN);
-              }
-            } else {
+            if (A_MN && B_MN && G.per_plane) {
+              // reductions over one plane (one example's tokens) of 3-D maps
+              tma_load_3d(sa, ma, fb, U.tm * kBM, kc, U.split);
+              tma_load_3d(sa + 8192u, ma, fb, U.tm * kBM + 64, kc, U.split);
 #pragma unroll
-              for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * 8192u, mb0, fb, U.tn * BN + c * 64, kc);
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_3d(sb + c * 8192u, mb0, fb, U.tn * BN + c * 64, kc, U.split);
+            } else {
+              if (!A_MN) {
+                tma_load_2d(sa, ma, fb, kc, U.tm * kBM);
+              } else {
+                tma_load_2d(sa, ma, fb, U.tm * kBM, kc);
+                tma_load_2d(sa + 8192u, ma, fb, U.tm * kBM + 64, kc);
+              }
+              if (!B_MN) {
+                if (b1 >= 0) {
+                  tma_load_2d(sb, mb0, fb, kc, U.tn * (BN / 2));
+                  tma_load_2d(sb + (BN / 2) * 128u, mb1, fb, kc, U.tn * (BN / 2));
+                } else {
+                  tma_load_2d(sb, mb0, fb, kc, U.tn * BN);
+                }
+              } else {
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c) tma_load_2d(sb + c * 8192u, mb0, fb, U.tn * BN + c * 64, kc);
+              }
             }
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }

@@ -45,7 +45,10 @@ int tc_smem_bytes(int variant);
 int num_sms();
 bool encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
                 uint32_t box_inner, uint32_t box_outer);
+bool encode_map_planes(CUtensorMap* m, const void* base, uint64_t inner, uint64_t d1, uint64_t d2, uint64_t ld,
+                       uint32_t box_inner, uint32_t box_d1);
 lora_status_t launch_gemm(int variant, const TcParams& p, int kind, cudaStream_t st);
+lora_status_t launch_norms(const NormParams& p, int examples, cudaStream_t st);
 lora_status_t launch_pack(const PackParams& p, cudaStream_t st);
 lora_status_t launch_reduce(const RedParams& p, cudaStream_t st);
 
@@ -148,6 +151,19 @@ struct GemmPlan {
   // B operand, MN-major: source [K x N] (N contiguous).
   int b_mnmajor(const void* base, int64_t N, int64_t K, int64_t ld) {
     return add_map(base, N, K, ld, 64, 64);
+  }
+  // MN-major operands read as planes: source [planes * K x rows], plane p = rows
+  // [p K, (p+1) K); 3-D view {rows, K, planes} (per-example token reductions).
+  int add_map_planes(const void* base, int64_t rows, int64_t K, int64_t planes, int64_t ld) {
+    if (!ok || p.nmaps >= kMaxMaps) { ok = false; return -1; }
+    if (!encode_map_planes(&p.maps[p.nmaps], base, rows, K, planes, ld, 64, 64)) { ok = false; return -1; }
+    return p.nmaps++;
+  }
+  int a_mnmajor_planes(const void* base, int64_t rows, int64_t K, int64_t planes, int64_t ld) {
+    return add_map_planes(base, rows, K, planes, ld);
+  }
+  int b_mnmajor_planes(const void* base, int64_t N, int64_t K, int64_t planes, int64_t ld) {
+    return add_map_planes(base, N, K, planes, ld);
   }
 
   GroupDesc& group(int M, int N, int epi, bool split_n_tile) {

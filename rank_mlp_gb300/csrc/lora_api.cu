@@ -50,6 +50,21 @@ bool encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map {inner, d1, d2} with row stride ld (elements) and plane stride
+// ld * d1; box {box_inner, box_d1, 1}.
+bool encode_map_planes(CUtensorMap* m, const void* base, uint64_t inner, uint64_t d1, uint64_t d2, uint64_t ld,
+                       uint32_t box_inner, uint32_t box_d1) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr || inner == 0 || d1 == 0 || d2 == 0) return false;
+  const cuuint64_t dims[3] = {inner, d1, d2};
+  const cuuint64_t strides[2] = {ld * 2, ld * 2 * d1};
+  const cuuint32_t box[3] = {box_inner, box_d1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- counters, trace
 
 static std::atomic<uint64_t> g_launches{0};
@@ -106,6 +121,17 @@ lora_status_t launch_pack(const PackParams& p, cudaStream_t st) {
   gx = gx > 1024 ? 1024 : gx;
   const int slot = trace_begin(LORA_KIND_PACK, st);
   pack_kernel<<<dim3(static_cast<unsigned>(gx), p.njob), 256, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  trace_end(slot, st);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return LORA_OK;
+}
+
+lora_status_t launch_norms(const NormParams& p, int examples, cudaStream_t st) {
+  if (examples <= 0) return LORA_OK;
+  const int slot = trace_begin(LORA_KIND_REDUCE, st);
+  norms_kernel<<<examples, 256, 0, st>>>(p);
   cudaError_t e = cudaGetLastError();
   trace_end(slot, st);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
@@ -231,22 +257,31 @@ struct GradJob {
   void* dst;
   int trans;          // 1: dst is [r x f] (dA), 0: dst is [f x r] (dB)
 };
-static int64_t token_grad_part(int64_t M, int kf, const int64_t* fs, int n) {
+// f32 slab elements of the token reductions of n products (fs[j] features each).
+// n_ex > 0: per-example mode, one slab per example.
+static int64_t token_grad_part(int64_t M, int kf, const int64_t* fs, int n, int64_t n_ex = 0) {
   const int bn = skinny_bn(kf);
+  const int splits = n_ex > 0 ? static_cast<int>(n_ex) : max_splits(ceil_div(M, kBK));
   int64_t tot = 0;
-  for (int j = 0; j < n; ++j) tot += round_up(partial_elems(fs[j], kf, bn, max_splits(ceil_div(M, kBK))), 64);
+  for (int j = 0; j < n; ++j) tot += round_up(partial_elems(fs[j], kf, bn, splits), 64);
   return tot;
 }
 // Jobs with the same Q share one slab (several rank slots out of one product).
+// n_ex == 0: the sums over all M tokens.  n_ex > 0: one result per example (example e
+// = tokens [e seq, (e+1) seq), seq = M / n_ex), each written at dst + e * r * f; the
+// products read 3-D views {features, seq, examples} so no k-block straddles two
+// examples (rows past seq read as zero).
 static lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* T, const GradJob* jobs, int njobs,
-                                 float* part, unsigned* status, cudaStream_t st) {
+                                 float* part, unsigned* status, cudaStream_t st, int64_t n_ex = 0) {
   const int variant = skinny_mnmn(kf);
   GemmPlan g(variant);
-  const int tmap = g.b_mnmajor(T, kf, M, kf);
+  const int64_t seq = n_ex > 0 ? M / n_ex : M;
+  const int tmap = n_ex > 0 ? g.b_mnmajor_planes(T, kf, seq, n_ex, kf) : g.b_mnmajor(T, kf, M, kf);
   const void* qs[kMaxGroups];
   int nq = 0, group_of[kMaxRedOuts];
   float* parts[kMaxGroups];
   float* cur = part;
+  const int slab_splits = n_ex > 0 ? static_cast<int>(n_ex) : max_splits(ceil_div(M, kBK));
   for (int j = 0; j < njobs; ++j) {
     int gi = -1;
     for (int q = 0; q < nq; ++q)
@@ -255,14 +290,20 @@ static lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* 
       gi = nq++;
       qs[gi] = jobs[j].Q;
       const int64_t tiles = ceil_div(jobs[j].f, kBM) * ceil_div(kf, g.bn);
-      const int splits = choose_splits(tiles, ceil_div(M, kBK), num_sms());
       GroupDesc& G = g.group(static_cast<int>(jobs[j].f), kf, EPI_PARTIAL, false);
-      G.splits = splits;
-      const int a = g.a_mnmajor(jobs[j].Q, jobs[j].f, M, jobs[j].f);
-      GemmPlan::seg(G, a, tmap, -1, M, M);
+      if (n_ex > 0) {
+        G.splits = static_cast<int>(n_ex);
+        G.per_plane = 1;
+        const int a = g.a_mnmajor_planes(jobs[j].Q, jobs[j].f, seq, n_ex, jobs[j].f);
+        GemmPlan::seg(G, a, tmap, -1, seq, seq);
+      } else {
+        G.splits = choose_splits(tiles, ceil_div(M, kBK), num_sms());
+        const int a = g.a_mnmajor(jobs[j].Q, jobs[j].f, M, jobs[j].f);
+        GemmPlan::seg(G, a, tmap, -1, M, M);
+      }
       G.part = cur;
       parts[gi] = cur;
-      cur += round_up(partial_elems(jobs[j].f, kf, g.bn, max_splits(ceil_div(M, kBK))), 64);
+      cur += round_up(partial_elems(jobs[j].f, kf, g.bn, slab_splits), 64);
     }
     group_of[j] = gi;
   }
@@ -279,6 +320,7 @@ static lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* 
     std::memset(static_cast<void*>(&rp), 0, sizeof(rp));
     rp.splits = sp;
     rp.scale = s;
+    rp.per_split = n_ex > 0 ? 1 : 0;
     for (int j = j0; j < njobs; ++j) {
       if (done[j] || g.p.grp[group_of[j]].splits != sp) continue;
       done[j] = true;
@@ -292,6 +334,7 @@ static lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* 
       o.ncols = r;
       o.ld = jobs[j].trans ? jobs[j].f : r;
       o.trans = jobs[j].trans;
+      o.split_stride = static_cast<long long>(r) * jobs[j].f;
     }
     LGB_TRY(launch_reduce(rp, st));
   }
@@ -487,7 +530,8 @@ struct MlpLayout {
   size_t off_g, off_u, off_h, off_tgu, off_td;
 };
 
-MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r) {
+// n_ex > 0: workspace of the per-example backward (one reduction slab per example).
+MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r, int64_t n_ex = 0) {
   MlpLayout L;
   L.kfg = fold_width(2, r);
   L.kfd = fold_width(1, r);
@@ -523,10 +567,10 @@ MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r) {
     int64_t p = rank_projection_part(M, kfd, ceil_div(h, kBK));
     const int64_t cand[] = {
         rank_projection_part(M, kfg, 2 * ceil_div(i, kBK)),
-        token_grad_part(M, kfd, &h, 1),
-        token_grad_part(M, kfd, &i, 1),
-        [&] { const int64_t f2[2] = {i, i}; return token_grad_part(M, kfg, f2, 2); }(),
-        token_grad_part(M, kfg, &h, 1)};
+        token_grad_part(M, kfd, &h, 1, n_ex),
+        token_grad_part(M, kfd, &i, 1, n_ex),
+        [&] { const int64_t f2[2] = {i, i}; return token_grad_part(M, kfg, f2, 2, n_ex); }(),
+        token_grad_part(M, kfg, &h, 1, n_ex)};
     for (int64_t v : cand) p = v > p ? v : p;
     c.take_n<float>(p);
     L.ws_bwd = c.off;
@@ -659,11 +703,14 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
   return launch_gemm(kBigKK, g.p, LORA_KIND_PROJ, stream);
 }
 
-extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int r, float s, lora_act_t act,
-                                           const void* x, lora_linear_t gate, lora_linear_t up,
-                                           lora_linear_t down, const void* saved, const void* dy, void* dx,
-                                           lora_grads_t d_gate, lora_grads_t d_up, lora_grads_t d_down, void* ws,
-                                           size_t ws_bytes, cudaStream_t stream) {
+// Backward of the gated MLP.  n_ex == 0: dA/dB summed over all tokens.  n_ex > 0:
+// dA/dB per example (n_ex examples of M / n_ex consecutive tokens, written at
+// example stride), plus their squared norms into sq_norms when it is not NULL.
+static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, float s, lora_act_t act,
+                                       int64_t n_ex, const void* x, lora_linear_t gate, lora_linear_t up,
+                                       lora_linear_t down, const void* saved, const void* dy, void* dx,
+                                       lora_grads_t d_gate, lora_grads_t d_up, lora_grads_t d_down, float* sq_norms,
+                                       void* ws, size_t ws_bytes, cudaStream_t stream) {
   LGB_TRY(check_mlp(M, h, i, r, s, static_cast<int>(act)));
   if ((M > 0 && (!x || !dy || !dx)) || !saved || !ws || !lin_ok(gate) || !lin_ok(up) || !lin_ok(down) || !d_gate.dA ||
       !d_gate.dB || !d_up.dA || !d_up.dB || !d_down.dA || !d_down.dB)
@@ -673,10 +720,15 @@ extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int 
       !aligned(d_gate.dB, 2) || !aligned(d_up.dA, 2) || !aligned(d_up.dB, 2) || !aligned(d_down.dA, 2) ||
       !aligned(d_down.dB, 2))
     return LORA_ERR_ALIGNMENT;
-  const MlpLayout L = mlp_layout(M, h, i, r);
+  if (n_ex < 0 || (n_ex > 0 && M % n_ex != 0)) return LORA_ERR_INVALID_ARG;
+  if (sq_norms != nullptr && !aligned(sq_norms, 4)) return LORA_ERR_ALIGNMENT;
+  const MlpLayout L = mlp_layout(M, h, i, r, n_ex);
   if (ws_bytes < L.ws_bwd) return LORA_ERR_WORKSPACE;
   if (M == 0) {
-    const size_t ah = sizeof(bf16) * r * h, ai = sizeof(bf16) * r * i;
+    const size_t ne = n_ex > 0 ? static_cast<size_t>(n_ex) : 1;
+    const size_t ah = ne * sizeof(bf16) * r * h, ai = ne * sizeof(bf16) * r * i;
+    if (n_ex > 0 && sq_norms != nullptr && cudaMemsetAsync(sq_norms, 0, sizeof(float) * n_ex, stream) != cudaSuccess)
+      return LORA_ERR_CUDA;
     if (cudaMemsetAsync(d_gate.dA, 0, ah, stream) || cudaMemsetAsync(d_gate.dB, 0, ai, stream) ||
         cudaMemsetAsync(d_up.dA, 0, ah, stream) || cudaMemsetAsync(d_up.dB, 0, ai, stream) ||
         cudaMemsetAsync(d_down.dA, 0, ai, stream) || cudaMemsetAsync(d_down.dB, 0, ah, stream))
@@ -721,7 +773,7 @@ extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int 
   const ProjSeg p1 = {dy, bt_d, h};
   LGB_TRY(rank_projection(M, kfd, &p1, 1, ud, part, status, stream));
   const GradJob j1 = {dy, h, 0, d_down.dB, 0};
-  LGB_TRY(token_grads(M, r, kfd, s, td, &j1, 1, part, status, stream));
+  LGB_TRY(token_grads(M, r, kfd, s, td, &j1, 1, part, status, stream, n_ex));
 
   // dh = [dy | U_d] [W_d ; s A_d];  dg = dh u act'(g), du = dh act(g)
   {
@@ -744,7 +796,7 @@ extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int 
 
   // dA_d = s U_d^T h
   const GradJob j2 = {hsv, i, 0, d_down.dA, 1};
-  LGB_TRY(token_grads(M, r, kfd, s, ud, &j2, 1, part, status, stream));
+  LGB_TRY(token_grads(M, r, kfd, s, ud, &j2, 1, part, status, stream, n_ex));
 
   // V = [dg B_g | du B_u]
   const ProjSeg p3[2] = {{dg, bt_g, i}, {du, bt_u, i}};
@@ -752,7 +804,7 @@ extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int 
 
   // dB_g = s dg^T T_g,  dB_u = s du^T T_u
   const GradJob j3[2] = {{dg, i, 0, d_gate.dB, 0}, {du, i, r, d_up.dB, 0}};
-  LGB_TRY(token_grads(M, r, kfg, s, tgu, j3, 2, part, status, stream));
+  LGB_TRY(token_grads(M, r, kfg, s, tgu, j3, 2, part, status, stream, n_ex));
 
   // dx = [dg | du | V] [W_g ; W_u ; s A_g ; s A_u]
   {
@@ -771,7 +823,48 @@ extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int 
 
   // dA_g = s V_g^T x,  dA_u = s V_u^T x
   const GradJob j4[2] = {{x, h, 0, d_gate.dA, 1}, {x, h, r, d_up.dA, 1}};
-  return token_grads(M, r, kfg, s, V, j4, 2, part, status, stream);
+  LGB_TRY(token_grads(M, r, kfg, s, V, j4, 2, part, status, stream, n_ex));
+  if (n_ex > 0 && sq_norms != nullptr) {
+    NormParams np;
+    std::memset(static_cast<void*>(&np), 0, sizeof(np));
+    const lora_grads_t* gs[3] = {&d_gate, &d_up, &d_down};
+    const int64_t fin[3] = {h, h, i}, fout[3] = {i, i, h};
+    for (int a = 0; a < 3; ++a) {
+      np.src[np.ntensors] = static_cast<const bf16*>(gs[a]->dA);
+      np.count[np.ntensors++] = static_cast<long long>(r) * fin[a];
+      np.src[np.ntensors] = static_cast<const bf16*>(gs[a]->dB);
+      np.count[np.ntensors++] = static_cast<long long>(r) * fout[a];
+    }
+    np.out = sq_norms;
+    LGB_TRY(launch_norms(np, static_cast<int>(n_ex), stream));
+  }
+  return LORA_OK;
+}
+
+extern "C" lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int r, float s, lora_act_t act,
+                                           const void* x, lora_linear_t gate, lora_linear_t up,
+                                           lora_linear_t down, const void* saved, const void* dy, void* dx,
+                                           lora_grads_t d_gate, lora_grads_t d_up, lora_grads_t d_down, void* ws,
+                                           size_t ws_bytes, cudaStream_t stream) {
+  return mlp_backward_impl(M, h, i, r, s, act, 0, x, gate, up, down, saved, dy, dx, d_gate, d_up, d_down,
+                           nullptr, ws, ws_bytes, stream);
+}
+
+extern "C" size_t lora_mlp_per_example_workspace_bytes(int64_t M, int64_t h, int64_t i, int r, int64_t n_examples) {
+  if (M < 0 || h <= 0 || i <= 0 || r < 1 || n_examples < 1 || M % n_examples != 0) return 0;
+  return mlp_layout(M, h, i, r, n_examples).ws_bwd;
+}
+
+extern "C" lora_status_t lora_mlp_backward_per_example(int64_t M, int64_t h, int64_t i, int r, float s,
+                                                       lora_act_t act, int64_t n_examples, const void* x,
+                                                       lora_linear_t gate, lora_linear_t up, lora_linear_t down,
+                                                       const void* saved, const void* dy, void* dx,
+                                                       lora_grads_t d_gate, lora_grads_t d_up, lora_grads_t d_down,
+                                                       float* sq_norms, void* ws, size_t ws_bytes,
+                                                       cudaStream_t stream) {
+  if (n_examples < 1) return LORA_ERR_INVALID_ARG;
+  return mlp_backward_impl(M, h, i, r, s, act, n_examples, x, gate, up, down, saved, dy, dx, d_gate, d_up, d_down,
+                           sq_norms, ws, ws_bytes, stream);
 }
 
 // ================================================================ Q/K/V + O

@@ -344,3 +344,19 @@ def test_frozen_bias_adds_a_row_vector_and_leaves_grads():
     for j, n in enumerate(("q", "k", "v")):
         np.testing.assert_allclose(b[n] - a[n], np.broadcast_to(bias[j], a[n].shape), rtol=0, atol=1e-12)
     np.testing.assert_array_equal(a["o"], b["o"])
+
+
+def test_per_example_grads_sum_to_the_batch_gradient():
+    """Per-example adapter gradients add up to the full-batch gradient (the loss is a
+    sum over examples), and each squared norm is the sum over the six adapters."""
+    p, dy = _mlp_params(M=6, h=8, i=12, r=2)
+    args = (p["x"], p["Wg"], p["Ag"], p["Bg"], p["Wu"], p["Au"], p["Bu"], p["Wd"], p["Ad"], p["Bd"], 1.5,
+            "swiglu")
+    full = oracle.mlp_backward(*args, dy)
+    per = oracle.mlp_backward_per_example(*args, dy, 3)
+    for k in ("dA_gate", "dB_gate", "dA_up", "dB_up", "dA_down", "dB_down"):
+        assert per[k].shape == (3,) + full[k].shape
+        np.testing.assert_allclose(per[k].sum(axis=0), full[k], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(per["dx"], full["dx"], rtol=1e-12, atol=1e-12)
+    e1 = sum(float(np.sum(per[k][1] ** 2)) for k in ("dA_gate", "dB_gate", "dA_up", "dB_up", "dA_down", "dB_down"))
+    assert math.isclose(per["sq_norms"][1], e1, rel_tol=1e-12)

@@ -196,3 +196,28 @@ def test_qkvo_frozen_bias(lib):
         parity(k, out[k], f[k])
     for k in b:
         parity(k, g[k], b[k])
+
+
+@pytest.mark.parametrize("name,over,n_ex", [
+    ("tiny", {}, 2),                                # seq 32: less than one 64-token block
+    ("tiny", {"M": 300, "i": 520, "h": 256}, 3),    # seq 100: ragged block per example
+    ("qwen05b", {"M": 2048}, 4),                    # seq 512
+])
+def test_mlp_per_example_grads(lib, name, over, n_ex):
+    """DP-SGD per-example adapter gradients and their squared norms."""
+    cfg = synth.MLP_CONFIGS[name].replace(**over)
+    t, v = _mlp_inputs(cfg, seed=8)
+    lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
+    y, saved = lib.mlp_forward(t["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act)
+    g = lib.mlp_backward_per_example(t["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, saved,
+                                     t["dy"], n_ex)
+    torch.cuda.synchronize()
+    assert lib.poll_status() == 0
+    args = (v["x"], v["W_gate"], v["A_gate"], v["B_gate"], v["W_up"], v["A_up"], v["B_up"],
+            v["W_down"], v["A_down"], v["B_down"], cfg.s, cfg.act)
+    ref = oracle.mlp_backward_per_example(*args, v["dy"], n_ex)
+    parity("dx", g["dx"], ref["dx"])
+    for k in ("dA_gate", "dB_gate", "dA_up", "dB_up", "dA_down", "dB_down"):
+        for e in range(n_ex):
+            parity(f"{k}[{e}]", g[k][e], ref[k][e])
+    np.testing.assert_allclose(g["sq_norms"].double().cpu().numpy(), ref["sq_norms"], rtol=2e-2)
