@@ -40,12 +40,15 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
-def dist_init(backend: str):
+def dist_init(backend: str, timeout_s: float = 600.0):
+    """Joins the process group.  A rank that dies or never arrives makes the others'
+    next barrier or reduction raise within timeout_s instead of waiting forever."""
     rank, world, _ = dist_env()
     if world > 1:
+        import datetime
         import torch.distributed as dist
         if not dist.is_initialized():
-            dist.init_process_group(backend=backend)
+            dist.init_process_group(backend=backend, timeout=datetime.timedelta(seconds=timeout_s))
     return rank, world
 
 
@@ -365,35 +368,73 @@ def run_ours(args):
     ms_step = secs / args.steps * 1e3
     tflops = cfg.flops() / (ms_step * 1e-3) / 1e12
 
-    # ---- end to end through host buffers: H2D of x, dy; D2H of y, dx and the grads
+    # ---- end to end through host buffers: every step copies its x, dy from pinned host
+    # memory and its y, dx, dA, dB back.  Double-buffered, as a training loop would:
+    # the copy stream moves step k+1's inputs in and step k's results out while the
+    # compute stream runs step k.
     e2e = None
     if not args.no_e2e and not n_ex:
+        cs = torch.cuda.Stream(device)
         xh = x.cpu().pin_memory()
         dyh = dy.cpu().pin_memory()
+        xd = [torch.empty_like(x) for _ in range(2)]
+        dyd = [torch.empty_like(dy) for _ in range(2)]
+        yd = [torch.empty_like(y) for _ in range(2)]
+        dxd = [torch.empty_like(dx) for _ in range(2)]
+        gd = [{k: torch.empty_like(v) for k, v in grads.items()} for _ in range(2)]
         yh = torch.empty(M, h, dtype=torch.bfloat16).pin_memory()
         dxh = torch.empty(M, h, dtype=torch.bfloat16).pin_memory()
         gh = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in grads.items()}
-        xd, dyd = torch.empty_like(x), torch.empty_like(dy)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step():
-            xd.copy_(xh, non_blocking=True)
-            dyd.copy_(dyh, non_blocking=True)
-            lib.mlp_forward(xd, gate, up, down, cfg.s, cfg.act, y=y, saved=saved, ws=ws)
-            lib.mlp_backward(xd, gate, up, down, cfg.s, cfg.act, saved, dyd, dx=dx, grads=grads, ws=ws)
-            yh.copy_(y, non_blocking=True)
-            dxh.copy_(dx, non_blocking=True)
-            for k in grads:
-                gh[k].copy_(grads[k], non_blocking=True)
+        def e2e_run(steps):
+            """steps fwd+bwd through host buffers; returns seconds (CUDA events)."""
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(cs)
+            with torch.cuda.stream(cs):
+                xd[0].copy_(xh, non_blocking=True)
+                dyd[0].copy_(dyh, non_blocking=True)
+                ev_in[0].record(cs)
+            for k in range(steps):
+                b = k & 1
+                stream.wait_event(ev_in[b])
+                if k >= 2:
+                    stream.wait_event(ev_out[b])              # step k-2's results have left buffers b
+                lib.mlp_forward(xd[b], gate, up, down, cfg.s, cfg.act, y=yd[b], saved=saved, ws=ws)
+                lib.mlp_backward(xd[b], gate, up, down, cfg.s, cfg.act, saved, dyd[b], dx=dxd[b], grads=gd[b],
+                                 ws=ws)
+                ev_done[b].record(stream)
+                with torch.cuda.stream(cs):
+                    if k + 1 < steps:
+                        if k >= 1:
+                            cs.wait_event(ev_done[1 - b])     # step k-1 finished reading buffers 1-b
+                        xd[1 - b].copy_(xh, non_blocking=True)
+                        dyd[1 - b].copy_(dyh, non_blocking=True)
+                        ev_in[1 - b].record(cs)
+                    cs.wait_event(ev_done[b])
+                    yh.copy_(yd[b], non_blocking=True)
+                    dxh.copy_(dxd[b], non_blocking=True)
+                    for n in grads:
+                        gh[n].copy_(gd[b][n], non_blocking=True)
+                    ev_out[b].record(cs)
+            t1.record(cs)
+            t1.synchronize()
+            return t0.elapsed_time(t1) / 1e3
 
-        for _ in range(3):
-            e2e_step()
+        e2e_run(3)
         ke = max(1, min(args.steps, 50))
-        esecs = timed_steps(e2e_step, ke, world, device, torch.cuda.synchronize, cuda_timer(torch, stream))
+        barrier(world, device)
+        torch.cuda.synchronize()
+        esecs = max_over_ranks(e2e_run(ke), world, device)
+        barrier(world, device)
         h2d = 2 * M * h * 2
         d2h = 2 * M * h * 2 + sum(v.numel() * 2 for v in grads.values())
         e2e = {"value": world * M * ke / esecs, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": ke,
-               "path": "pinned host x, dy -> device; lora_mlp_forward + lora_mlp_backward; y, dx, dA, dB -> host"}
+               "path": "pinned host x, dy -> device; lora_mlp_forward + lora_mlp_backward; y, dx, dA, dB -> "
+                       "host; copies of step k+1 / k overlap step k's compute (copy stream, double buffers)"}
 
     if rank != 0:
         return 0

@@ -204,6 +204,32 @@ const char* lora_status_string(lora_status_t status);
 /* Kernels this library has launched in this process (all entry points). */
 uint64_t lora_launch_count(void);
 
+/* ---------------------------------------------------------------- bounded waits
+ * Every wait inside the GEMM kernels (a pipeline stage, an accumulator buffer) is
+ * bounded.  When one runs out, the kernel stops issuing work, lets its own copies and
+ * MMAs in flight finish, frees its tensor memory and exits; the status word in `ws`
+ * then reads LORA_ERR_TIMEOUT (see lora_poll_status) and that call's outputs are
+ * undefined.  The CUDA context stays usable.  The pages define no such mechanism.
+ *
+ * lora_set_wait_timeout: the limit in nanoseconds for launches enqueued after the
+ * call, process-wide (all devices, all threads).  0 restores the default of 2 s.
+ * Accepted range 1 ms .. 60 s, else LORA_ERR_INVALID_ARG.  A limit shorter than
+ * the slowest tile of a workload (tens of microseconds for the shapes here, longer
+ * when the GPU is time-sliced with other processes) makes healthy calls fail.
+ * The limit is counted in SM cycles at 2.5 GHz, so at a lower clock the wait lasts
+ * proportionally longer.
+ * lora_wait_timeout: the current limit in nanoseconds. */
+lora_status_t lora_set_wait_timeout(uint64_t ns);
+uint64_t lora_wait_timeout(void);
+
+/* Test hook for the failure path (no counterpart in the pages): the next `launches`
+ * GEMM launches (0 .. 64; 0 cancels) each leave the first pipeline stage of every
+ * CTA's first tile unfilled, so the waits on it expire after the wait limit and the
+ * call reports LORA_ERR_TIMEOUT through the status word.  Nothing faults, traps or
+ * hangs: the waits are the bounded ones above.  Returns LORA_ERR_INVALID_ARG out of
+ * range. */
+lora_status_t lora_test_expire_waits(int launches);
+
 /* Launch tracing, for measurement.  lora_trace_enable(n) makes every later launch
  * record a pair of CUDA events around itself on its stream, keeping the first n
  * launches (0 disables and frees the events).  lora_trace_read synchronises the

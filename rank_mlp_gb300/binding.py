@@ -72,6 +72,9 @@ _SIGS = {
     "lora_poll_status": (_INT, [_VP, _VP]),
     "lora_status_string": (ctypes.c_char_p, [_INT]),
     "lora_launch_count": (ctypes.c_uint64, []),
+    "lora_set_wait_timeout": (_INT, [ctypes.c_uint64]),
+    "lora_wait_timeout": (ctypes.c_uint64, []),
+    "lora_test_expire_waits": (_INT, [_INT]),
     "lora_trace_enable": (_INT, [_INT]),
     "lora_trace_read": (_INT, [ctypes.POINTER(_INT), ctypes.POINTER(_F32), _INT]),
 }
@@ -149,6 +152,20 @@ def poll_status(ws: torch.Tensor | None = None) -> int:
 
 def launch_count() -> int:
     return int(load().lora_launch_count())
+
+
+def set_wait_timeout(ns: int):
+    """Limit of the kernels' bounded waits, in ns (0 = the default of 2 s)."""
+    _check(load().lora_set_wait_timeout(ns), "lora_set_wait_timeout")
+
+
+def wait_timeout() -> int:
+    return int(load().lora_wait_timeout())
+
+
+def test_expire_waits(launches: int):
+    """Failure-path tests: the next `launches` GEMM launches let a bounded wait expire."""
+    _check(load().lora_test_expire_waits(launches), "lora_test_expire_waits")
 
 
 def trace_enable(capacity: int):

@@ -95,6 +95,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
       int armed[STAGES];
       for (int s = 0; s < STAGES; ++s) armed[s] = -1;
       bool ok = true;
+      bool first_stage = true;
       for (int u = pair; u < p.total_units && ok; u += npairs) {
         const Unit U = decode_unit(p, u);
         const GroupDesc& G = p.grp[U.g];
@@ -114,6 +115,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
             const int kc = j * kBK;
             if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) { ok = false; break; }
             const uint32_t fb = full_bar(stage);
+            if (p.inject_stall && first_stage && leader) {   // failure-path tests: never arm it
+              first_stage = false;
+              if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+              continue;
+            }
+            first_stage = false;
             if (leader) {
               mbar_arrive_expect_tx(fb, C::kTxBytes);
               armed[stage] = static_cast<int>(phase);
@@ -212,12 +219,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
     }
   }
 
-  if (*abort_flag) {
-    // after an abort, give copies still in flight time to land before shared memory goes
-    const uint64_t t0 = global_timer_ns();
-    while (global_timer_ns() - t0 < 200000ull) {
-    }
-  }
+  if (*abort_flag) settle_after_abort();
   __syncwarp();
   tc_fence_before_sync();
   cluster_sync_all();                     // no remote arrive or MMA read of either CTA is pending

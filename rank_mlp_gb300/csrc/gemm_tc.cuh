@@ -68,6 +68,8 @@ struct TcParams {
   int act;
   unsigned int* status;
   unsigned long long timeout_ns;
+  int inject_stall;          // failure-path tests only: the first stage of the first unit
+                             // is never filled, so the waits on it run out
 };
 
 template <int BN, int STAGES>
@@ -138,14 +140,23 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
-// Drain wait after an abort: bounded by time only.
+// Drain wait after an abort (this CTA's own copies or MMAs, which finish in
+// microseconds): bounded by a fixed 20 ms at up to 2.5 GHz, whatever timeout_ns is.
 __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity, const TcParams& p) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > timeout_cycles(p)) {
+    if (clock64() - t0 > 50000000ll) {
       if (p.status) atomicOr(p.status, kStatusTimeout);
       return;
     }
+  }
+}
+
+// After an abort: give copies still in flight time to land before shared memory is
+// released (200 us).
+__device__ __forceinline__ void settle_after_abort() {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < 200000ull) {
   }
 }
 
@@ -420,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       int armed[STAGES];
       for (int s = 0; s < STAGES; ++s) armed[s] = -1;
       bool ok = true;
+      bool first_stage = true;
       for (int u = blockIdx.x; u < p.total_units && ok; u += gridDim.x) {
         const Unit U = decode_unit(p, u);
         const GroupDesc& G = p.grp[U.g];
@@ -438,6 +450,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const int kc = j * kBK;
             if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) { ok = false; break; }
             const uint32_t fb = full_bar(stage);
+            if (p.inject_stall && first_stage) {   // failure-path tests: leave this stage empty
+              first_stage = false;
+              if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+              continue;
+            }
+            first_stage = false;
             mbar_arrive_expect_tx(fb, C::kStageBytes);
             armed[stage] = static_cast<int>(phase);
             const uint32_t sa = sbase + stage * C::kStageBytes;
@@ -552,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
   }
 
+  if (*abort_flag) settle_after_abort();
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {

@@ -93,8 +93,23 @@ static void trace_end(int slot, cudaStream_t st) {
   cudaEventRecord(g_trace.ev[2 * slot + 1], st);
 }
 
-lora_status_t launch_gemm(int variant, const TcParams& p, int kind, cudaStream_t st) {
-  if (p.total_units <= 0) return LORA_OK;
+// Wait limit of the GEMM kernels' bounded waits, and the number of coming GEMM
+// launches that are told to leave one pipeline stage empty (failure-path tests).
+static std::atomic<unsigned long long> g_timeout_ns{kTimeoutNs};
+static std::atomic<int> g_expire_next{0};
+
+static int take_expiry() {
+  int n = g_expire_next.load();
+  while (n > 0 && !g_expire_next.compare_exchange_weak(n, n - 1)) {
+  }
+  return n > 0 ? 1 : 0;
+}
+
+lora_status_t launch_gemm(int variant, const TcParams& plan, int kind, cudaStream_t st) {
+  if (plan.total_units <= 0) return LORA_OK;
+  TcParams p = plan;
+  p.timeout_ns = g_timeout_ns.load();
+  p.inject_stall = take_expiry();
   int grid;
   if (variant_pair(variant)) {
     const int pairs = num_sms() / 2;
@@ -1184,6 +1199,21 @@ extern "C" const char* lora_status_string(lora_status_t status) {
     case LORA_ERR_TIMEOUT: return "a kernel's bounded wait expired";
   }
   return "unknown status";
+}
+
+extern "C" lora_status_t lora_set_wait_timeout(uint64_t ns) {
+  if (ns == 0) ns = kTimeoutNs;
+  if (ns < 1000000ull || ns > 60000000000ull) return LORA_ERR_INVALID_ARG;
+  g_timeout_ns.store(ns);
+  return LORA_OK;
+}
+
+extern "C" uint64_t lora_wait_timeout(void) { return g_timeout_ns.load(); }
+
+extern "C" lora_status_t lora_test_expire_waits(int launches) {
+  if (launches < 0 || launches > 64) return LORA_ERR_INVALID_ARG;
+  g_expire_next.store(launches);
+  return LORA_OK;
 }
 
 extern "C" uint64_t lora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -134,3 +134,20 @@ def test_linear_rejects(L):
                                  ALIGNED, ws, None) == 2
     assert L.lora_linear_forward(64, 128, 256, 8, 1.0, ALIGNED, lin, ALIGNED, None, ALIGNED, 10, None) == 4
     assert L.lora_poll_status(None, None) == 1
+
+
+def test_wait_limit_range(L):
+    assert L.lora_wait_timeout() == 2_000_000_000
+    assert L.lora_set_wait_timeout(999_999) == 1          # below 1 ms
+    assert L.lora_set_wait_timeout(60_000_000_001) == 1   # above 60 s
+    assert L.lora_wait_timeout() == 2_000_000_000
+    assert L.lora_set_wait_timeout(5_000_000) == 0
+    assert L.lora_wait_timeout() == 5_000_000
+    assert L.lora_set_wait_timeout(0) == 0                # back to the default
+    assert L.lora_wait_timeout() == 2_000_000_000
+
+
+def test_expiry_hook_range(L):
+    assert L.lora_test_expire_waits(-1) == 1
+    assert L.lora_test_expire_waits(65) == 1
+    assert L.lora_test_expire_waits(0) == 0

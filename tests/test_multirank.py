@@ -1,6 +1,8 @@
 """bench.py's multi-rank path on the CPU: two gloo ranks run independent replicas;
 the timed region is bracketed by barriers and the reported time is the slowest
-rank's (max over ranks).  No collective touches the data path."""
+rank's (max over ranks).  No collective touches the data path.  A rank that fails
+between steps is detected on the host: the surviving rank's next barrier raises
+instead of waiting forever."""
 
 import os
 import socket
@@ -80,3 +82,36 @@ def test_kernel_flops_sum_to_the_block_minus_rank_work():
     base = 12.0 * cfg.M * cfg.h * cfg.i
     assert sum(f.values()) > base
     assert sum(f.values()) < cfg.flops()
+
+
+def _failing_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench
+    bench.dist_init("gloo", timeout_s=10.0)
+    bench.barrier(world)                       # both ranks joined
+    if rank == 1:
+        os._exit(3)                            # dies between steps, nothing in flight
+    t0 = time.perf_counter()
+    try:
+        bench.timed_steps(lambda: time.sleep(0.01), 4, world, None, None,
+                          (lambda: None, lambda: 0.0))
+        q.put((rank, "no error", time.perf_counter() - t0))
+    except Exception as e:                     # noqa: BLE001 - any error is the detection
+        q.put((rank, type(e).__name__, time.perf_counter() - t0))
+
+
+def test_a_dead_rank_is_detected_not_waited_for():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.SimpleQueue()
+    procs = [ctx.Process(target=_failing_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert procs[1].exitcode == 3
+    assert procs[0].exitcode is not None, "the surviving rank is still waiting"
+    rank, what, secs = q.get()
+    assert rank == 0 and what != "no error"
+    assert secs < 60.0
