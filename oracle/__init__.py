@@ -11,4 +11,5 @@ function follows.
 from .lora import (  # noqa: F401
     ACTS, act, act_prime, silu, gelu_tanh, gelu_erf, lora_linear, lora_linear_grad,
     mlp_forward, mlp_backward, mlp_backward_per_example, qkvo_forward, qkvo_backward, linear_t,
+    rope_tables, apply_rope, apply_rope_transpose,
 )

@@ -17,6 +17,9 @@ Sources (web pages; each function names the passage it follows):
 * same page, section "Fused linear cross-entropy", "Key design decisions": a frozen
   weight gets no gradient.  Base weights W are frozen here, so backward returns
   dX and the adapter gradients dA, dB only.
+* same page, section "Rotary position embeddings (RoPE)": rotary embeddings applied
+  to q and k together, with different head counts for q and k (GQA), following the
+  RoFormer position encoding.
 * "monkeypatch.lora_kernels" (axolotl API reference), ``apply_lora_kernel_patches``
   note: adapters have no dropout and no bias; ``original_apply_qkv`` returns
   (query, key, value) from one hidden-state input; ``original_apply_o`` is the
@@ -34,11 +37,19 @@ Readings where the pages leave a step open (plainest reading, stated once here):
    dA/dB are the full gradients of the scalar <dY, Y> (no accumulation into old
    values).
 6. Nothing is rounded: inputs are the bf16 values widened to float64.
+7. RoPE: head j of q and k (head_dim d) is rotated pair by pair, the pair being
+   features (i, i + d/2) of the head (the half-split pairing of the HF LLaMA family
+   the page lists as patched; RoFormer's own pairing (2i, 2i+1) differs only by a
+   fixed permutation of a head's features).  The angle of pair i at position p is
+   p * base^(-2i/d), base 10000 unless stated.  It is applied after the frozen bias,
+   to q and k only, and the position of each token is an input.
 
 Every function is pinned by tests that do not restate its formula: the LoRA
 merged-weight identity, the B = 0 reduction to a base MLP built from library
 routines, central finite differences of <dY, Y>, closed-form activation
-derivatives against finite differences, and linearity in s.
+derivatives against finite differences, and linearity in s; RoPE by RoFormer's
+complex form of the rotation, closed table values, norm preservation, the
+relative-position property of rotated dot products, and finite differences.
 """
 
 from __future__ import annotations
@@ -196,24 +207,68 @@ def mlp_backward_per_example(x, Wg, Ag, Bg, Wu, Au, Bu, Wd, Ad, Bd, s, kind, dy,
 # The attention between them is not part of this path; o_in is its output.
 # --------------------------------------------------------------------------------
 
-def qkvo_forward(x, lin_q, lin_k, lin_v, o_in, lin_o, s, bias=None):
+# --------------------------------------------------------------------------------
+# RoPE -- "Model Patches and Kernels", "Rotary position embeddings (RoPE)": rotary
+# embeddings of q and k (RoFormer), GQA head counts.
+# --------------------------------------------------------------------------------
+
+def rope_tables(n_pos, head_dim, base=10000.0):
+    """cos and sin of the rotation angles, [n_pos, head_dim/2]: entry (p, i) is the
+    angle p * base^(-2i/head_dim) (RoFormer's frequencies)."""
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    theta = np.power(float(base), -2.0 * i / head_dim)
+    ang = np.arange(n_pos, dtype=np.float64)[:, None] * theta[None, :]
+    return np.cos(ang), np.sin(ang)
+
+
+def _rotate(y, cos, sin, pos, head_dim, sign):
+    M, n = y.shape
+    half = head_dim // 2
+    yh = y.reshape(M, n // head_dim, head_dim)
+    a, b = yh[:, :, :half], yh[:, :, half:]
+    c = cos[pos][:, None, :]
+    s_ = sign * sin[pos][:, None, :]
+    return np.concatenate([a * c - b * s_, b * c + a * s_], axis=2).reshape(M, n)
+
+
+def apply_rope(y, cos, sin, pos, head_dim):
+    """Rotates every head of y [M, heads * head_dim]: in token m's head, the pair
+    (y_i, y_{i + d/2}) turns by the angle of row pos[m], column i of the tables."""
+    return _rotate(y, cos, sin, pos, head_dim, 1.0)
+
+
+def apply_rope_transpose(dy, cos, sin, pos, head_dim):
+    """The transpose of apply_rope (each pair turned by minus the angle): the gradient
+    with respect to the unrotated input, given the gradient dy of the rotated one."""
+    return _rotate(dy, cos, sin, pos, head_dim, -1.0)
+
+
+def qkvo_forward(x, lin_q, lin_k, lin_v, o_in, lin_o, s, bias=None, rope=None):
     """lin_p = (W, A, B).  Returns dict(q, k, v, o).
 
     bias: optional frozen base-layer biases (b_q, b_k, b_v) added to q, k, v
     ("Fused LoRA operations": QKV fusion supports optional frozen base-layer biases).
-    A frozen bias gets no gradient and does not change the backward."""
+    A frozen bias gets no gradient and does not change the backward.
+    rope: optional dict(cos, sin, pos, head_dim): q and k (bias included) are then
+    rotated by apply_rope."""
     out = {}
     for j, (name, lin) in enumerate((("q", lin_q), ("k", lin_k), ("v", lin_v))):
         out[name] = lora_linear(x, *lin, s)
         if bias is not None:
             out[name] = out[name] + bias[j][None, :]
+        if rope is not None and name in ("q", "k"):
+            out[name] = apply_rope(out[name], rope["cos"], rope["sin"], rope["pos"], rope["head_dim"])
     out["o"] = lora_linear(o_in, *lin_o, s)
     return out
 
 
-def qkvo_backward(x, lin_q, lin_k, lin_v, o_in, lin_o, s, dy_q, dy_k, dy_v, dy_o):
+def qkvo_backward(x, lin_q, lin_k, lin_v, o_in, lin_o, s, dy_q, dy_k, dy_v, dy_o, rope=None):
     """Gradients of <dy_q, q> + <dy_k, k> + <dy_v, v> + <dy_o, o>: dx (sum over the
-    three projections), d o_in, and dA/dB of q, k, v and o."""
+    three projections), d o_in, and dA/dB of q, k, v and o.  With rope, dy_q and dy_k
+    are gradients of the rotated q and k and pass through apply_rope_transpose first."""
+    if rope is not None:
+        dy_q = apply_rope_transpose(dy_q, rope["cos"], rope["sin"], rope["pos"], rope["head_dim"])
+        dy_k = apply_rope_transpose(dy_k, rope["cos"], rope["sin"], rope["pos"], rope["head_dim"])
     res = {}
     dx = None
     for name, lin, d in (("q", lin_q, dy_q), ("k", lin_k, dy_k), ("v", lin_v, dy_v)):

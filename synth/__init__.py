@@ -313,3 +313,16 @@ def make_qkvo_inputs(cfg: QkvoConfig, seed: int = 0, only=None, device="cpu") ->
         makers[f"dy_{p}"] = (lambda p=p, n_out=n_out: _act(seed, sid[f"dy_{p}"], M, n_out, d))
     names = QKVO_TENSORS if only is None else only
     return {n: makers[n]() for n in names}
+
+
+def positions(M: int, seq: int = 0, lengths=None, device="cpu") -> torch.Tensor:
+    """int32 position of each of M tokens laid out as sequences end to end: the
+    position restarts at 0 where a sequence starts.  Either equal sequences of `seq`
+    tokens, or the explicit `lengths` (packed sequences; they must add up to M)."""
+    if lengths is None:
+        if seq <= 0:
+            raise ValueError("give seq or lengths")
+        return (torch.arange(M, dtype=torch.int64) % seq).to(torch.int32).to(device)
+    if sum(lengths) != M:
+        raise ValueError("lengths must add up to M")
+    return torch.cat([torch.arange(n, dtype=torch.int32) for n in lengths]).to(device)

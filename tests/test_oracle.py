@@ -174,16 +174,17 @@ def _qkvo_params(M=4, h=8, nq=8, nkv=4, r=2, seed=11):
     return p, dys
 
 
-def _qkvo_loss(p, dys, s):
-    out = oracle.qkvo_forward(p["x"], p["q"], p["k"], p["v"], p["o_in"], p["o"], s)
+def _qkvo_loss(p, dys, s, rope=None, mod=olora):
+    out = mod.qkvo_forward(p["x"], p["q"], p["k"], p["v"], p["o_in"], p["o"], s, rope=rope)
     return float(sum(np.sum(dys[k] * out[k]) for k in ("q", "k", "v", "o")))
 
 
-def test_qkvo_backward_matches_finite_differences():
-    p, dys = _qkvo_params()
-    s, eps = 2.0, 1e-6
-    g = oracle.qkvo_backward(p["x"], p["q"], p["k"], p["v"], p["o_in"], p["o"], s,
-                             dys["q"], dys["k"], dys["v"], dys["o"])
+def qkvo_fd_error(rope=None, mod=olora, s=2.0, eps=1e-6, **shape):
+    """Largest error of the Q/K/V + O backward against central differences of
+    <dy, out>, relative to the largest difference quotient of each tensor."""
+    p, dys = _qkvo_params(**shape)
+    g = mod.qkvo_backward(p["x"], p["q"], p["k"], p["v"], p["o_in"], p["o"], s,
+                          dys["q"], dys["k"], dys["v"], dys["o"], rope=rope)
 
     def fd_of(getter):
         base = getter(p)
@@ -191,9 +192,9 @@ def test_qkvo_backward_matches_finite_differences():
         for idx in np.ndindex(base.shape):
             orig = base[idx]
             base[idx] = orig + eps
-            lp = _qkvo_loss(p, dys, s)
+            lp = _qkvo_loss(p, dys, s, rope, mod)
             base[idx] = orig - eps
-            lm = _qkvo_loss(p, dys, s)
+            lm = _qkvo_loss(p, dys, s, rope, mod)
             base[idx] = orig
             fd[idx] = (lp - lm) / (2 * eps)
         return fd
@@ -202,9 +203,15 @@ def test_qkvo_backward_matches_finite_differences():
     for name in ("q", "k", "v", "o"):
         checks.append((lambda q, name=name: q[name][1], g[f"dA_{name}"]))
         checks.append((lambda q, name=name: q[name][2], g[f"dB_{name}"]))
+    worst = 0.0
     for getter, got in checks:
         fd = fd_of(getter)
-        assert np.max(np.abs(got - fd)) <= 1e-6 * np.max(np.abs(fd))
+        worst = max(worst, float(np.max(np.abs(got - fd)) / np.max(np.abs(fd))))
+    return worst
+
+
+def test_qkvo_backward_matches_finite_differences():
+    assert qkvo_fd_error() <= 1e-6
 
 
 # ---------------------------------------------------------------- B = 0: the base MLP
@@ -265,7 +272,8 @@ class _Mutant:
         self.__dict__.update({k: getattr(olora, k) for k in dir(olora) if not k.startswith("__")})
         self.__dict__.update(repl)
         # rebind the functions that call the replaced ones
-        for name in ("mlp_forward", "mlp_backward"):
+        for name in ("mlp_forward", "mlp_backward", "qkvo_forward", "qkvo_backward", "apply_rope",
+                     "apply_rope_transpose"):
             if name not in repl:
                 self.__dict__[name] = _rebind(getattr(olora, name), self)
 
@@ -360,3 +368,118 @@ def test_per_example_grads_sum_to_the_batch_gradient():
     np.testing.assert_allclose(per["dx"], full["dx"], rtol=1e-12, atol=1e-12)
     e1 = sum(float(np.sum(per[k][1] ** 2)) for k in ("dA_gate", "dB_gate", "dA_up", "dB_up", "dA_down", "dB_down"))
     assert math.isclose(per["sq_norms"][1], e1, rel_tol=1e-12)
+
+
+# ---------------------------------------------------------------- RoPE
+
+def _rope(M=4, n_pos=40, head_dim=4, seed=2, base=10000.0):
+    cos, sin = oracle.rope_tables(n_pos, head_dim, base)
+    pos = np.random.default_rng(seed).integers(0, n_pos, M)
+    return {"cos": cos, "sin": sin, "pos": pos, "head_dim": head_dim}
+
+
+def test_rope_table_closed_values():
+    """Frequency 0 turns 1 rad per position; with d = 4 and base 10000 the other
+    frequency is 10000^(-1/2) = 0.01 rad; consecutive frequencies fall by the factor
+    base^(-2/d) (RoFormer's geometric frequencies)."""
+    cos, sin = oracle.rope_tables(7, 4)
+    for p in range(7):
+        assert math.isclose(cos[p, 0], math.cos(p), abs_tol=1e-15)
+        assert math.isclose(sin[p, 0], math.sin(p), abs_tol=1e-15)
+        assert math.isclose(cos[p, 1], math.cos(0.01 * p), abs_tol=1e-15)
+        assert math.isclose(sin[p, 1], math.sin(0.01 * p), abs_tol=1e-15)
+    cos, sin = oracle.rope_tables(2, 128, base=500000.0)
+    ang = np.arctan2(sin[1], cos[1])                   # position 1: every angle below pi
+    np.testing.assert_allclose(ang[1:] / ang[:-1], 500000.0 ** (-2.0 / 128), rtol=1e-12)
+
+
+def rope_complex_error(mod=olora, d=8):
+    """apply_rope against RoFormer's complex form: the pair (y_i, y_{i+d/2}) is the
+    number y_i + 1j y_{i+d/2}, multiplied by exp(1j p theta_i), theta_i =
+    10000^(-2(i-1)/d) for i = 1 .. d/2."""
+    rng = np.random.default_rng(3)
+    M, heads, n_pos = 6, 3, 50
+    y = rng.standard_normal((M, heads * d))
+    pos = rng.integers(0, n_pos, M)
+    cos, sin = oracle.rope_tables(n_pos, d)
+    got = mod.apply_rope(y, cos, sin, pos, d).reshape(M, heads, d)
+    yh = y.reshape(M, heads, d)
+    z = yh[:, :, :d // 2] + 1j * yh[:, :, d // 2:]
+    theta = 10000.0 ** (-2.0 * (np.arange(1, d // 2 + 1) - 1) / d)
+    w = z * np.exp(1j * pos[:, None, None] * theta[None, None, :])
+    return max(float(np.max(np.abs(got[:, :, :d // 2] - w.real))),
+               float(np.max(np.abs(got[:, :, d // 2:] - w.imag))))
+
+
+def test_rope_is_the_complex_rotation():
+    assert rope_complex_error() < 1e-12
+
+
+def test_rope_keeps_norms_and_depends_on_relative_position():
+    """A rotation keeps each head's norm, position 0 is the identity, and the dot
+    product of a rotated q head with a rotated k head depends only on the distance
+    between their positions (RoFormer's relative-position property)."""
+    d = 16
+    cos, sin = oracle.rope_tables(64, d)
+    rng = np.random.default_rng(9)
+    q, k = rng.standard_normal((1, d)), rng.standard_normal((1, d))
+    y = rng.standard_normal((5, 3 * d))
+    pos = np.array([0, 1, 7, 30, 63])
+    r = oracle.apply_rope(y, cos, sin, pos, d)
+    np.testing.assert_allclose(np.linalg.norm(r.reshape(5, 3, d), axis=2),
+                               np.linalg.norm(y.reshape(5, 3, d), axis=2), rtol=1e-13)
+    np.testing.assert_array_equal(r[0], y[0])
+
+    def dot(pq, pk):
+        return float(np.sum(oracle.apply_rope(q, cos, sin, [pq], d) * oracle.apply_rope(k, cos, sin, [pk], d)))
+
+    assert math.isclose(dot(10, 3), dot(20, 13), rel_tol=1e-12)
+    assert math.isclose(dot(40, 40), float(np.sum(q * k)), rel_tol=1e-12)
+    assert not math.isclose(dot(10, 3), dot(10, 4), rel_tol=1e-3)
+
+
+def test_rope_transpose_is_adjoint_and_inverse():
+    rp = _rope(M=5, head_dim=8)
+    rng = np.random.default_rng(4)
+    y, z = rng.standard_normal((5, 16)), rng.standard_normal((5, 16))
+    args = (rp["cos"], rp["sin"], rp["pos"], 8)
+    ry = oracle.apply_rope(y, *args)
+    assert math.isclose(float(np.sum(ry * z)), float(np.sum(y * oracle.apply_rope_transpose(z, *args))),
+                        rel_tol=1e-12)
+    np.testing.assert_allclose(oracle.apply_rope_transpose(ry, *args), y, atol=1e-13)
+
+
+def test_qkvo_rope_backward_matches_finite_differences():
+    """Q/K/V + O with RoPE on q and k (two heads of q, one of k: GQA)."""
+    assert qkvo_fd_error(rope=_rope(head_dim=4)) <= 1e-6
+
+
+def test_rope_leaves_v_and_o_alone():
+    p, _ = _qkvo_params()
+    a = oracle.qkvo_forward(p["x"], p["q"], p["k"], p["v"], p["o_in"], p["o"], 2.0)
+    b = oracle.qkvo_forward(p["x"], p["q"], p["k"], p["v"], p["o_in"], p["o"], 2.0, rope=_rope())
+    np.testing.assert_array_equal(a["v"], b["v"])
+    np.testing.assert_array_equal(a["o"], b["o"])
+    assert np.max(np.abs(a["q"] - b["q"])) > 1e-3
+
+
+def _rope_no_negation(dy, cos, sin, pos, head_dim):
+    return olora.apply_rope(dy, cos, sin, pos, head_dim)
+
+
+def _rope_interleaved(y, cos, sin, pos, head_dim):
+    M, n = y.shape
+    yh = y.reshape(M, n // head_dim, head_dim // 2, 2)
+    a, b = yh[..., 0], yh[..., 1]
+    c, s_ = cos[pos][:, None, :], sin[pos][:, None, :]
+    return np.stack([a * c - b * s_, b * c + a * s_], axis=-1).reshape(M, n)
+
+
+def _rope_swapped_tables(y, cos, sin, pos, head_dim):
+    return olora._rotate(y, sin, cos, pos, head_dim, 1.0)
+
+
+def test_planted_rope_mistakes_are_caught():
+    assert qkvo_fd_error(rope=_rope(), mod=_Mutant(apply_rope_transpose=_rope_no_negation)) > 1e-3
+    assert rope_complex_error(mod=_Mutant(apply_rope=_rope_interleaved)) > 1e-3
+    assert rope_complex_error(mod=_Mutant(apply_rope=_rope_swapped_tables)) > 1e-3

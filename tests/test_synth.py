@@ -114,3 +114,11 @@ def test_config_flop_counts(name):
     base = 3 * (2 * c.M * c.h * c.i) * 2      # three projections: forward product + dX product
     lora = 3 * 6 * c.M * c.r * (c.h + c.i)    # per linear: T, T B^T, U, U A, dA, dB
     assert c.flops() == pytest.approx(base + lora, rel=1e-12)
+
+
+def test_positions_restart_at_each_sequence():
+    assert synth.positions(7, seq=3).tolist() == [0, 1, 2, 0, 1, 2, 0]
+    assert synth.positions(6, lengths=[2, 4]).tolist() == [0, 1, 0, 1, 2, 3]
+    assert synth.positions(4, seq=3).dtype == torch.int32
+    with pytest.raises(ValueError):
+        synth.positions(5, lengths=[2, 2])
