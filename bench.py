@@ -469,6 +469,99 @@ def run_ours(args):
     return 0
 
 
+def qkvo_kernel_flops(cfg):
+    """Algorithmic FLOPs per step of each GEMM kind of one Q/K/V + O fwd+bwd (two
+    launches per kind: the q/k/v half and the O half)."""
+    M, h, r, nq, nkv = cfg.M, cfg.h, cfg.r, cfg.n_q, cfg.n_kv
+    return {"proj": 2.0 * M * ((nq + 2 * nkv) * (h + r) + h * (nq + r)),
+            "dgrad": 2.0 * M * (h * (nq + 2 * nkv + 3 * r) + nq * (h + r))}
+
+
+def run_qkvo(args):
+    """Q/K/V + O fwd+bwd (optionally with RoPE on q and k): device-resident timing."""
+    import torch
+    import synth
+    from rank_mlp_gb300 import binding as lib
+
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist_init("nccl")
+    lib.load()
+    cfg = synth.QKVO_CONFIGS[args.workload]
+    t = synth.make_qkvo_inputs(cfg, seed=0, device=device)
+    lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
+    rope = None
+    if args.rope:
+        cos, sin = lib.rope_table(cfg.seq, cfg.head_dim, 10000.0, device=device)
+        rope = {"cos": cos, "sin": sin, "pos": synth.positions(cfg.M, seq=cfg.seq, device=device),
+                "head_dim": cfg.head_dim}
+    M, h, r = cfg.M, cfg.h, cfg.r
+    ws = torch.zeros(lib.load().lora_qkvo_workspace_bytes(M, h, cfg.n_q, cfg.n_kv, r), dtype=torch.uint8,
+                     device=device)
+    saved = torch.empty(lib.load().lora_qkvo_saved_bytes(M, h, cfg.n_q, cfg.n_kv, r), dtype=torch.uint8,
+                        device=device)
+
+    def step():
+        lib.qkvo_forward(t["x"], lin("q"), lin("k"), lin("v"), t["o_in"], lin("o"), cfg.s, rope=rope,
+                         saved=saved, ws=ws)
+        lib.qkvo_backward(t["x"], lin("q"), lin("k"), lin("v"), t["o_in"], lin("o"), cfg.s, saved,
+                          t["dy_q"], t["dy_k"], t["dy_v"], t["dy_o"], rope=rope, ws=ws)
+
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    lib.trace_enable(64 * args.steps + 64)
+    n0 = lib.launch_count()
+    clocks = ClockSampler()
+    if rank == 0:
+        clocks.start()
+    secs = timed_steps(step, args.steps, world, device, torch.cuda.synchronize, cuda_timer(torch, stream))
+    clk = clocks.stop() if rank == 0 else None
+    launches = lib.launch_count() - n0
+    trace = lib.trace_read(64 * args.steps + 64)
+    lib.trace_enable(0)
+    status = lib.poll_status(ws)
+    if status != 0:
+        raise RuntimeError(f"kernel status {status} after the timed region")
+    if rank != 0:
+        return 0
+    per_kind = {}
+    for k, ms in trace:
+        a = per_kind.setdefault(k, [0, 0.0])
+        a[0] += 1
+        a[1] += ms
+    flops = qkvo_kernel_flops(cfg)
+    dom = max((k for k in per_kind if k in flops), key=lambda k: per_kind[k][1])
+    dom_ms_step = per_kind[dom][1] / args.steps
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops_sustained"])
+    achieved = flops[dom] / (dom_ms_step * 1e-3) / 1e12
+    ms_step = secs / args.steps * 1e3
+    tflops = cfg.flops() / (ms_step * 1e-3) / 1e12
+    name = (f"{cfg.name}-shaped LoRA Q/K/V+O fwd+bwd: M={cfg.M} tokens ({cfg.batch}x{cfg.seq}), h={h}, "
+            f"{cfg.heads_q}/{cfg.heads_kv} heads x {cfg.head_dim}, r={r}, alpha={cfg.alpha:g}"
+            + (", RoPE on q and k (base 10000, positions restart per sequence)" if args.rope else ""))
+    line = {
+        "metric": "LoRA Q/K/V+O fwd+bwd tokens/s", "value": world * M * args.steps / secs, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded generator)",
+        "config": {"workload": name, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2"},
+        "tflops": tflops, "pct_of_peak": 100.0 * tflops / peak, "peak_tflops": peak,
+        "peak_source": f"{peak_src} bf16_tflops_sustained",
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "ms_per_step": dom_ms_step,
+                     "flops_per_step": flops[dom]},
+        "kernels_ms_per_step": {k: v[1] / args.steps for k, v in sorted(per_kind.items())},
+        "gpu_launches": launches, "clocks": clk, "e2e": None, "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -480,13 +573,21 @@ def main(argv=None):
                     help="override the workload's activation")
     ap.add_argument("--per-example", type=int, default=0, metavar="N",
                     help="backward with per-example adapter gradients of N examples (DP-SGD)")
+    ap.add_argument("--rope", action="store_true", help="Q/K/V+O workloads: RoPE on q and k")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    import synth
+    if args.workload not in synth.MLP_CONFIGS and args.workload not in synth.QKVO_CONFIGS:
+        ap.error(f"unknown workload {args.workload}")
     if args.impl == "reference":
+        if args.workload not in synth.MLP_CONFIGS:
+            ap.error("the reference arm times the MLP workloads")
         return run_reference(args)
+    if args.workload in synth.QKVO_CONFIGS:
+        return run_qkvo(args)
     return run_ours(args)
 
 

@@ -78,7 +78,10 @@ typedef enum {
   LORA_ERR_UNSUPPORTED = 3,   /* rank beyond the limits above */
   LORA_ERR_WORKSPACE = 4,     /* ws_bytes below the workspace query */
   LORA_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
-  LORA_ERR_TIMEOUT = 6        /* a kernel's bounded wait expired (read by lora_poll_status) */
+  LORA_ERR_TIMEOUT = 6,       /* a kernel's bounded wait expired (read by lora_poll_status) */
+  LORA_ERR_DEVICE_INPUT = 7   /* a value in device memory was out of range: a RoPE position
+                                 outside [0, n_pos) (read by lora_poll_status; position 0
+                                 was used in its place) */
 } lora_status_t;
 
 /* One frozen base weight and its adapter: device pointers, bf16, row-major.
@@ -166,6 +169,31 @@ lora_status_t lora_mlp_backward_per_example(int64_t M, int64_t h, int64_t i, int
                                             lora_grads_t d_up, lora_grads_t d_down, float* sq_norms,
                                             void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Rotary position embedding of q and k ("Model Patches and Kernels", section "Rotary
+ * position embeddings (RoPE)": q and k rotated together, GQA head counts; RoFormer's
+ * position encoding).  Every head (head_dim features) of q and k is rotated pair by
+ * pair, the pair being features (c, c + head_dim/2) of the head:
+ *   q'[c] = q[c] cos - q[c + d/2] sin,  q'[c + d/2] = q[c + d/2] cos + q[c] sin,
+ * with cos, sin = cos[pos[m]][c], sin[pos[m]][c] for token m.  The tables are the
+ * caller's (lora_rope_table fills RoFormer's p * base^(-2c/d); scaled variants are
+ * any other table).  Device pointers: cos, sin f32 [n_pos x head_dim/2] row-major,
+ * 16-byte aligned; pos int32 [M], 4-byte aligned.  head_dim is 64, 128 or 256 and
+ * divides n_q and n_kv.  A position outside [0, n_pos) is read as 0 and reported by
+ * lora_poll_status as LORA_ERR_DEVICE_INPUT. */
+typedef struct {
+  const float* cos;
+  const float* sin;
+  const int32_t* pos;
+  int64_t n_pos;
+  int head_dim;
+} lora_rope_t;
+
+/* Fills cos/sin [n_pos x head_dim/2] (f32, device, 16-byte aligned) with the cosine
+ * and sine of p * base^(-2c/head_dim), computed in double and rounded once.
+ * head_dim even and >= 2, n_pos >= 1, base > 0, else LORA_ERR_INVALID_ARG. */
+lora_status_t lora_rope_table(float* cos, float* sin, int64_t n_pos, int head_dim, double base,
+                              cudaStream_t stream);
+
 /* ---------------------------------------------------------------- Q/K/V + O
  * q = (1)(x; q) [M x n_q], k, v = (1)(x; k or v) [M x n_kv] ("opake_lora_qkv"), and
  * yo = (1)(o_in; o) [M x h] with W_o [h x n_q] ("original_apply_o").  Attention runs
@@ -174,22 +202,27 @@ lora_status_t lora_mlp_backward_per_example(int64_t M, int64_t h, int64_t i, int
  * biases of q, k and v, bf16 [n_q + 2 n_kv] (q's, then k's, then v's), 16-byte
  * aligned, added to q, k, v ("Fused LoRA operations": QKV fusion supports optional
  * frozen base-layer biases); a frozen bias gets no gradient, so backward does not
- * take it. */
+ * take it.  rope is NULL or the rotary embedding applied to q and k after the bias,
+ * in the projection's epilogue (lora_rope_t above; ignored when x == NULL). */
 size_t lora_qkvo_saved_bytes(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r);
 size_t lora_qkvo_workspace_bytes(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r);
 lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r, float s,
                                 const void* x, lora_linear_t q, lora_linear_t k,
                                 lora_linear_t v, void* yq, void* yk, void* yv,
                                 const void* o_in, lora_linear_t o, void* yo,
-                                const void* bias_qkv, void* saved,
+                                const void* bias_qkv, const lora_rope_t* rope, void* saved,
                                 void* ws, size_t ws_bytes, cudaStream_t stream);
 /* Gradients of <dyq, q> + <dyk, k> + <dyv, v> (dx = their sum over the three
  * projections, and dA/dB of q, k, v) and of <dyo, yo> (do_in and dA/dB of o).
- * x == NULL skips the q/k/v half, o_in == NULL the O half. */
+ * x == NULL skips the q/k/v half, o_in == NULL the O half.  With rope (the one the
+ * forward used), dyq and dyk are gradients of the rotated q and k: they are turned
+ * back by the transpose rotation (into the workspace) before the projections'
+ * backward. */
 lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r, float s,
                                  const void* x, lora_linear_t q, lora_linear_t k,
                                  lora_linear_t v, const void* o_in, lora_linear_t o,
-                                 const void* saved, const void* dyq, const void* dyk,
+                                 const void* saved, const lora_rope_t* rope,
+                                 const void* dyq, const void* dyk,
                                  const void* dyv, void* dx, const void* dyo, void* do_in,
                                  lora_grads_t d_q, lora_grads_t d_k, lora_grads_t d_v,
                                  lora_grads_t d_o, void* ws, size_t ws_bytes,
@@ -197,8 +230,9 @@ lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv
 
 /* ---------------------------------------------------------------- status, counters
  * lora_poll_status: synchronises `stream`, reads the asynchronous status word in
- * ws (LORA_OK or LORA_ERR_TIMEOUT), clears it, and returns it (LORA_ERR_CUDA if the
- * synchronisation itself fails). */
+ * ws, clears it, and returns LORA_OK, LORA_ERR_TIMEOUT or LORA_ERR_DEVICE_INPUT
+ * (timeout first when both are set; LORA_ERR_CUDA if the synchronisation itself
+ * fails). */
 lora_status_t lora_poll_status(void* ws, cudaStream_t stream);
 const char* lora_status_string(lora_status_t status);
 /* Kernels this library has launched in this process (all entry points). */
@@ -243,7 +277,8 @@ enum {
   LORA_KIND_GATE_UP = 4,     /* gate/up GEMM with the activation epilogue */
   LORA_KIND_PROJ = 5,        /* plain projection GEMM (down, q/k/v, o) */
   LORA_KIND_ACT_BWD = 6,     /* dh GEMM with the activation-derivative epilogue */
-  LORA_KIND_DGRAD = 7        /* input-gradient GEMM (dx, d o_in) */
+  LORA_KIND_DGRAD = 7,       /* input-gradient GEMM (dx, d o_in) */
+  LORA_KIND_ROPE = 8         /* RoPE transpose rotation of dy_q, dy_k; RoPE tables */
 };
 lora_status_t lora_trace_enable(int capacity);
 int lora_trace_read(int* kind, float* ms, int max);

@@ -21,9 +21,9 @@ from . import build as _build
 
 ACT = {"swiglu": 0, "geglu_tanh": 1, "geglu_erf": 2}
 KIND_NAMES = {0: "pack", 1: "reduce", 2: "rank_proj", 3: "rank_grad", 4: "gate_up",
-              5: "proj", 6: "act_bwd", 7: "dgrad"}
+              5: "proj", 6: "act_bwd", 7: "dgrad", 8: "rope"}
 STATUS = {0: "ok", 1: "invalid argument", 2: "alignment", 3: "unsupported",
-          4: "workspace too small", 5: "CUDA error", 6: "timeout"}
+          4: "workspace too small", 5: "CUDA error", 6: "timeout", 7: "device input out of range"}
 
 
 class LoraError(RuntimeError):
@@ -39,6 +39,11 @@ class LoraLinear(ctypes.Structure):
 
 class LoraGrads(ctypes.Structure):
     _fields_ = [("dA", ctypes.c_void_p), ("dB", ctypes.c_void_p)]
+
+
+class LoraRope(ctypes.Structure):
+    _fields_ = [("cos", ctypes.c_void_p), ("sin", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+                ("n_pos", ctypes.c_int64), ("head_dim", ctypes.c_int)]
 
 
 _LIB = None
@@ -64,11 +69,13 @@ _SIGS = {
                                              _SZ, _VP]),
     "lora_qkvo_saved_bytes": (_SZ, [_I64, _I64, _I64, _I64, _INT]),
     "lora_qkvo_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64, _INT]),
+    "lora_rope_table": (_INT, [_VP, _VP, _I64, _INT, ctypes.c_double, _VP]),
     "lora_qkvo_forward": (_INT, [_I64, _I64, _I64, _I64, _INT, _F32, _VP, LoraLinear, LoraLinear, LoraLinear,
-                                 _VP, _VP, _VP, _VP, LoraLinear, _VP, _VP, _VP, _VP, _SZ, _VP]),
+                                 _VP, _VP, _VP, _VP, LoraLinear, _VP, _VP, ctypes.POINTER(LoraRope), _VP, _VP,
+                                 _SZ, _VP]),
     "lora_qkvo_backward": (_INT, [_I64, _I64, _I64, _I64, _INT, _F32, _VP, LoraLinear, LoraLinear, LoraLinear,
-                                  _VP, LoraLinear, _VP, _VP, _VP, _VP, _VP, _VP, _VP, LoraGrads, LoraGrads,
-                                  LoraGrads, LoraGrads, _VP, _SZ, _VP]),
+                                  _VP, LoraLinear, _VP, ctypes.POINTER(LoraRope), _VP, _VP, _VP, _VP, _VP, _VP,
+                                  LoraGrads, LoraGrads, LoraGrads, LoraGrads, _VP, _SZ, _VP]),
     "lora_poll_status": (_INT, [_VP, _VP]),
     "lora_status_string": (ctypes.c_char_p, [_INT]),
     "lora_launch_count": (ctypes.c_uint64, []),
@@ -304,10 +311,36 @@ def mlp_backward_per_example(x, gate, up, down, s, act, saved, dy, n_examples, *
 
 # ------------------------------------------------------------------ Q/K/V + O
 
-def qkvo_forward(x, q, k, v, o_in, o, s, *, bias=None, saved=None, training=True, ws=None, outs=None):
+def rope_table(n_pos: int, head_dim: int, base: float = 10000.0, device="cuda"):
+    """(cos, sin), f32 [n_pos, head_dim/2] on `device`: the angle p * base^(-2c/head_dim)."""
+    dev = torch.device(device)
+    cos = torch.empty(n_pos, head_dim // 2, dtype=torch.float32, device=dev)
+    sin = torch.empty_like(cos)
+    _check(load().lora_rope_table(cos.data_ptr(), sin.data_ptr(), n_pos, head_dim, float(base), _stream(dev)),
+           "lora_rope_table")
+    return cos, sin
+
+
+def _rope(rope):
+    """None, or dict(cos, sin, pos, head_dim): f32 tables [n_pos, head_dim/2] and int32
+    positions [M] on the device."""
+    if rope is None:
+        return None
+    cos, sin, pos = rope["cos"], rope["sin"], rope["pos"]
+    for t, dt, name in ((cos, torch.float32, "cos"), (sin, torch.float32, "sin"), (pos, torch.int32, "pos")):
+        if t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"rope {name}: contiguous {dt} on the GPU expected")
+    if cos.shape != sin.shape or cos.shape[1] * 2 != rope["head_dim"]:
+        raise ValueError("rope tables must be [n_pos, head_dim/2]")
+    return ctypes.pointer(LoraRope(cos.data_ptr(), sin.data_ptr(), pos.data_ptr(), cos.shape[0], rope["head_dim"]))
+
+
+def qkvo_forward(x, q, k, v, o_in, o, s, *, bias=None, rope=None, saved=None, training=True, ws=None,
+                 outs=None):
     """q/k/v from x (skipped if x is None) and the O projection of o_in (skipped if
     o_in is None).  bias: None or the frozen q/k/v biases, one bf16 tensor
-    [n_q + 2 n_kv].  Returns (dict(q, k, v, o), saved)."""
+    [n_q + 2 n_kv].  rope: None or dict(cos, sin, pos, head_dim), applied to q and k.
+    Returns (dict(q, k, v, o), saved)."""
     lib = load()
     ref = x if x is not None else o_in
     dev = ref.device
@@ -335,13 +368,16 @@ def qkvo_forward(x, q, k, v, o_in, o, s, *, bias=None, saved=None, training=True
         _lin(v, "v") if x is not None else z,
         _opt(res.get("q"), "yq"), _opt(res.get("k"), "yk"), _opt(res.get("v"), "yv"),
         _opt(o_in, "o_in"), _lin(o, "o") if o_in is not None else z, _opt(res.get("o"), "yo"),
-        _opt(bias, "bias"), None if saved is None else saved.data_ptr(), ws.data_ptr(), ws.numel(), _stream(dev)),
+        _opt(bias, "bias"), _rope(rope), None if saved is None else saved.data_ptr(), ws.data_ptr(), ws.numel(),
+        _stream(dev)),
         "lora_qkvo_forward")
     return res, saved
 
 
-def qkvo_backward(x, q, k, v, o_in, o, s, saved, dyq=None, dyk=None, dyv=None, dyo=None, *, ws=None):
-    """Returns dict(dx, do_in, dA_q, dB_q, ..., dA_o, dB_o) for the halves present."""
+def qkvo_backward(x, q, k, v, o_in, o, s, saved, dyq=None, dyk=None, dyv=None, dyo=None, *, rope=None,
+                  ws=None):
+    """Returns dict(dx, do_in, dA_q, dB_q, ..., dA_o, dB_o) for the halves present.
+    With rope (the forward's), dyq and dyk are gradients of the rotated q and k."""
     lib = load()
     ref = x if x is not None else o_in
     dev = ref.device
@@ -368,7 +404,7 @@ def qkvo_backward(x, q, k, v, o_in, o, s, saved, dyq=None, dyk=None, dyv=None, d
         M, h, nq, nkv, r, s, _opt(x, "x"),
         _lin(q, "q") if x is not None else zl, _lin(k, "k") if x is not None else zl,
         _lin(v, "v") if x is not None else zl, _opt(o_in, "o_in"),
-        _lin(o, "o") if o_in is not None else zl, saved.data_ptr(),
+        _lin(o, "o") if o_in is not None else zl, saved.data_ptr(), _rope(rope),
         _opt(dyq, "dyq"), _opt(dyk, "dyk"), _opt(dyv, "dyv"), _opt(out.get("dx"), "dx"),
         _opt(dyo, "dyo"), _opt(out.get("do_in"), "do_in"), gr("q"), gr("k"), gr("v"), gr("o"),
         ws.data_ptr(), ws.numel(), _stream(dev)), "lora_qkvo_backward")

@@ -68,4 +68,33 @@ struct NormParams {
   float* out;                           // [examples]
 };
 
+// RoPE helpers ("Model Patches and Kernels", RoPE):
+//  * rope_rotate: rotates the heads of up to two bf16 [M x n] tensors pair by pair,
+//    (c, c + half) of each head, by sign * the angle of each token's position (sign
+//    -1: the transpose rotation, which turns the gradient of rotated q, k into the
+//    gradient of the projections' outputs).
+//  * rope_table: cos and sin of p * base^(-2i/head_dim), computed in double.
+struct RopeParams {
+  const __nv_bfloat16* src[2];
+  __nv_bfloat16* dst[2];
+  long long n[2];          // columns of each tensor (a multiple of 2 * half)
+  int ntensors;
+  long long M;
+  const float* cos;        // [npos x half]
+  const float* sin;
+  const int* pos;          // [M]
+  int half;
+  int npos;
+  float sign;
+  unsigned* status;
+};
+
+struct RopeTableParams {
+  float* cos;
+  float* sin;
+  long long npos;
+  int half;
+  double base;
+};
+
 }  // namespace lgb

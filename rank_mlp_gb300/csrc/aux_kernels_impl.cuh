@@ -1,8 +1,10 @@
-// Kernel bodies of the pack and reduce kernels (parameter structs in aux_kernels.cuh).
+// Kernel bodies of the pack, reduce, norms and RoPE kernels (parameter structs in
+// aux_kernels.cuh).
 // Included by exactly one translation unit, the one that launches them.
 #pragma once
 
 #include "aux_kernels.cuh"
+#include "gemm_tc.cuh"
 
 namespace lgb {
 
@@ -69,6 +71,65 @@ __global__ void __launch_bounds__(256) norms_kernel(const __grid_constant__ Norm
     __syncthreads();
   }
   if (threadIdx.x == 0) p.out[e] = red[0];
+}
+
+// One thread per 8 pairs: columns [c, c + 8) and [c + half, c + half + 8) of a head.
+__global__ void __launch_bounds__(256) rope_rotate_kernel(const __grid_constant__ RopeParams p) {
+  const int t = blockIdx.y;
+  const long long groups_per_row = p.n[t] / 16;       // (n / head_dim) heads x (half / 8)
+  const long long total = p.M * groups_per_row;
+  const int gph = p.half / 8;
+  for (long long it = blockIdx.x * 256ll + threadIdx.x; it < total; it += 256ll * gridDim.x) {
+    const long long m = it / groups_per_row;
+    const int rem = static_cast<int>(it - m * groups_per_row);
+    const int head = rem / gph, g = rem - head * gph;
+    const long long ca = static_cast<long long>(head) * 2 * p.half + 8 * g, cb = ca + p.half;
+    int pos = __ldg(p.pos + m);
+    if (pos < 0 || pos >= p.npos) {
+      if (p.status) atomicOr(p.status, kStatusInput);
+      pos = 0;
+    }
+    const uint4 ua = __ldg(reinterpret_cast<const uint4*>(p.src[t] + m * p.n[t] + ca));
+    const uint4 ub = __ldg(reinterpret_cast<const uint4*>(p.src[t] + m * p.n[t] + cb));
+    const float4* cr = reinterpret_cast<const float4*>(p.cos + static_cast<long long>(pos) * p.half + 8 * g);
+    const float4* sr = reinterpret_cast<const float4*>(p.sin + static_cast<long long>(pos) * p.half + 8 * g);
+    const float4 c0 = __ldg(cr), c1 = __ldg(cr + 1), s0 = __ldg(sr), s1 = __ldg(sr + 1);
+    const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+    uint32_t oa[4], ob[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float ra[2], rb[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float x0 = h ? __uint_as_float(wa[e] & 0xFFFF0000u) : __uint_as_float(wa[e] << 16);
+        const float x1 = h ? __uint_as_float(wb[e] & 0xFFFF0000u) : __uint_as_float(wb[e] << 16);
+        const float c = cc[2 * e + h], sn = p.sign * ss[2 * e + h];
+        ra[h] = x0 * c - x1 * sn;
+        rb[h] = x1 * c + x0 * sn;
+      }
+      __nv_bfloat162 va = __floats2bfloat162_rn(ra[0], ra[1]);
+      __nv_bfloat162 vb = __floats2bfloat162_rn(rb[0], rb[1]);
+      oa[e] = *reinterpret_cast<uint32_t*>(&va);
+      ob[e] = *reinterpret_cast<uint32_t*>(&vb);
+    }
+    *reinterpret_cast<uint4*>(p.dst[t] + m * p.n[t] + ca) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+    *reinterpret_cast<uint4*>(p.dst[t] + m * p.n[t] + cb) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+  }
+}
+
+__global__ void __launch_bounds__(256) rope_table_kernel(const __grid_constant__ RopeTableParams p) {
+  const long long total = p.npos * p.half;
+  for (long long it = blockIdx.x * 256ll + threadIdx.x; it < total; it += 256ll * gridDim.x) {
+    const long long pos = it / p.half;
+    const int i = static_cast<int>(it - pos * p.half);
+    const double theta = pow(p.base, -static_cast<double>(i) / p.half);   // base^(-2i/d)
+    double sn, cs;
+    sincos(static_cast<double>(pos) * theta, &sn, &cs);
+    p.cos[it] = static_cast<float>(cs);
+    p.sin[it] = static_cast<float>(sn);
+  }
 }
 
 }  // namespace lgb

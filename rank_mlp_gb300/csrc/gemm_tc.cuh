@@ -30,8 +30,9 @@ constexpr int kMaxMaps = 12;
 constexpr int kMaxGroups = 3;
 constexpr int kMaxSegs = 4;
 constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusInput = 2u;   // a device-side input out of range (a RoPE position)
 
-enum EpiKind : int { EPI_STORE = 0, EPI_ACT_FWD = 1, EPI_ACT_BWD = 2, EPI_PARTIAL = 3 };
+enum EpiKind : int { EPI_STORE = 0, EPI_ACT_FWD = 1, EPI_ACT_BWD = 2, EPI_PARTIAL = 3, EPI_ROPE = 4 };
 enum ActKind : int { ACT_SWIGLU = 0, ACT_GEGLU_TANH = 1, ACT_GEGLU_ERF = 2 };
 
 struct SegDesc {
@@ -70,6 +71,12 @@ struct TcParams {
   unsigned long long timeout_ns;
   int inject_stall;          // failure-path tests only: the first stage of the first unit
                              // is never filled, so the waits on it run out
+  // EPI_ROPE groups: cos/sin tables [rope_npos x rope_half] f32, token positions [M]
+  const float* rope_cos;
+  const float* rope_sin;
+  const int* rope_pos;
+  int rope_half;             // head_dim / 2: 32, 64 or 128
+  int rope_npos;
 };
 
 template <int BN, int STAGES>
@@ -359,6 +366,83 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
         for (int j = 0; j < 4; ++j) {
           gw[j] = gn[j];
           uw[j] = un[j];
+        }
+      }
+    }
+  } else if (G.epi == EPI_ROPE) {
+    // EPI_STORE (bias included) followed by the rotary embedding of every head in the
+    // tile ("Model Patches and Kernels", RoPE): the pair (c, c + half) of a head turns
+    // by the angle of this token's position.  Heads never straddle a 256-column tile
+    // (head_dim divides 256) and the whole row of the tile is this thread's (nparts 1).
+    if constexpr (BN == 256) {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(G.out0);
+      const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(G.in0);
+      const bool v8 = rows_v8_aligned(out, G.ldo);
+      const int half = p.rope_half;
+      int pos = 0;
+      if (row_ok) {
+        pos = __ldg(p.rope_pos + row);
+        if (pos < 0 || pos >= p.rope_npos) {
+          if (p.status) atomicOr(p.status, kStatusInput);
+          pos = 0;
+        }
+      }
+      const float* crow = p.rope_cos + static_cast<long long>(pos) * half;
+      const float* srow = p.rope_sin + static_cast<long long>(pos) * half;
+#pragma unroll 1
+      for (int hb = 0; hb < BN; hb += 2 * half) {
+#pragma unroll 1
+        for (int c = 0; c < half; c += 32) {
+          uint32_t va[32], vb[32];
+          __syncwarp();
+          tmem_ld32(tacc + hb + c, va);
+          tmem_ld32(tacc + hb + half + c, vb);
+          tmem_ld_wait();
+          const int cola = U.tn * BN + hb + c, colb = cola + half;
+          if (row_ok && cola < G.N) {     // N is a multiple of head_dim: colb < N too
+            float a[32], b[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              a[e] = __uint_as_float(va[e]);
+              b[e] = __uint_as_float(vb[e]);
+            }
+            if (bias != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint4 ba = __ldg(reinterpret_cast<const uint4*>(bias + cola + 8 * j));
+                const uint4 bb = __ldg(reinterpret_cast<const uint4*>(bias + colb + 8 * j));
+                const uint32_t xa[4] = {ba.x, ba.y, ba.z, ba.w}, xb[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  a[8 * j + 2 * e] += bf16_lo(xa[e]);
+                  a[8 * j + 2 * e + 1] += bf16_hi(xa[e]);
+                  b[8 * j + 2 * e] += bf16_lo(xb[e]);
+                  b[8 * j + 2 * e + 1] += bf16_hi(xb[e]);
+                }
+              }
+            }
+            uint32_t wa[16], wb[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 cs = __ldg(reinterpret_cast<const float4*>(crow + c) + j);
+              const float4 sn = __ldg(reinterpret_cast<const float4*>(srow + c) + j);
+              const float cc[4] = {cs.x, cs.y, cs.z, cs.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
+              float ra[4], rb[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float x0 = a[4 * j + e], x1 = b[4 * j + e];
+                ra[e] = x0 * cc[e] - x1 * ss[e];
+                rb[e] = x1 * cc[e] + x0 * ss[e];
+              }
+              wa[2 * j] = pack_bf16x2(ra[0], ra[1]);
+              wa[2 * j + 1] = pack_bf16x2(ra[2], ra[3]);
+              wb[2 * j] = pack_bf16x2(rb[0], rb[1]);
+              wb[2 * j + 1] = pack_bf16x2(rb[2], rb[3]);
+            }
+            __nv_bfloat16* orow = out + static_cast<long long>(row) * G.ldo;
+            store_row32_bf16(orow + cola, wa, cola, G.N, v8);
+            store_row32_bf16(orow + colb, wb, colb, G.N, v8);
+          }
         }
       }
     }

@@ -5,8 +5,8 @@
 #include <mutex>
 #include <vector>
 
-#include "aux_kernels_impl.cuh"
 #include "host.cuh"
+#include "aux_kernels_impl.cuh"
 
 namespace lgb {
 
@@ -165,6 +165,21 @@ lora_status_t launch_reduce(const RedParams& p, cudaStream_t st) {
   gx = gx > 2048 ? 2048 : gx;
   const int slot = trace_begin(LORA_KIND_REDUCE, st);
   reduce_kernel<<<dim3(static_cast<unsigned>(gx), p.nout), 256, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  trace_end(slot, st);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return LORA_OK;
+}
+
+lora_status_t launch_rope(const RopeParams& p, cudaStream_t st) {
+  if (p.ntensors == 0 || p.M == 0) return LORA_OK;
+  long long most = 1;
+  for (int t = 0; t < p.ntensors; ++t) most = p.M * (p.n[t] / 16) > most ? p.M * (p.n[t] / 16) : most;
+  long long gx = ceil_div(most, 256);
+  gx = gx > 4 * num_sms() ? 4 * num_sms() : gx;
+  const int slot = trace_begin(LORA_KIND_ROPE, st);
+  rope_rotate_kernel<<<dim3(static_cast<unsigned>(gx), p.ntensors), 256, 0, st>>>(p);
   cudaError_t e = cudaGetLastError();
   trace_end(slot, st);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
@@ -923,6 +938,8 @@ QkvoLayout qkvo_layout(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r) {
     c.take_n<bf16>(kfo * nq);
     c.take_n<bf16>(M * kfo);
     c.take_n<bf16>(M * kfq);
+    c.take_n<bf16>(M * nq);     // dy_q, dy_k turned back by the transpose RoPE rotation
+    c.take_n<bf16>(M * nkv);
     const int64_t f3[3] = {nq, nkv, nkv};
     const int64_t cand[] = {rank_projection_part(M, kfo, ceil_div(h, kBK)),
                             token_grad_part(M, kfo, &h, 1),
@@ -942,6 +959,18 @@ QkvoLayout qkvo_layout(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r) {
     L.saved = c.off;
   }
   return L;
+}
+
+// RoPE arguments: NULL is "no RoPE"; otherwise the rules of lora_rope_t.
+lora_status_t check_rope(const lora_rope_t* rope, int64_t nq, int64_t nkv) {
+  if (rope == nullptr) return LORA_OK;
+  if (!rope->cos || !rope->sin || !rope->pos || rope->n_pos < 1 || rope->n_pos > 0x7fffffff)
+    return LORA_ERR_INVALID_ARG;
+  const int d = rope->head_dim;
+  if (d != 64 && d != 128 && d != 256) return LORA_ERR_UNSUPPORTED;
+  if (nq % d || nkv % d) return LORA_ERR_INVALID_ARG;
+  if (!aligned(rope->cos, 16) || !aligned(rope->sin, 16) || !aligned(rope->pos, 4)) return LORA_ERR_ALIGNMENT;
+  return LORA_OK;
 }
 
 lora_status_t check_qkvo(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r, float s) {
@@ -970,10 +999,11 @@ extern "C" size_t lora_qkvo_workspace_bytes(int64_t M, int64_t h, int64_t n_q, i
 extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r, float s,
                                            const void* x, lora_linear_t q, lora_linear_t k, lora_linear_t v,
                                            void* yq, void* yk, void* yv, const void* o_in, lora_linear_t o,
-                                           void* yo, const void* bias_qkv, void* saved, void* ws,
-                                           size_t ws_bytes, cudaStream_t stream) {
+                                           void* yo, const void* bias_qkv, const lora_rope_t* rope,
+                                           void* saved, void* ws, size_t ws_bytes, cudaStream_t stream) {
   LGB_TRY(check_qkvo(M, h, n_q, n_kv, r, s));
   if (!ws || (!x && !o_in)) return LORA_ERR_INVALID_ARG;
+  if (x) LGB_TRY(check_rope(rope, n_q, n_kv));
   if (bias_qkv != nullptr && !aligned(bias_qkv, 16)) return LORA_ERR_ALIGNMENT;
   if (x && ((M > 0 && (!yq || !yk || !yv)) || !lin_ok(q) || !lin_ok(k) || !lin_ok(v))) return LORA_ERR_INVALID_ARG;
   if (o_in && ((M > 0 && !yo) || !lin_ok(o))) return LORA_ERR_INVALID_ARG;
@@ -1031,8 +1061,16 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
     bf16* bfs[3] = {bfq, bfk, bfv};
     void* ys[3] = {yq, yk, yv};
     const int64_t ns[3] = {n_q, n_kv, n_kv};
+    if (rope != nullptr) {
+      g.p.rope_cos = rope->cos;
+      g.p.rope_sin = rope->sin;
+      g.p.rope_pos = rope->pos;
+      g.p.rope_half = rope->head_dim / 2;
+      g.p.rope_npos = static_cast<int>(rope->n_pos);
+    }
     for (int p = 0; p < 3; ++p) {
-      GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(ns[p]), EPI_STORE, false);
+      const int epi = (rope != nullptr && p < 2) ? EPI_ROPE : EPI_STORE;
+      GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(ns[p]), epi, false);
       GemmPlan::seg(G, ax, g.b_kmajor(lins[p]->W, ns[p], h, h, g.b_rows_full()), -1, h, h);
       GemmPlan::seg(G, at, g.b_kmajor(bfs[p], ns[p], kfq, kfq, g.b_rows_full()), -1, kfq, (p + 1) * r);
       G.out0 = ys[p];
@@ -1064,12 +1102,14 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
 extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r, float s,
                                             const void* x, lora_linear_t q, lora_linear_t k, lora_linear_t v,
                                             const void* o_in, lora_linear_t o, const void* saved,
-                                            const void* dyq, const void* dyk, const void* dyv, void* dx,
+                                            const lora_rope_t* rope, const void* dyq, const void* dyk,
+                                            const void* dyv, void* dx,
                                             const void* dyo, void* do_in, lora_grads_t d_q, lora_grads_t d_k,
                                             lora_grads_t d_v, lora_grads_t d_o, void* ws, size_t ws_bytes,
                                             cudaStream_t stream) {
   LGB_TRY(check_qkvo(M, h, n_q, n_kv, r, s));
   if (!ws || !saved || (!x && !o_in)) return LORA_ERR_INVALID_ARG;
+  if (x) LGB_TRY(check_rope(rope, n_q, n_kv));
   if (x && ((M > 0 && (!dyq || !dyk || !dyv || !dx)) || !lin_ok(q) || !lin_ok(k) || !lin_ok(v) || !d_q.dA || !d_q.dB ||
             !d_k.dA || !d_k.dB || !d_v.dA || !d_v.dB))
     return LORA_ERR_INVALID_ARG;
@@ -1113,6 +1153,8 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
   bf16* af_o = c.take_n<bf16>(kfo * n_q);
   bf16* uo = c.take_n<bf16>(M * kfo);
   bf16* V = c.take_n<bf16>(M * kfq);
+  bf16* dyq_r = c.take_n<bf16>(M * n_q);
+  bf16* dyk_r = c.take_n<bf16>(M * n_kv);
   float* part = reinterpret_cast<float*>(c.take(0));
 
   PackParams pk;
@@ -1151,6 +1193,29 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     LGB_TRY(token_grads(M, r, kfo, s, uo, &j2, 1, part, status, stream));
   }
   if (x) {
+    if (rope != nullptr) {
+      // gradients of the rotated q, k -> gradients of the projections' outputs
+      RopeParams rp;
+      std::memset(static_cast<void*>(&rp), 0, sizeof(rp));
+      rp.src[0] = static_cast<const bf16*>(dyq);
+      rp.src[1] = static_cast<const bf16*>(dyk);
+      rp.dst[0] = dyq_r;
+      rp.dst[1] = dyk_r;
+      rp.n[0] = n_q;
+      rp.n[1] = n_kv;
+      rp.ntensors = 2;
+      rp.M = M;
+      rp.cos = rope->cos;
+      rp.sin = rope->sin;
+      rp.pos = rope->pos;
+      rp.half = rope->head_dim / 2;
+      rp.npos = static_cast<int>(rope->n_pos);
+      rp.sign = -1.0f;
+      rp.status = status;
+      LGB_TRY(launch_rope(rp, stream));
+      dyq = dyq_r;
+      dyk = dyk_r;
+    }
     const ProjSeg p3[3] = {{dyq, btq, n_q}, {dyk, btk, n_kv}, {dyv, btv, n_kv}};
     LGB_TRY(rank_projection(M, kfq, p3, 3, V, part, status, stream));
     const GradJob j3[3] = {{dyq, n_q, 0, d_q.dB, 0}, {dyk, n_kv, r, d_k.dB, 0}, {dyv, n_kv, 2 * r, d_v.dB, 0}};
@@ -1185,7 +1250,30 @@ extern "C" lora_status_t lora_poll_status(void* ws, cudaStream_t stream) {
     if (cudaMemsetAsync(ws, 0, sizeof(unsigned), stream) != cudaSuccess) return LORA_ERR_CUDA;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return LORA_ERR_CUDA;
   }
-  return (host & kStatusTimeout) ? LORA_ERR_TIMEOUT : LORA_OK;
+  if (host & kStatusTimeout) return LORA_ERR_TIMEOUT;
+  return (host & kStatusInput) ? LORA_ERR_DEVICE_INPUT : LORA_OK;
+}
+
+extern "C" lora_status_t lora_rope_table(float* cos, float* sin, int64_t n_pos, int head_dim, double base,
+                                         cudaStream_t stream) {
+  if (!cos || !sin || n_pos < 1 || head_dim < 2 || head_dim % 2 || !(base > 0.0) || !std::isfinite(base))
+    return LORA_ERR_INVALID_ARG;
+  if (!aligned(cos, 16) || !aligned(sin, 16)) return LORA_ERR_ALIGNMENT;
+  RopeTableParams p;
+  p.cos = cos;
+  p.sin = sin;
+  p.npos = n_pos;
+  p.half = head_dim / 2;
+  p.base = base;
+  long long gx = ceil_div(n_pos * p.half, 256);
+  gx = gx > 4 * num_sms() ? 4 * num_sms() : gx;
+  const int slot = trace_begin(LORA_KIND_ROPE, stream);
+  rope_table_kernel<<<static_cast<unsigned>(gx), 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  trace_end(slot, stream);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return LORA_OK;
 }
 
 extern "C" const char* lora_status_string(lora_status_t status) {
@@ -1197,6 +1285,7 @@ extern "C" const char* lora_status_string(lora_status_t status) {
     case LORA_ERR_WORKSPACE: return "workspace smaller than the size query";
     case LORA_ERR_CUDA: return "CUDA runtime or launch failure";
     case LORA_ERR_TIMEOUT: return "a kernel's bounded wait expired";
+    case LORA_ERR_DEVICE_INPUT: return "a device-side input was out of range (RoPE position)";
   }
   return "unknown status";
 }

@@ -55,23 +55,27 @@ def mlp_oracle(v: dict, cfg, s=None):
     return oracle.mlp_forward(*args), oracle.mlp_backward(*args, v["dy"])
 
 
-def qkvo_gpu(lib, t: dict, cfg, s=None):
+def qkvo_gpu(lib, t: dict, cfg, s=None, rope=None, bias=None):
+    """rope: None or dict(cos, sin, pos, head_dim) of device tensors."""
     s = cfg.s if s is None else s
     lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
-    out, saved = lib.qkvo_forward(t["x"], lin("q"), lin("k"), lin("v"), t["o_in"], lin("o"), s)
+    out, saved = lib.qkvo_forward(t["x"], lin("q"), lin("k"), lin("v"), t["o_in"], lin("o"), s, rope=rope,
+                                  bias=bias)
     g = lib.qkvo_backward(t["x"], lin("q"), lin("k"), lin("v"), t["o_in"], lin("o"), s, saved,
-                          t["dy_q"], t["dy_k"], t["dy_v"], t["dy_o"])
+                          t["dy_q"], t["dy_k"], t["dy_v"], t["dy_o"], rope=rope)
     torch.cuda.synchronize()
     assert lib.poll_status() == 0
     return out, g
 
 
-def qkvo_oracle(v: dict, cfg, s=None):
+def qkvo_oracle(v: dict, cfg, s=None, rope=None, bias=None):
+    """rope: None or dict(cos, sin, pos, head_dim) of numpy arrays (the oracle's own
+    tables); bias: None or (b_q, b_k, b_v)."""
     s = cfg.s if s is None else s
     L = lambda n: (v["W_" + n], v["A_" + n], v["B_" + n])  # noqa: E731
-    f = oracle.qkvo_forward(v["x"], L("q"), L("k"), L("v"), v["o_in"], L("o"), s)
+    f = oracle.qkvo_forward(v["x"], L("q"), L("k"), L("v"), v["o_in"], L("o"), s, bias=bias, rope=rope)
     b = oracle.qkvo_backward(v["x"], L("q"), L("k"), L("v"), v["o_in"], L("o"), s,
-                             v["dy_q"], v["dy_k"], v["dy_v"], v["dy_o"])
+                             v["dy_q"], v["dy_k"], v["dy_v"], v["dy_o"], rope=rope)
     return f, b
 
 

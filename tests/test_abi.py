@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for code in range(7):
+    for code in range(8):
         s = L.lora_status_string(code)
         assert s and s != b"unknown status"
     assert L.lora_status_string(99) == b"unknown status"
@@ -109,12 +109,47 @@ def test_qkvo_rejects_misaligned_bias_and_large_rank(L):
     lin = _lin(L)
     ws = L.lora_qkvo_workspace_bytes(64, 256, 256, 128, 8)
     args = lambda r, bias: (64, 256, 256, 128, r, 2.0, ALIGNED, lin, lin, lin, ALIGNED, ALIGNED, ALIGNED,  # noqa
-                            None, lin, None, bias, None, ALIGNED, ws, None)
+                            None, lin, None, bias, None, None, ALIGNED, ws, None)
     assert L.lora_qkvo_forward(*args(8, ALIGNED + 2)) == 2
     assert L.lora_qkvo_forward(*args(86, None)) == 3
     # both halves skipped: nothing to do is an argument error
     assert L.lora_qkvo_forward(64, 256, 256, 128, 8, 2.0, None, lin, lin, lin, None, None, None,
-                               None, lin, None, None, None, ALIGNED, ws, None) == 1
+                               None, lin, None, None, None, None, ALIGNED, ws, None) == 1
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=96), 3),                # head_dim not 64, 128 or 256
+    (dict(head_dim=256), 1),               # does not divide n_kv = 128
+    (dict(cos=None), 1),
+    (dict(pos=None), 1),
+    (dict(n_pos=0), 1),
+    (dict(cos=ALIGNED + 4), 2),            # tables 16-byte aligned
+    (dict(pos=ALIGNED + 2), 2),            # positions 4-byte aligned
+])
+def test_qkvo_rejects_bad_rope(L, kw, code):
+    import ctypes
+    from rank_mlp_gb300.binding import LoraGrads, LoraRope
+    a = dict(cos=ALIGNED, sin=ALIGNED, pos=ALIGNED, n_pos=2048, head_dim=128)
+    a.update(kw)
+    rope = ctypes.pointer(LoraRope(a["cos"], a["sin"], a["pos"], a["n_pos"], a["head_dim"]))
+    lin = _lin(L)
+    ws = L.lora_qkvo_workspace_bytes(64, 256, 256, 128, 8)
+    before = L.lora_launch_count()
+    assert L.lora_qkvo_forward(64, 256, 256, 128, 8, 2.0, ALIGNED, lin, lin, lin, ALIGNED, ALIGNED, ALIGNED,
+                               None, lin, None, None, rope, None, ALIGNED, ws, None) == code
+    g = LoraGrads(ALIGNED, ALIGNED)
+    assert L.lora_qkvo_backward(64, 256, 256, 128, 8, 2.0, ALIGNED, lin, lin, lin, None, lin, ALIGNED, rope,
+                                ALIGNED, ALIGNED, ALIGNED, ALIGNED, None, None, g, g, g, g, ALIGNED, ws,
+                                None) == code
+    assert L.lora_launch_count() == before
+
+
+def test_rope_table_rejects(L):
+    assert L.lora_rope_table(ALIGNED, ALIGNED, 16, 7, 10000.0, None) == 1     # odd head_dim
+    assert L.lora_rope_table(ALIGNED, ALIGNED, 0, 64, 10000.0, None) == 1     # no positions
+    assert L.lora_rope_table(ALIGNED, ALIGNED, 16, 64, -1.0, None) == 1       # base <= 0
+    assert L.lora_rope_table(ALIGNED, ALIGNED, 16, 64, float("nan"), None) == 1
+    assert L.lora_rope_table(ALIGNED + 4, ALIGNED, 16, 64, 10000.0, None) == 2
 
 
 def test_backward_needs_saved(L):

@@ -45,15 +45,26 @@ def test_mlp_config(lib, name, over):
     gc.collect()
 
 
-def test_qkvo_config(lib):
+@pytest.mark.parametrize("rope", [False, True], ids=["plain", "rope"])
+def test_qkvo_config(lib, rope):
+    """The GQA Q/K/V + O workload; with RoPE on q and k (positions restart every
+    sequence of cfg.seq tokens, base 10000)."""
+    import oracle
     cfg = synth.QKVO_CONFIGS["gqa7b"]
     t = synth.make_qkvo_inputs(cfg, seed=0, device=DEV)
-    out, g = qkvo_gpu(lib, t, cfg)
+    rg = ro = None
+    if rope:
+        pos = synth.positions(cfg.M, seq=cfg.seq)
+        cos, sin = lib.rope_table(cfg.seq, cfg.head_dim, 10000.0, device=DEV)
+        rg = {"cos": cos, "sin": sin, "pos": pos.to(DEV), "head_dim": cfg.head_dim}
+        oc, os_ = oracle.rope_tables(cfg.seq, cfg.head_dim, 10000.0)
+        ro = {"cos": oc, "sin": os_, "pos": pos.numpy().astype(int), "head_dim": cfg.head_dim}
+    out, g = qkvo_gpu(lib, t, cfg, rope=rg)
     got = {**{k: out[k].cpu() for k in out}, **{k: g[k].cpu() for k in g}}
     v = to_f64_dict(t)
-    del t, out, g
+    del t, out, g, rg
     torch.cuda.empty_cache()
-    f, b = qkvo_oracle(v, cfg)
+    f, b = qkvo_oracle(v, cfg, rope=ro)
     for k in ("q", "k", "v", "o"):
         parity(k, got[k], f[k])
     for k in b:
