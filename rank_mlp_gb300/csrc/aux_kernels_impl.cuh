@@ -9,6 +9,8 @@
 namespace lgb {
 
 __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const PackJob& J = p.job[blockIdx.y];
   const long long total = static_cast<long long>(J.rows) * J.cols;
   for (long long idx = blockIdx.x * 256LL + threadIdx.x; idx < total; idx += 256LL * gridDim.x) {
@@ -29,6 +31,8 @@ __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackP
 }
 
 __global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ RedParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const RedOut& O = p.out[blockIdx.y];
   const long long total = static_cast<long long>(O.rows) * O.ncols;
   const long long slab = O.rows_pad * O.width;
@@ -54,6 +58,8 @@ __global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ Red
 }
 
 __global__ void __launch_bounds__(256) norms_kernel(const __grid_constant__ NormParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int e = blockIdx.x;
   float acc = 0.0f;
   for (int t = 0; t < p.ntensors; ++t) {
@@ -75,6 +81,8 @@ __global__ void __launch_bounds__(256) norms_kernel(const __grid_constant__ Norm
 
 // One thread per 8 pairs: columns [c, c + 8) and [c + half, c + half + 8) of a head.
 __global__ void __launch_bounds__(256) rope_rotate_kernel(const __grid_constant__ RopeParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int t = blockIdx.y;
   const long long groups_per_row = p.n[t] / 16;       // (n / head_dim) heads x (half / 8)
   const long long total = p.M * groups_per_row;
@@ -120,6 +128,8 @@ __global__ void __launch_bounds__(256) rope_rotate_kernel(const __grid_constant_
 }
 
 __global__ void __launch_bounds__(256) rope_table_kernel(const __grid_constant__ RopeTableParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   const long long total = p.npos * p.half;
   for (long long it = blockIdx.x * 256ll + threadIdx.x; it < total; it += 256ll * gridDim.x) {
     const long long pos = it / p.half;

@@ -15,8 +15,7 @@ static cudaError_t launch_pair(const TcParams& p, int grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k<<<grid, pair_threads(EPIW), smem, st>>>(p);  // grid is a multiple of the cluster size (2)
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(grid), dim3(pair_threads(EPIW)), smem, st, p);  // grid: a multiple of 2
 }
 
 cudaError_t launch_tc_big(int variant, const TcParams& p, int grid, cudaStream_t st) {

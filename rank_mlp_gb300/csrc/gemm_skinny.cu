@@ -15,8 +15,7 @@ static cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  k<<<grid, kThreads, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, p);
 }
 
 cudaError_t launch_tc_skinny(int variant, const TcParams& p, int grid, cudaStream_t st) {

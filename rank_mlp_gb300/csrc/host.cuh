@@ -8,6 +8,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "lora_gb300.h"
@@ -35,6 +36,33 @@ constexpr bool variant_b_mn(int v) { return v == VP_KMN || v == V64_MNMN || v ==
 // The big projection GEMMs run on CTA pairs (256 x 256 tiles).
 constexpr int kBigKK = VP_KK;
 constexpr int kBigKMN = VP_KMN;
+
+// Programmatic dependent launch for every kernel of the library (on unless the
+// environment sets LORA_PDL=0): a kernel may be scheduled while the previous kernel
+// in the stream drains, runs its prologue (barriers, tensor memory, descriptor
+// prefetch) and then waits in griddepcontrol.wait for that kernel's completion.
+inline bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("LORA_PDL");
+    return !(e != nullptr && e[0] == '0');
+  }();
+  return on;
+}
+
+template <typename Kernel, typename Arg>
+inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const Arg& arg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
 
 // Defined in gemm_big.cu / gemm_skinny.cu.
 cudaError_t launch_tc_big(int variant, const TcParams& p, int grid, cudaStream_t st);

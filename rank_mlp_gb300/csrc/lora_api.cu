@@ -135,8 +135,7 @@ lora_status_t launch_pack(const PackParams& p, cudaStream_t st) {
   int64_t gx = ceil_div(most, 256);
   gx = gx > 1024 ? 1024 : gx;
   const int slot = trace_begin(LORA_KIND_PACK, st);
-  pack_kernel<<<dim3(static_cast<unsigned>(gx), p.njob), 256, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(pack_kernel, dim3(static_cast<unsigned>(gx), p.njob), dim3(256), 0, st, p);
   trace_end(slot, st);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -146,8 +145,7 @@ lora_status_t launch_pack(const PackParams& p, cudaStream_t st) {
 lora_status_t launch_norms(const NormParams& p, int examples, cudaStream_t st) {
   if (examples <= 0) return LORA_OK;
   const int slot = trace_begin(LORA_KIND_REDUCE, st);
-  norms_kernel<<<examples, 256, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(norms_kernel, dim3(examples), dim3(256), 0, st, p);
   trace_end(slot, st);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -164,8 +162,7 @@ lora_status_t launch_reduce(const RedParams& p, cudaStream_t st) {
   int64_t gx = ceil_div(most, 256);
   gx = gx > 2048 ? 2048 : gx;
   const int slot = trace_begin(LORA_KIND_REDUCE, st);
-  reduce_kernel<<<dim3(static_cast<unsigned>(gx), p.nout), 256, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(reduce_kernel, dim3(static_cast<unsigned>(gx), p.nout), dim3(256), 0, st, p);
   trace_end(slot, st);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -179,8 +176,7 @@ lora_status_t launch_rope(const RopeParams& p, cudaStream_t st) {
   long long gx = ceil_div(most, 256);
   gx = gx > 4 * num_sms() ? 4 * num_sms() : gx;
   const int slot = trace_begin(LORA_KIND_ROPE, st);
-  rope_rotate_kernel<<<dim3(static_cast<unsigned>(gx), p.ntensors), 256, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(rope_rotate_kernel, dim3(static_cast<unsigned>(gx), p.ntensors), dim3(256), 0, st, p);
   trace_end(slot, st);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -1268,8 +1264,7 @@ extern "C" lora_status_t lora_rope_table(float* cos, float* sin, int64_t n_pos, 
   long long gx = ceil_div(n_pos * p.half, 256);
   gx = gx > 4 * num_sms() ? 4 * num_sms() : gx;
   const int slot = trace_begin(LORA_KIND_ROPE, stream);
-  rope_table_kernel<<<static_cast<unsigned>(gx), 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(rope_table_kernel, dim3(static_cast<unsigned>(gx)), dim3(256), 0, stream, p);
   trace_end(slot, stream);
   if (e != cudaSuccess) return LORA_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
