@@ -282,6 +282,10 @@ enum {
 };
 lora_status_t lora_trace_enable(int capacity);
 int lora_trace_read(int* kind, float* ms, int max);
+/* Restricts tracing to the kinds whose bit is set in mask (bit k: kind k; all by
+ * default).  Events between two launches serialise them, so tracing only the kernel
+ * being measured keeps the others' overlap (programmatic dependent launch) intact. */
+void lora_trace_kinds(unsigned mask);
 
 #ifdef __cplusplus
 }

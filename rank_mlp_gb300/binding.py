@@ -83,6 +83,7 @@ _SIGS = {
     "lora_wait_timeout": (ctypes.c_uint64, []),
     "lora_test_expire_waits": (_INT, [_INT]),
     "lora_trace_enable": (_INT, [_INT]),
+    "lora_trace_kinds": (None, [ctypes.c_uint]),
     "lora_trace_read": (_INT, [ctypes.POINTER(_INT), ctypes.POINTER(_F32), _INT]),
 }
 EXPORTS = tuple(_SIGS)
@@ -173,6 +174,18 @@ def wait_timeout() -> int:
 def test_expire_waits(launches: int):
     """Failure-path tests: the next `launches` GEMM launches let a bounded wait expire."""
     _check(load().lora_test_expire_waits(launches), "lora_test_expire_waits")
+
+
+def trace_kinds(names=None):
+    """Trace only these kinds (names of KIND_NAMES; None: all)."""
+    if names is None:
+        mask = 0xFFFFFFFF
+    else:
+        inv = {v: k for k, v in KIND_NAMES.items()}
+        mask = 0
+        for n in names:
+            mask |= 1 << inv[n]
+    load().lora_trace_kinds(mask)
 
 
 def trace_enable(capacity: int):

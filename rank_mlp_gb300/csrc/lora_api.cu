@@ -75,13 +75,14 @@ struct Trace {
   std::vector<cudaEvent_t> ev;     // 2 per entry
   std::vector<int> kind;
   int used = 0;
+  unsigned kinds = ~0u;            // bit k: launches of kind k are traced
 };
 static Trace g_trace;
 
 // Records the start event of a traced launch; returns its slot or -1.
 static int trace_begin(int kind, cudaStream_t st) {
   std::lock_guard<std::mutex> lk(g_trace.mu);
-  if (g_trace.capacity == 0 || g_trace.used >= g_trace.capacity) return -1;
+  if (g_trace.capacity == 0 || g_trace.used >= g_trace.capacity || !((g_trace.kinds >> kind) & 1u)) return -1;
   const int slot = g_trace.used++;
   g_trace.kind[slot] = kind;
   cudaEventRecord(g_trace.ev[2 * slot], st);
@@ -1301,6 +1302,11 @@ extern "C" lora_status_t lora_test_expire_waits(int launches) {
 }
 
 extern "C" uint64_t lora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+extern "C" void lora_trace_kinds(unsigned mask) {
+  std::lock_guard<std::mutex> lk(g_trace.mu);
+  g_trace.kinds = mask;
+}
 
 extern "C" lora_status_t lora_trace_enable(int capacity) {
   if (capacity < 0) return LORA_ERR_INVALID_ARG;

@@ -114,3 +114,22 @@ def test_launch_count_and_trace(lib):
     assert {"gate_up", "proj", "act_bwd", "dgrad", "pack", "rank_proj", "rank_grad"} <= kinds
     assert all(ms > 0 for _, ms in tr)
     assert lib.poll_status() == 0
+
+
+def test_trace_kinds_filter(lib):
+    """Tracing only one kind records only its launches (the bench traces the dominant
+    kernel alone inside its timed region)."""
+    cfg = synth.MLP_CONFIGS["tiny"].replace(M=512)
+    ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg).items()}
+    lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
+    lib.trace_kinds(["gate_up"])
+    lib.trace_enable(64)
+    try:
+        for _ in range(3):
+            lib.mlp_forward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, training=False)
+        tr = lib.trace_read()
+    finally:
+        lib.trace_enable(0)
+        lib.trace_kinds(None)
+    assert [k for k, _ in tr] == ["gate_up"] * 3
+    assert lib.poll_status() == 0
