@@ -9,12 +9,9 @@ template <int STAGES, bool B_MN, int EPIW>
 static cudaError_t launch_pair(const TcParams& p, int grid, cudaStream_t st) {
   auto* k = tc_gemm_pair_kernel<STAGES, B_MN, EPIW>;
   constexpr int smem = PairCfg<STAGES>::kSmemBytes;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  const cudaError_t e = ensure_smem_limit(k, smem, configured);
+  if (e != cudaSuccess) return e;
   return launch_pdl(k, dim3(grid), dim3(pair_threads(EPIW)), smem, st, p);  // grid: a multiple of 2
 }
 

@@ -9,12 +9,9 @@ template <int BN, int STAGES, bool A_MN, bool B_MN>
 static cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t st) {
   auto* k = tc_gemm_kernel<BN, STAGES, A_MN, B_MN>;
   constexpr int smem = TcCfg<BN, STAGES>::kSmemBytes;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static std::atomic<unsigned long long> configured{0};
+  const cudaError_t e = ensure_smem_limit(k, smem, configured);
+  if (e != cudaSuccess) return e;
   return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, p);
 }
 
