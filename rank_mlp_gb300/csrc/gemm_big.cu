@@ -17,8 +17,10 @@ static cudaError_t launch_pair(const TcParams& p, int grid, cudaStream_t st) {
 
 cudaError_t launch_tc_big(int variant, const TcParams& p, int grid, cudaStream_t st) {
   switch (variant) {
-    // forward (gate/up activation, down): 4 epilogue warps; backward (act', dx): 8
+    // forward (gate/up activation, down): 4 epilogue warps, 8 for short K; backward
+    // (act', dx): 8
     case VP_KK: return launch_pair<6, false, 4>(p, grid, st);
+    case VP_KK8: return launch_pair<6, false, 8>(p, grid, st);
     case VP_KMN: return launch_pair<6, true, 8>(p, grid, st);
     default: return cudaErrorInvalidValue;
   }

@@ -28,6 +28,7 @@ cudaError_t launch_tc_skinny(int variant, const TcParams& p, int grid, cudaStrea
 int tc_smem_bytes(int variant) {
   switch (variant) {
     case VP_KK:
+    case VP_KK8:
     case VP_KMN: return PairCfg<6>::kSmemBytes;
     case V64_KK:
     case V64_MNMN: return TcCfg<64, 8>::kSmemBytes;

@@ -373,7 +373,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
     // EPI_STORE (bias included) followed by the rotary embedding of every head in the
     // tile ("Model Patches and Kernels", RoPE): the pair (c, c + half) of a head turns
     // by the angle of this token's position.  Heads never straddle a 256-column tile
-    // (head_dim divides 256) and the whole row of the tile is this thread's (nparts 1).
+    // (head_dim divides 256).  The tile row's BN/64 (head, 32-column) chunk pairs are
+    // shared out among the `nparts` warps that own this row.
     if constexpr (BN == 256) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(G.out0);
       const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(G.in0);
@@ -389,10 +390,11 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
       }
       const float* crow = p.rope_cos + static_cast<long long>(pos) * half;
       const float* srow = p.rope_sin + static_cast<long long>(pos) * half;
+      const int cph = half / 32;                       // chunk pairs per head
 #pragma unroll 1
-      for (int hb = 0; hb < BN; hb += 2 * half) {
-#pragma unroll 1
-        for (int c = 0; c < half; c += 32) {
+      for (int t = part; t < BN / 64; t += nparts) {
+        const int hb = (t / cph) * 2 * half, c = (t % cph) * 32;
+        {
           uint32_t va[32], vb[32];
           __syncwarp();
           tmem_ld32(tacc + hb + c, va);

@@ -26,10 +26,17 @@ enum Variant : int {
   V64_MNMN = 3,    // reductions over tokens (dA, dB), padded rank <= 64
   V128_KK = 4,
   V128_MNMN = 5,
-  kNumVariants = 6
+  VP_KK8 = 6,      // VP_KK with 8 epilogue warps: short-K launches, where 4 warps' epilogue
+                   // outlasts a tile's MMAs
+  kNumVariants = 7
 };
 
-constexpr bool variant_pair(int v) { return v == VP_KK || v == VP_KMN; }
+// A forward pair launch whose longest K is at most this many 64-wide k-blocks runs
+// VP_KK8: a tile's MMAs (~0.28 us per k-block) then no longer cover the 4-warp
+// epilogue of the previous tile (~8 us for gate/up with SwiGLU).
+constexpr int kShortKBlocks = 32;
+
+constexpr bool variant_pair(int v) { return v == VP_KK || v == VP_KMN || v == VP_KK8; }
 constexpr int variant_bn(int v) { return variant_pair(v) ? 256 : (v <= V64_MNMN ? 64 : 128); }
 constexpr bool variant_a_mn(int v) { return v == V64_MNMN || v == V128_MNMN; }
 constexpr bool variant_b_mn(int v) { return v == VP_KMN || v == V64_MNMN || v == V128_MNMN; }

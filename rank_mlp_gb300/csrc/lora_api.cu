@@ -108,6 +108,11 @@ static int take_expiry() {
 
 lora_status_t launch_gemm(int variant, const TcParams& plan, int kind, cudaStream_t st) {
   if (plan.total_units <= 0) return LORA_OK;
+  if (variant == VP_KK) {
+    int kb = 0;
+    for (int g = 0; g < plan.ngroups; ++g) kb = plan.grp[g].kb_total > kb ? plan.grp[g].kb_total : kb;
+    if (kb <= kShortKBlocks) variant = VP_KK8;
+  }
   TcParams p = plan;
   p.timeout_ns = g_timeout_ns.load();
   p.inject_stall = take_expiry();
