@@ -260,8 +260,9 @@ def oracle_step_fn(cfg, tokens: int, host):
     def step():
         args = (x, v["W_gate"], v["A_gate"], v["B_gate"], v["W_up"], v["A_up"], v["B_up"],
                 v["W_down"], v["A_down"], v["B_down"], cfg.s, cfg.act)
-        oracle.mlp_forward(*args)
-        oracle.mlp_backward(*args, dy)
+        f = oracle.mlp_forward(*args)
+        b = oracle.mlp_backward(*args, dy)
+        return f, b
     return step
 
 
@@ -275,8 +276,21 @@ def host_inputs(cfg, max_tokens: int):
     return {k: synth.bf16_to_f64(x) for k, x in t.items()}
 
 
-def cpu_baseline(cfg, budget_s: float = 15.0):
-    """Times the oracle as it stands on a sample of tokens sized for ~budget_s."""
+def parity_errors(got, ref) -> dict:
+    """Relative Frobenius error and max-abs error / max |ref| of a GPU result (bf16
+    tensor) against the float64 oracle."""
+    import numpy as np
+    import synth
+    g = np.asarray(synth.bf16_to_f64(got), np.float64)
+    ref = np.asarray(ref, np.float64)
+    return {"rel_fro": float(np.linalg.norm(g - ref) / np.linalg.norm(ref)),
+            "max_abs_over_max_ref": float(np.abs(g - ref).max() / np.abs(ref).max())}
+
+
+def cpu_baseline(cfg, budget_s: float = 15.0, got=None):
+    """Times the oracle as it stands on a sample of tokens sized for ~budget_s.  got:
+    the GPU's results for the first tokens ({"y": ..., "dx": ...}, bf16 on the host):
+    the sample's oracle results then also give the parity errors of those rows."""
     probe = 64
     host = host_inputs(cfg, 4096)
     t0 = time.perf_counter()
@@ -285,11 +299,19 @@ def cpu_baseline(cfg, budget_s: float = 15.0):
     tokens = int(max(probe, min(4096, budget_s / max(per_tok, 1e-9))))
     step = oracle_step_fn(cfg, tokens, host)
     t0 = time.perf_counter()
-    step()
+    f, b = step()
     dt = time.perf_counter() - t0
-    return {"value": tokens / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"fwd+bwd of the first {tokens} of {cfg.M} tokens (all weights full size), "
-                      f"float64 numpy/BLAS, {dt:.1f} s"}
+    out = {"value": tokens / dt, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+           "sample": f"fwd+bwd of the first {tokens} of {cfg.M} tokens (all weights full size), "
+                     f"float64 numpy/BLAS, {dt:.1f} s"}
+    if got:
+        n = min(tokens, got["y"].shape[0])
+        par = {"tokens": n, "tolerance": {"rel_fro": 1e-2, "max_abs_over_max_ref": 3e-2}}
+        par["y"] = parity_errors(got["y"][:n], f["y"][:n])
+        if "dx" in got:
+            par["dx"] = parity_errors(got["dx"][:n], b["dx"][:n])
+        out["parity"] = par
+    return out
 
 
 # ---------------------------------------------------------------------------- arms
@@ -468,9 +490,12 @@ def run_ours(args):
         return 0
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
+        got = {"y": y[:4096].cpu()}
+        if not n_ex:
+            got["dx"] = dx[:4096].cpu()
         del t
         torch.cuda.empty_cache()
-        cpu = cpu_baseline(cfg)
+        cpu = cpu_baseline(cfg, got=got)
     traffic = ncu_traffic(dom)
     line = {
         "metric": METRIC, "value": world * M * args.steps / secs, "unit": "tokens/s", "n_gpus": world,

@@ -133,3 +133,60 @@ def test_trace_kinds_filter(lib):
         lib.trace_kinds(None)
     assert [k for k, _ in tr] == ["gate_up"] * 3
     assert lib.poll_status() == 0
+
+
+def _kinds(lib, fn):
+    import collections
+    lib.trace_enable(256)
+    try:
+        fn()
+        tr = lib.trace_read()
+    finally:
+        lib.trace_enable(0)
+    return collections.Counter(k for k, _ in tr)
+
+
+def test_launches_per_call(lib):
+    """The launch structure of each call.  MLP forward: pack, the two rank-r
+    projections (x A^T, h A^T), the gate/up and down GEMMs, and one split-K reduction
+    per rank-r projection that was split.  MLP backward: pack, two rank-r projections
+    (dy B_d, [dg du][B_g B_u]), four reductions over tokens (dB_d, dA_d, dB_g|dB_u,
+    dA_g|dA_u), the act' and dx GEMMs, and their split-K reductions.  Q/K/V + O with
+    RoPE: the same per half, plus one transpose-rotation launch in the backward."""
+    cfg = synth.MLP_CONFIGS["qwen05b"].replace(M=1024)
+    ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg).items()}
+    lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
+    saved = {}
+
+    def fwd():
+        saved["y"], saved["s"] = lib.mlp_forward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act)
+
+    def bwd():
+        lib.mlp_backward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, saved["s"], ins["dy"])
+
+    f = _kinds(lib, fwd)
+    assert (f["pack"], f["rank_proj"], f["gate_up"], f["proj"]) == (1, 2, 1, 1), f
+    assert f["reduce"] <= 2 and set(f) <= {"pack", "rank_proj", "gate_up", "proj", "reduce"}, f
+    b = _kinds(lib, bwd)
+    assert (b["pack"], b["rank_proj"], b["rank_grad"], b["act_bwd"], b["dgrad"]) == (1, 2, 4, 1, 1), b
+    assert 4 <= b["reduce"] <= 6 and set(b) <= {"pack", "rank_proj", "rank_grad", "act_bwd", "dgrad",
+                                                  "reduce"}, b
+
+    qc = synth.QKVO_CONFIGS["gqa7b"].replace(M=512, h=512, heads_q=4, heads_kv=2, head_dim=128)
+    t = {k: x.to(DEV) for k, x in synth.make_qkvo_inputs(qc).items()}
+    ql = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
+    cos, sin = lib.rope_table(512, 128, device=DEV)
+    rope = {"cos": cos, "sin": sin, "pos": synth.positions(512, seq=512, device=DEV), "head_dim": 128}
+
+    def qfwd():
+        saved["q"] = lib.qkvo_forward(t["x"], ql("q"), ql("k"), ql("v"), t["o_in"], ql("o"), qc.s, rope=rope)[1]
+
+    def qbwd():
+        lib.qkvo_backward(t["x"], ql("q"), ql("k"), ql("v"), t["o_in"], ql("o"), qc.s, saved["q"], t["dy_q"],
+                          t["dy_k"], t["dy_v"], t["dy_o"], rope=rope)
+
+    f = _kinds(lib, qfwd)
+    assert (f["pack"], f["rank_proj"], f["proj"]) == (1, 2, 2), f
+    b = _kinds(lib, qbwd)
+    assert (b["pack"], b["rope"], b["rank_proj"], b["rank_grad"], b["dgrad"]) == (1, 1, 2, 4, 2), b
+    assert lib.poll_status() == 0
