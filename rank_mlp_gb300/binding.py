@@ -140,13 +140,19 @@ _WS = {}
 
 
 def workspace(nbytes: int, device) -> torch.Tensor:
-    """A per-device workspace of at least nbytes (cached, grown on demand, first
-    256 bytes zeroed: they hold the asynchronous status word)."""
+    """A workspace of at least nbytes for the current stream of `device` (cached per
+    device and stream, grown on demand, first 256 bytes zeroed: they hold the
+    asynchronous status word).  Calls that share a workspace must not overlap on the
+    GPU, so each stream gets its own; calls on one stream are ordered anyway."""
     device = torch.device(device)
-    key = device.index if device.index is not None else torch.cuda.current_device()
+    idx = device.index if device.index is not None else torch.cuda.current_device()
+    key = (idx, torch.cuda.current_stream(idx).cuda_stream)
     ws = _WS.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        old = ws
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=torch.device("cuda", idx))
+        if old is not None:
+            ws[:4].copy_(old[:4])     # keep a status bit that has not been polled yet (same stream)
         _WS[key] = ws
     return ws
 

@@ -190,3 +190,30 @@ def test_launches_per_call(lib):
     b = _kinds(lib, qbwd)
     assert (b["pack"], b["rope"], b["rank_proj"], b["rank_grad"], b["dgrad"]) == (1, 1, 2, 4, 2), b
     assert lib.poll_status() == 0
+
+
+def test_two_streams_get_their_own_workspaces(lib):
+    """Calls on two streams run concurrently on separate cached workspaces and give
+    the same bits as the same calls run one after the other."""
+    cfg = synth.MLP_CONFIGS["qwen05b"].replace(M=1024)
+    ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg, seed=3).items()}
+    lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
+    ref, _ = lib.mlp_forward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, training=False)
+    x2 = torch.flip(ins["x"], dims=[0]).contiguous()
+    ref2, _ = lib.mlp_forward(x2, lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, training=False)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            a, _ = lib.mlp_forward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, training=False)
+        with torch.cuda.stream(s2):
+            b, _ = lib.mlp_forward(x2, lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, training=False)
+        outs.append((a, b))
+    torch.cuda.synchronize()
+    for a, b in outs:
+        assert torch.equal(a.view(torch.int16), ref.view(torch.int16))
+        assert torch.equal(b.view(torch.int16), ref2.view(torch.int16))
+    for st in (s1, s2):
+        with torch.cuda.stream(st):
+            assert lib.poll_status() == 0
