@@ -35,13 +35,16 @@ struct PackParams {
   int njob;
 };
 
-constexpr int kMaxRedOuts = 3;
+constexpr int kMaxRedOuts = 8;
 
 struct RedOut {
   const float* part;  // [splits][rows_pad][width] f32 slab
   int rows;           // valid rows of the slab
   long long rows_pad;
   int width;
+  int splits;
+  int per_split;      // 0: out = scale * sum over splits; 1: split k -> dst + k * split_stride
+  float scale;
   __nv_bfloat16* dst;
   int col0, ncols;    // columns [col0, col0 + ncols) of the slab
   long long ld;
@@ -50,9 +53,6 @@ struct RedOut {
 };
 
 struct RedParams {
-  int splits;
-  float scale;
-  int per_split;      // 0: out = scale * sum over splits; 1: split k -> dst + k * split_stride
   int nout;
   RedOut out[kMaxRedOuts];
 };

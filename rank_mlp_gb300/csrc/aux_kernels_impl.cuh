@@ -47,12 +47,12 @@ __global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ Red
     }
     const float* src = O.part + static_cast<long long>(m) * O.width + O.col0 + c;
     const long long d = O.trans ? static_cast<long long>(c) * O.ld + m : static_cast<long long>(m) * O.ld + c;
-    if (p.per_split) {
-      for (int k = 0; k < p.splits; ++k) O.dst[k * O.split_stride + d] = __float2bfloat16_rn(p.scale * src[k * slab]);
+    if (O.per_split) {
+      for (int k = 0; k < O.splits; ++k) O.dst[k * O.split_stride + d] = __float2bfloat16_rn(O.scale * src[k * slab]);
     } else {
       float s = 0.0f;
-      for (int k = 0; k < p.splits; ++k) s += src[k * slab];
-      O.dst[d] = __float2bfloat16_rn(p.scale * s);
+      for (int k = 0; k < O.splits; ++k) s += src[k * slab];
+      O.dst[d] = __float2bfloat16_rn(O.scale * s);
     }
   }
 }

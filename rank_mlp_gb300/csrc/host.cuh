@@ -107,6 +107,7 @@ constexpr int kMaxSplits = 16;        // split-K factors of the rank-r products
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t imax(int64_t a, int64_t b) { return a > b ? a : b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 // Padded width of the rank-r operands of `nslots` adapters sharing one input.

@@ -269,10 +269,10 @@ static lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int
   if (splits > 1) {
     RedParams r;
     std::memset(static_cast<void*>(&r), 0, sizeof(r));
-    r.splits = splits;
-    r.scale = 1.0f;
     r.nout = 1;
     RedOut& o = r.out[0];
+    o.splits = splits;
+    o.scale = 1.0f;
     o.part = part;
     o.rows = static_cast<int>(M);
     o.rows_pad = round_up(M, kBM);
@@ -309,21 +309,39 @@ static int64_t token_grad_part(int64_t M, int kf, const int64_t* fs, int n, int6
   for (int j = 0; j < n; ++j) tot += round_up(partial_elems(fs[j], kf, bn, splits), 64);
   return tot;
 }
+// Reductions over tokens whose results no later launch of a call reads (the dA, dB
+// outputs): each keeps its own f32 slabs, and one reduce launch at the end of the call
+// sums them all.
+struct Deferred {
+  RedParams rp;
+  float* cursor;      // next free slab element
+};
+static void defer_init(Deferred& d, float* slabs) {
+  std::memset(static_cast<void*>(&d.rp), 0, sizeof(d.rp));
+  d.cursor = slabs;
+}
+static lora_status_t defer_flush(Deferred& d, cudaStream_t st) {
+  const lora_status_t r = launch_reduce(d.rp, st);
+  d.rp.nout = 0;
+  return r;
+}
+
 // Jobs with the same Q share one slab (several rank slots out of one product).
 // n_ex == 0: the sums over all M tokens.  n_ex > 0: one result per example (example e
 // = tokens [e seq, (e+1) seq), seq = M / n_ex), each written at dst + e * r * f; the
 // products read 3-D views {features, seq, examples} so no k-block straddles two
-// examples (rows past seq read as zero).
+// examples (rows past seq read as zero).  The slabs start at defer.cursor and the
+// sums are left to defer_flush.
 static lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* T, const GradJob* jobs, int njobs,
-                                 float* part, unsigned* status, cudaStream_t st, int64_t n_ex = 0) {
+                                 Deferred& defer, unsigned* status, cudaStream_t st, int64_t n_ex = 0) {
   const int variant = skinny_mnmn(kf);
   GemmPlan g(variant);
   const int64_t seq = n_ex > 0 ? M / n_ex : M;
   const int tmap = n_ex > 0 ? g.b_mnmajor_planes(T, kf, seq, n_ex, kf) : g.b_mnmajor(T, kf, M, kf);
   const void* qs[kMaxGroups];
-  int nq = 0, group_of[kMaxRedOuts];
+  int nq = 0, group_of[kMaxGroups * 3];
   float* parts[kMaxGroups];
-  float* cur = part;
+  float* cur = defer.cursor;
   const int slab_splits = n_ex > 0 ? static_cast<int>(n_ex) : max_splits(ceil_div(M, kBK));
   for (int j = 0; j < njobs; ++j) {
     int gi = -1;
@@ -354,32 +372,23 @@ static lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* 
   g.finish();
   if (!g.ok) return LORA_ERR_CUDA;
   LGB_TRY(launch_gemm(variant, g.p, LORA_KIND_RANK_GRAD, st));
-  // one reduce launch per distinct split count (groups may differ)
-  bool done[kMaxRedOuts] = {false, false, false};
-  for (int j0 = 0; j0 < njobs; ++j0) {
-    if (done[j0]) continue;
-    const int sp = g.p.grp[group_of[j0]].splits;
-    RedParams rp;
-    std::memset(static_cast<void*>(&rp), 0, sizeof(rp));
-    rp.splits = sp;
-    rp.scale = s;
-    rp.per_split = n_ex > 0 ? 1 : 0;
-    for (int j = j0; j < njobs; ++j) {
-      if (done[j] || g.p.grp[group_of[j]].splits != sp) continue;
-      done[j] = true;
-      RedOut& o = rp.out[rp.nout++];
-      o.part = parts[group_of[j]];
-      o.rows = static_cast<int>(jobs[j].f);
-      o.rows_pad = round_up(jobs[j].f, kBM);
-      o.width = static_cast<int>(round_up(kf, g.bn));
-      o.dst = static_cast<bf16*>(jobs[j].dst);
-      o.col0 = jobs[j].col0;
-      o.ncols = r;
-      o.ld = jobs[j].trans ? jobs[j].f : r;
-      o.trans = jobs[j].trans;
-      o.split_stride = static_cast<long long>(r) * jobs[j].f;
-    }
-    LGB_TRY(launch_reduce(rp, st));
+  defer.cursor = cur;
+  for (int j = 0; j < njobs; ++j) {
+    if (defer.rp.nout >= kMaxRedOuts) return LORA_ERR_UNSUPPORTED;   // not reached: <= 8 per call
+    RedOut& o = defer.rp.out[defer.rp.nout++];
+    o.part = parts[group_of[j]];
+    o.rows = static_cast<int>(jobs[j].f);
+    o.rows_pad = round_up(jobs[j].f, kBM);
+    o.width = static_cast<int>(round_up(kf, g.bn));
+    o.splits = g.p.grp[group_of[j]].splits;
+    o.per_split = n_ex > 0 ? 1 : 0;
+    o.scale = s;
+    o.dst = static_cast<bf16*>(jobs[j].dst);
+    o.col0 = jobs[j].col0;
+    o.ncols = r;
+    o.ld = jobs[j].trans ? jobs[j].f : r;
+    o.trans = jobs[j].trans;
+    o.split_stride = static_cast<long long>(r) * jobs[j].f;
   }
   return LORA_OK;
 }
@@ -420,13 +429,8 @@ LinearLayout linear_layout(int64_t M, int64_t in, int64_t out, int r) {
     c.take_n<bf16>(kf * out);   // B^T
     c.take_n<bf16>(kf * in);    // s A
     c.take_n<bf16>(M * kf);     // U
-    const int64_t fs[2] = {out, in};
-    int64_t p = token_grad_part(M, kf, fs, 1);
-    const int64_t p2 = token_grad_part(M, kf, fs + 1, 1);
-    p = p > p2 ? p : p2;
-    const int64_t p3 = rank_projection_part(M, kf, ceil_div(out, kBK));
-    p = p > p3 ? p : p3;
-    c.take_n<float>(p);
+    c.take_n<float>(rank_projection_part(M, kf, ceil_div(out, kBK)));
+    c.take_n<float>(token_grad_part(M, kf, &out, 1) + token_grad_part(M, kf, &in, 1));   // dB, dA slabs
     L.ws_bwd = c.off;
   }
   {
@@ -535,7 +539,9 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   bf16* bt = c.take_n<bf16>(kf * out);
   bf16* af = c.take_n<bf16>(kf * in);
   bf16* U = c.take_n<bf16>(M * kf);
-  float* part = reinterpret_cast<float*>(c.take(0));
+  float* part = c.take_n<float>(rank_projection_part(M, kf, ceil_div(out, kBK)));
+  Deferred dr;
+  defer_init(dr, c.take_n<float>(token_grad_part(M, kf, &out, 1) + token_grad_part(M, kf, &in, 1)));
   const bf16* T = static_cast<const bf16*>(saved);
 
   PackParams pk;
@@ -547,7 +553,7 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   const ProjSeg ps = {dy, bt, out};
   LGB_TRY(rank_projection(M, kf, &ps, 1, U, part, status, stream));
   const GradJob jb = {dy, out, 0, grads.dB, 0};
-  LGB_TRY(token_grads(M, r, kf, s, T, &jb, 1, part, status, stream));
+  LGB_TRY(token_grads(M, r, kf, s, T, &jb, 1, dr, status, stream));
 
   GemmPlan g(kBigKMN);
   GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(in), EPI_STORE, false);
@@ -561,7 +567,8 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
 
   const GradJob ja = {x, in, 0, grads.dA, 1};
-  return token_grads(M, r, kf, s, U, &ja, 1, part, status, stream);
+  LGB_TRY(token_grads(M, r, kf, s, U, &ja, 1, dr, status, stream));
+  return defer_flush(dr, stream);
 }
 
 // ================================================================ gated MLP
@@ -576,6 +583,17 @@ struct MlpLayout {
 };
 
 // n_ex > 0: workspace of the per-example backward (one reduction slab per example).
+// Backward scratch: the rank-r projections' split-K slabs (reused), then the four token
+// reductions' slabs (kept until the call's final reduce).
+static int64_t mlp_bwd_rank_part(int64_t M, int64_t h, int64_t i, int kfd, int kfg) {
+  return imax(rank_projection_part(M, kfd, ceil_div(h, kBK)), rank_projection_part(M, kfg, 2 * ceil_div(i, kBK)));
+}
+static int64_t mlp_bwd_slabs(int64_t M, int64_t h, int64_t i, int kfd, int kfg, int64_t n_ex) {
+  const int64_t f2[2] = {i, i};
+  return token_grad_part(M, kfd, &h, 1, n_ex) + token_grad_part(M, kfd, &i, 1, n_ex) +
+         token_grad_part(M, kfg, f2, 2, n_ex) + token_grad_part(M, kfg, &h, 1, n_ex);
+}
+
 MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r, int64_t n_ex = 0) {
   MlpLayout L;
   L.kfg = fold_width(2, r);
@@ -609,15 +627,8 @@ MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r, int64_t n_ex = 0) {
     c.take_n<bf16>(M * i);       // dg
     c.take_n<bf16>(M * i);       // du
     c.take_n<bf16>(M * kfg);     // V
-    int64_t p = rank_projection_part(M, kfd, ceil_div(h, kBK));
-    const int64_t cand[] = {
-        rank_projection_part(M, kfg, 2 * ceil_div(i, kBK)),
-        token_grad_part(M, kfd, &h, 1, n_ex),
-        token_grad_part(M, kfd, &i, 1, n_ex),
-        [&] { const int64_t f2[2] = {i, i}; return token_grad_part(M, kfg, f2, 2, n_ex); }(),
-        token_grad_part(M, kfg, &h, 1, n_ex)};
-    for (int64_t v : cand) p = v > p ? v : p;
-    c.take_n<float>(p);
+    c.take_n<float>(mlp_bwd_rank_part(M, h, i, kfd, kfg));
+    c.take_n<float>(mlp_bwd_slabs(M, h, i, kfd, kfg, n_ex));
     L.ws_bwd = c.off;
   }
   {
@@ -800,7 +811,9 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   bf16* dg = c.take_n<bf16>(M * i);
   bf16* du = c.take_n<bf16>(M * i);
   bf16* V = c.take_n<bf16>(M * kfg);
-  float* part = reinterpret_cast<float*>(c.take(0));
+  float* part = c.take_n<float>(mlp_bwd_rank_part(M, h, i, kfd, kfg));
+  Deferred dr;
+  defer_init(dr, c.take_n<float>(mlp_bwd_slabs(M, h, i, kfd, kfg, n_ex)));
 
   PackParams pk;
   std::memset(static_cast<void*>(&pk), 0, sizeof(pk));
@@ -819,7 +832,7 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   const ProjSeg p1 = {dy, bt_d, h};
   LGB_TRY(rank_projection(M, kfd, &p1, 1, ud, part, status, stream));
   const GradJob j1 = {dy, h, 0, d_down.dB, 0};
-  LGB_TRY(token_grads(M, r, kfd, s, td, &j1, 1, part, status, stream, n_ex));
+  LGB_TRY(token_grads(M, r, kfd, s, td, &j1, 1, dr, status, stream, n_ex));
 
   // dh = [dy | U_d] [W_d ; s A_d];  dg = dh u act'(g), du = dh act(g)
   {
@@ -842,7 +855,7 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
 
   // dA_d = s U_d^T h
   const GradJob j2 = {hsv, i, 0, d_down.dA, 1};
-  LGB_TRY(token_grads(M, r, kfd, s, ud, &j2, 1, part, status, stream, n_ex));
+  LGB_TRY(token_grads(M, r, kfd, s, ud, &j2, 1, dr, status, stream, n_ex));
 
   // V = [dg B_g | du B_u]
   const ProjSeg p3[2] = {{dg, bt_g, i}, {du, bt_u, i}};
@@ -850,7 +863,7 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
 
   // dB_g = s dg^T T_g,  dB_u = s du^T T_u
   const GradJob j3[2] = {{dg, i, 0, d_gate.dB, 0}, {du, i, r, d_up.dB, 0}};
-  LGB_TRY(token_grads(M, r, kfg, s, tgu, j3, 2, part, status, stream, n_ex));
+  LGB_TRY(token_grads(M, r, kfg, s, tgu, j3, 2, dr, status, stream, n_ex));
 
   // dx = [dg | du | V] [W_g ; W_u ; s A_g ; s A_u]
   {
@@ -869,7 +882,8 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
 
   // dA_g = s V_g^T x,  dA_u = s V_u^T x
   const GradJob j4[2] = {{x, h, 0, d_gate.dA, 1}, {x, h, r, d_up.dA, 1}};
-  LGB_TRY(token_grads(M, r, kfg, s, V, j4, 2, part, status, stream, n_ex));
+  LGB_TRY(token_grads(M, r, kfg, s, V, j4, 2, dr, status, stream, n_ex));
+  LGB_TRY(defer_flush(dr, stream));
   if (n_ex > 0 && sq_norms != nullptr) {
     NormParams np;
     std::memset(static_cast<void*>(&np), 0, sizeof(np));
@@ -924,6 +938,17 @@ struct QkvoLayout {
   size_t ws_fwd, ws_bwd, saved, off_to;
 };
 
+// Backward scratch, as for the MLP: rank-r projection slabs, then the token reductions'.
+static int64_t qkvo_bwd_rank_part(int64_t M, int64_t h, int64_t nq, int64_t nkv, int kfq, int kfo) {
+  return imax(rank_projection_part(M, kfo, ceil_div(h, kBK)),
+              rank_projection_part(M, kfq, ceil_div(nq, kBK) + 2 * ceil_div(nkv, kBK)));
+}
+static int64_t qkvo_bwd_slabs(int64_t M, int64_t h, int64_t nq, int64_t nkv, int kfq, int kfo) {
+  const int64_t f3[3] = {nq, nkv, nkv};
+  return token_grad_part(M, kfo, &h, 1) + token_grad_part(M, kfo, &nq, 1) + token_grad_part(M, kfq, f3, 3) +
+         token_grad_part(M, kfq, &h, 1);
+}
+
 QkvoLayout qkvo_layout(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r) {
   QkvoLayout L;
   L.kfq = fold_width(3, r);
@@ -958,16 +983,8 @@ QkvoLayout qkvo_layout(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r) {
     c.take_n<bf16>(M * kfq);
     c.take_n<bf16>(M * nq);     // dy_q, dy_k turned back by the transpose RoPE rotation
     c.take_n<bf16>(M * nkv);
-    const int64_t f3[3] = {nq, nkv, nkv};
-    const int64_t cand[] = {rank_projection_part(M, kfo, ceil_div(h, kBK)),
-                            token_grad_part(M, kfo, &h, 1),
-                            token_grad_part(M, kfo, &nq, 1),
-                            rank_projection_part(M, kfq, ceil_div(nq, kBK) + 2 * ceil_div(nkv, kBK)),
-                            token_grad_part(M, kfq, f3, 3),
-                            token_grad_part(M, kfq, &h, 1)};
-    int64_t p = 0;
-    for (int64_t v : cand) p = v > p ? v : p;
-    c.take_n<float>(p);
+    c.take_n<float>(qkvo_bwd_rank_part(M, h, nq, nkv, kfq, kfo));
+    c.take_n<float>(qkvo_bwd_slabs(M, h, nq, nkv, kfq, kfo));
     L.ws_bwd = c.off;
   }
   {
@@ -1175,7 +1192,9 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
   bf16* V = c.take_n<bf16>(M * kfq);
   bf16* dyq_r = c.take_n<bf16>(M * n_q);
   bf16* dyk_r = c.take_n<bf16>(M * n_kv);
-  float* part = reinterpret_cast<float*>(c.take(0));
+  float* part = c.take_n<float>(qkvo_bwd_rank_part(M, h, n_q, n_kv, kfq, kfo));
+  Deferred dr;
+  defer_init(dr, c.take_n<float>(qkvo_bwd_slabs(M, h, n_q, n_kv, kfq, kfo)));
 
   PackParams pk;
   std::memset(static_cast<void*>(&pk), 0, sizeof(pk));
@@ -1198,7 +1217,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     const ProjSeg p1 = {dyo, bt_o, h};
     LGB_TRY(rank_projection(M, kfo, &p1, 1, uo, part, status, stream));
     const GradJob j1 = {dyo, h, 0, d_o.dB, 0};
-    LGB_TRY(token_grads(M, r, kfo, s, to, &j1, 1, part, status, stream));
+    LGB_TRY(token_grads(M, r, kfo, s, to, &j1, 1, dr, status, stream));
     GemmPlan g(kBigKMN);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(n_q), EPI_STORE, false);
     GemmPlan::seg(G, g.a_kmajor(dyo, M, h, h), g.b_mnmajor(o.W, n_q, h, n_q), -1, h, h);
@@ -1210,7 +1229,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
     const GradJob j2 = {o_in, n_q, 0, d_o.dA, 1};
-    LGB_TRY(token_grads(M, r, kfo, s, uo, &j2, 1, part, status, stream));
+    LGB_TRY(token_grads(M, r, kfo, s, uo, &j2, 1, dr, status, stream));
   }
   if (x) {
     if (rope != nullptr) {
@@ -1239,7 +1258,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     const ProjSeg p3[3] = {{dyq, btq, n_q}, {dyk, btk, n_kv}, {dyv, btv, n_kv}};
     LGB_TRY(rank_projection(M, kfq, p3, 3, V, part, status, stream));
     const GradJob j3[3] = {{dyq, n_q, 0, d_q.dB, 0}, {dyk, n_kv, r, d_k.dB, 0}, {dyv, n_kv, 2 * r, d_v.dB, 0}};
-    LGB_TRY(token_grads(M, r, kfq, s, tqkv, j3, 3, part, status, stream));
+    LGB_TRY(token_grads(M, r, kfq, s, tqkv, j3, 3, dr, status, stream));
     GemmPlan g(kBigKMN);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(h), EPI_STORE, false);
     GemmPlan::seg(G, g.a_kmajor(dyq, M, n_q, n_q), g.b_mnmajor(q.W, h, n_q, h), -1, n_q, n_q);
@@ -1253,9 +1272,9 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
     const GradJob j4[3] = {{x, h, 0, d_q.dA, 1}, {x, h, r, d_k.dA, 1}, {x, h, 2 * r, d_v.dA, 1}};
-    LGB_TRY(token_grads(M, r, kfq, s, V, j4, 3, part, status, stream));
+    LGB_TRY(token_grads(M, r, kfq, s, V, j4, 3, dr, status, stream));
   }
-  return LORA_OK;
+  return defer_flush(dr, stream);
 }
 
 // ================================================================ status and trace

@@ -150,8 +150,9 @@ def test_launches_per_call(lib):
     """The launch structure of each call.  MLP forward: pack, the two rank-r
     projections (x A^T, h A^T), the gate/up and down GEMMs, and one split-K reduction
     per rank-r projection that was split.  MLP backward: pack, two rank-r projections
-    (dy B_d, [dg du][B_g B_u]), four reductions over tokens (dB_d, dA_d, dB_g|dB_u,
-    dA_g|dA_u), the act' and dx GEMMs, and their split-K reductions.  Q/K/V + O with
+    (dy B_d, [dg du][B_g B_u]) with their split-K sums, four reductions over tokens
+    (dB_d, dA_d, dB_g|dB_u, dA_g|dA_u) whose sums share one launch at the end, and the
+    act' and dx GEMMs.  Q/K/V + O with
     RoPE: the same per half, plus one transpose-rotation launch in the backward."""
     cfg = synth.MLP_CONFIGS["qwen05b"].replace(M=1024)
     ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg).items()}
@@ -169,7 +170,9 @@ def test_launches_per_call(lib):
     assert f["reduce"] <= 2 and set(f) <= {"pack", "rank_proj", "gate_up", "proj", "reduce"}, f
     b = _kinds(lib, bwd)
     assert (b["pack"], b["rank_proj"], b["rank_grad"], b["act_bwd"], b["dgrad"]) == (1, 2, 4, 1, 1), b
-    assert 4 <= b["reduce"] <= 6 and set(b) <= {"pack", "rank_proj", "rank_grad", "act_bwd", "dgrad",
+    # split-K sums of the two rank-r projections (if split), then one for all four
+    # reductions over tokens at the end of the call
+    assert 1 <= b["reduce"] <= 3 and set(b) <= {"pack", "rank_proj", "rank_grad", "act_bwd", "dgrad",
                                                   "reduce"}, b
 
     qc = synth.QKVO_CONFIGS["gqa7b"].replace(M=512, h=512, heads_q=4, heads_kv=2, head_dim=128)
@@ -189,6 +192,7 @@ def test_launches_per_call(lib):
     assert (f["pack"], f["rank_proj"], f["proj"]) == (1, 2, 2), f
     b = _kinds(lib, qbwd)
     assert (b["pack"], b["rope"], b["rank_proj"], b["rank_grad"], b["dgrad"]) == (1, 1, 2, 4, 2), b
+    assert 1 <= b["reduce"] <= 3, b
     assert lib.poll_status() == 0
 
 
