@@ -146,7 +146,7 @@ lora_status_t launch_pack(const PackParams& p, cudaStream_t st) {
   if (p.njob == 0) return LORA_OK;
   int64_t most = 1;
   for (int j = 0; j < p.njob; ++j) {
-    const int64_t n = static_cast<int64_t>(p.job[j].rows) * p.job[j].cols;
+    const int64_t n = static_cast<int64_t>(p.job[j].rows) * (p.job[j].cols / 8);   // 8 elements per thread
     most = n > most ? n : most;
   }
   int64_t gx = ceil_div(most, 256);
