@@ -39,6 +39,8 @@ def _linear(M, fin, fout, r, seed):
     (1, 64, 64, 1),          # one token, rank 1
     (129, 4096, 1024, 64),   # one row past a tile, full fold width
     (127, 520, 136, 16),     # K not a multiple of 64, N < one tile
+    (200, 512, 384, 128),    # the widest fold of one adapter (128-column rank tiles)
+    (1031, 896, 4864, 16),   # a prime token count at the Qwen-0.5B width
 ])
 def test_linear_forward_backward(lib, M, fin, fout, r):
     s = 2.0
@@ -202,6 +204,8 @@ def test_qkvo_frozen_bias(lib):
     ("tiny", {}, 2),                                # seq 32: less than one 64-token block
     ("tiny", {"M": 300, "i": 520, "h": 256}, 3),    # seq 100: ragged block per example
     ("qwen05b", {"M": 2048}, 4),                    # seq 512
+    ("tiny", {"M": 256, "i": 520, "h": 256, "act": "geglu_tanh"}, 4),
+    ("tiny", {"M": 192, "i": 344, "h": 128, "act": "geglu_erf", "r": 64, "alpha": 128}, 3),
 ])
 def test_mlp_per_example_grads(lib, name, over, n_ex):
     """DP-SGD per-example adapter gradients and their squared norms."""
@@ -221,3 +225,17 @@ def test_mlp_per_example_grads(lib, name, over, n_ex):
         for e in range(n_ex):
             parity(f"{k}[{e}]", g[k][e], ref[k][e])
     np.testing.assert_allclose(g["sq_norms"].double().cpu().numpy(), ref["sq_norms"], rtol=2e-2)
+
+
+def test_qkvo_largest_rank(lib):
+    """r = 85: three adapters fill the 256-column fold of q, k, v (the rank limit)."""
+    cfg = synth.QKVO_CONFIGS["gqa7b"].replace(M=257, h=384, heads_q=3, heads_kv=1, head_dim=128, r=85,
+                                              alpha=170)
+    ins = synth.make_qkvo_inputs(cfg, seed=9)
+    t = {k: x.to(DEV) for k, x in ins.items()}
+    out, g = qkvo_gpu(lib, t, cfg)
+    f, b = qkvo_oracle(to_f64_dict(ins), cfg)
+    for k in ("q", "k", "v", "o"):
+        parity(k, out[k], f[k])
+    for k in b:
+        parity(k, g[k], b[k])
