@@ -77,6 +77,10 @@ struct TcParams {
   const int* rope_pos;
   int rope_half;             // head_dim / 2: 32, 64 or 128
   int rope_npos;
+  // 1: the launch reads nothing the previous kernel in the stream writes, and writes
+  // nothing it reads, so it starts at once (on SMs the previous kernel has freed) and
+  // waits for that kernel only before it exits, keeping the stream's completion order
+  int pdl_late;
 };
 
 template <int BN, int STAGES>
@@ -508,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();                             // the previous kernel's writes are visible from here
+  if (!p.pdl_late) pdl_wait();            // the previous kernel's writes are visible from here
   pdl_launch_dependents();
 
   if (warp == 0) {
@@ -659,6 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   }
 
   if (*abort_flag) settle_after_abort();
+  if (p.pdl_late) pdl_wait();             // complete only after the previous kernel
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {

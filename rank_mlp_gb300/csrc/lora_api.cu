@@ -332,10 +332,14 @@ static lora_status_t defer_flush(Deferred& d, cudaStream_t st) {
 // products read 3-D views {features, seq, examples} so no k-block straddles two
 // examples (rows past seq read as zero).  The slabs start at defer.cursor and the
 // sums are left to defer_flush.
+// late: the launch follows a kernel whose outputs it does not read (and whose inputs
+// it does not write), so it may start on SMs that kernel has freed (pdl_late).
 static lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* T, const GradJob* jobs, int njobs,
-                                 Deferred& defer, unsigned* status, cudaStream_t st, int64_t n_ex = 0) {
+                                 Deferred& defer, unsigned* status, cudaStream_t st, int64_t n_ex = 0,
+                                 bool late = false) {
   const int variant = skinny_mnmn(kf);
   GemmPlan g(variant);
+  g.p.pdl_late = late ? 1 : 0;
   const int64_t seq = n_ex > 0 ? M / n_ex : M;
   const int tmap = n_ex > 0 ? g.b_mnmajor_planes(T, kf, seq, n_ex, kf) : g.b_mnmajor(T, kf, M, kf);
   const void* qs[kMaxGroups];
@@ -552,8 +556,6 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
 
   const ProjSeg ps = {dy, bt, out};
   LGB_TRY(rank_projection(M, kf, &ps, 1, U, part, status, stream));
-  const GradJob jb = {dy, out, 0, grads.dB, 0};
-  LGB_TRY(token_grads(M, r, kf, s, T, &jb, 1, dr, status, stream));
 
   GemmPlan g(kBigKMN);
   GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(in), EPI_STORE, false);
@@ -567,7 +569,10 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
 
   const GradJob ja = {x, in, 0, grads.dA, 1};
-  LGB_TRY(token_grads(M, r, kf, s, U, &ja, 1, dr, status, stream));
+  // dB = s dy^T T and dA = s U^T x read nothing the dx GEMM writes
+  const GradJob jb = {dy, out, 0, grads.dB, 0};
+  LGB_TRY(token_grads(M, r, kf, s, T, &jb, 1, dr, status, stream, 0, true));
+  LGB_TRY(token_grads(M, r, kf, s, U, &ja, 1, dr, status, stream, 0, true));
   return defer_flush(dr, stream);
 }
 
@@ -828,11 +833,9 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   }
   LGB_TRY(launch_pack(pk, stream));
 
-  // U_d = dy B_d;  dB_d = s dy^T T_d
+  // U_d = dy B_d
   const ProjSeg p1 = {dy, bt_d, h};
   LGB_TRY(rank_projection(M, kfd, &p1, 1, ud, part, status, stream));
-  const GradJob j1 = {dy, h, 0, d_down.dB, 0};
-  LGB_TRY(token_grads(M, r, kfd, s, td, &j1, 1, dr, status, stream, n_ex));
 
   // dh = [dy | U_d] [W_d ; s A_d];  dg = dh u act'(g), du = dh act(g)
   {
@@ -853,17 +856,17 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_ACT_BWD, stream));
   }
 
-  // dA_d = s U_d^T h
+  // dB_d = s dy^T T_d and dA_d = s U_d^T h read nothing the dh GEMM writes: they start
+  // on the SMs its last wave leaves idle
+  const GradJob j1 = {dy, h, 0, d_down.dB, 0};
+  LGB_TRY(token_grads(M, r, kfd, s, td, &j1, 1, dr, status, stream, n_ex, true));
   const GradJob j2 = {hsv, i, 0, d_down.dA, 1};
-  LGB_TRY(token_grads(M, r, kfd, s, ud, &j2, 1, dr, status, stream, n_ex));
+  LGB_TRY(token_grads(M, r, kfd, s, ud, &j2, 1, dr, status, stream, n_ex, true));
 
   // V = [dg B_g | du B_u]
   const ProjSeg p3[2] = {{dg, bt_g, i}, {du, bt_u, i}};
   LGB_TRY(rank_projection(M, kfg, p3, 2, V, part, status, stream));
 
-  // dB_g = s dg^T T_g,  dB_u = s du^T T_u
-  const GradJob j3[2] = {{dg, i, 0, d_gate.dB, 0}, {du, i, r, d_up.dB, 0}};
-  LGB_TRY(token_grads(M, r, kfg, s, tgu, j3, 2, dr, status, stream, n_ex));
 
   // dx = [dg | du | V] [W_g ; W_u ; s A_g ; s A_u]
   {
@@ -880,9 +883,12 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
   }
 
-  // dA_g = s V_g^T x,  dA_u = s V_u^T x
+  // dB_g = s dg^T T_g, dB_u = s du^T T_u and dA_g = s V_g^T x, dA_u = s V_u^T x read
+  // nothing the dx GEMM writes: they start on the SMs its last wave leaves idle
+  const GradJob j3[2] = {{dg, i, 0, d_gate.dB, 0}, {du, i, r, d_up.dB, 0}};
+  LGB_TRY(token_grads(M, r, kfg, s, tgu, j3, 2, dr, status, stream, n_ex, true));
   const GradJob j4[2] = {{x, h, 0, d_gate.dA, 1}, {x, h, r, d_up.dA, 1}};
-  LGB_TRY(token_grads(M, r, kfg, s, V, j4, 2, dr, status, stream, n_ex));
+  LGB_TRY(token_grads(M, r, kfg, s, V, j4, 2, dr, status, stream, n_ex, true));
   LGB_TRY(defer_flush(dr, stream));
   if (n_ex > 0 && sq_norms != nullptr) {
     NormParams np;
@@ -1216,8 +1222,6 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
   if (o_in) {
     const ProjSeg p1 = {dyo, bt_o, h};
     LGB_TRY(rank_projection(M, kfo, &p1, 1, uo, part, status, stream));
-    const GradJob j1 = {dyo, h, 0, d_o.dB, 0};
-    LGB_TRY(token_grads(M, r, kfo, s, to, &j1, 1, dr, status, stream));
     GemmPlan g(kBigKMN);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(n_q), EPI_STORE, false);
     GemmPlan::seg(G, g.a_kmajor(dyo, M, h, h), g.b_mnmajor(o.W, n_q, h, n_q), -1, h, h);
@@ -1228,8 +1232,11 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     g.finish();
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
+    // dB_o = s dy_o^T T_o and dA_o = s U_o^T o_in read nothing the d o_in GEMM writes
+    const GradJob j1 = {dyo, h, 0, d_o.dB, 0};
+    LGB_TRY(token_grads(M, r, kfo, s, to, &j1, 1, dr, status, stream, 0, true));
     const GradJob j2 = {o_in, n_q, 0, d_o.dA, 1};
-    LGB_TRY(token_grads(M, r, kfo, s, uo, &j2, 1, dr, status, stream));
+    LGB_TRY(token_grads(M, r, kfo, s, uo, &j2, 1, dr, status, stream, 0, true));
   }
   if (x) {
     if (rope != nullptr) {
@@ -1257,8 +1264,6 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     }
     const ProjSeg p3[3] = {{dyq, btq, n_q}, {dyk, btk, n_kv}, {dyv, btv, n_kv}};
     LGB_TRY(rank_projection(M, kfq, p3, 3, V, part, status, stream));
-    const GradJob j3[3] = {{dyq, n_q, 0, d_q.dB, 0}, {dyk, n_kv, r, d_k.dB, 0}, {dyv, n_kv, 2 * r, d_v.dB, 0}};
-    LGB_TRY(token_grads(M, r, kfq, s, tqkv, j3, 3, dr, status, stream));
     GemmPlan g(kBigKMN);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(h), EPI_STORE, false);
     GemmPlan::seg(G, g.a_kmajor(dyq, M, n_q, n_q), g.b_mnmajor(q.W, h, n_q, h), -1, n_q, n_q);
@@ -1272,7 +1277,10 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
     const GradJob j4[3] = {{x, h, 0, d_q.dA, 1}, {x, h, r, d_k.dA, 1}, {x, h, 2 * r, d_v.dA, 1}};
-    LGB_TRY(token_grads(M, r, kfq, s, V, j4, 3, dr, status, stream));
+    // the q, k, v dB and dA read nothing the dx GEMM writes
+    const GradJob j3[3] = {{dyq, n_q, 0, d_q.dB, 0}, {dyk, n_kv, r, d_k.dB, 0}, {dyv, n_kv, 2 * r, d_v.dB, 0}};
+    LGB_TRY(token_grads(M, r, kfq, s, tqkv, j3, 3, dr, status, stream, 0, true));
+    LGB_TRY(token_grads(M, r, kfq, s, V, j4, 3, dr, status, stream, 0, true));
   }
   return defer_flush(dr, stream);
 }
