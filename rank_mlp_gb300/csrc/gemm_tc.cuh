@@ -17,6 +17,11 @@
 //
 // Every wait is bounded in time; on expiry the CTA records a timeout in the status
 // word, lets its own copies and MMAs finish (again bounded), frees TMEM and exits.
+//
+// Launches use programmatic dependent launch: the prologue (barriers, TMEM, descriptor
+// prefetch) runs while the previous kernel drains, then griddepcontrol.wait; a launch
+// marked pdl_late reads nothing the previous kernel writes and waits only before exit.
+// The CTA-pair variant for the projection GEMMs is in gemm_pair.cuh.
 #pragma once
 
 #include "ptx.cuh"
