@@ -221,3 +221,34 @@ def test_two_streams_get_their_own_workspaces(lib):
     for st in (s1, s2):
         with torch.cuda.stream(st):
             assert lib.poll_status() == 0
+
+
+def test_per_example_edge_cases(lib):
+    """One example is the whole batch (the per-example gradients equal the batch
+    gradients, to the parity bar, and the squared norm is their sum of squares); zero
+    tokens zero-fill every example's gradients and norms."""
+    cfg = synth.MLP_CONFIGS["tiny"].replace(M=192, h=256, i=344)
+    ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg, seed=12).items()}
+    lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
+    y, saved = lib.mlp_forward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act)
+    one = lib.mlp_backward_per_example(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, saved,
+                                       ins["dy"], 1)
+    full = lib.mlp_backward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, saved, ins["dy"])
+    torch.cuda.synchronize()
+    sq = 0.0
+    for k in MLP_GRADS:
+        a = one[k] if k == "dx" else one[k][0]
+        parity(k, a, f64(full[k]))
+        if k != "dx":
+            sq += float((a.double() ** 2).sum())
+    assert abs(float(one["sq_norms"][0]) - sq) <= 1e-3 * sq
+
+    x0 = torch.empty(0, cfg.h, dtype=torch.bfloat16, device=DEV)
+    _, saved0 = lib.mlp_forward(x0, lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act)
+    z = lib.mlp_backward_per_example(x0, lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, saved0,
+                                     torch.empty(0, cfg.h, dtype=torch.bfloat16, device=DEV), 3)
+    torch.cuda.synchronize()
+    for k in ("dA_gate", "dB_gate", "dA_up", "dB_up", "dA_down", "dB_down"):
+        assert z[k].shape[0] == 3 and bool(torch.all(z[k] == 0))
+    assert bool(torch.all(z["sq_norms"] == 0))
+    assert lib.poll_status() == 0
