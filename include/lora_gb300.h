@@ -36,8 +36,11 @@
  *   memory, token-major for activations: x [M x in], y [M x out]; M = batch * seq.
  *   W [out x in], A [r x in], B [out x r], dA [r x in], dB [out x r].
  * - The caller owns and allocates every buffer, including `saved` and `ws`; the
- *   library allocates no memory and never synchronises (lora_poll_status aside).
- *   All work is enqueued on `stream`, in order.
+ *   library allocates no memory and never synchronises (lora_poll_status and
+ *   lora_trace_read aside).  All work is enqueued on `stream`, in order.  Kernels are
+ *   launched with programmatic dependent launch (each waits for the previous work on
+ *   the stream before it touches memory; environment LORA_PDL=0 turns the attribute
+ *   off), so stream order holds as usual for the caller's own work around the calls.
  * - Gradient outputs (dx, dA, dB) are overwritten, not accumulated.
  * - Alignment: every pointer 16-byte aligned (`ws` and `saved` 256-byte aligned);
  *   every feature size (in, out, h, i, n_q, n_kv) a multiple of 8.  A and B need no
@@ -264,14 +267,15 @@ uint64_t lora_wait_timeout(void);
  * range. */
 lora_status_t lora_test_expire_waits(int launches);
 
-/* Launch tracing, for measurement.  lora_trace_enable(n) makes every later launch
- * record a pair of CUDA events around itself on its stream, keeping the first n
- * launches (0 disables and frees the events).  lora_trace_read synchronises the
+/* Launch tracing, for measurement.  lora_trace_enable(n) makes every later launch (of
+ * the kinds lora_trace_kinds selects; all by default) record a pair of CUDA events
+ * around itself on its stream, keeping the first n launches (0 disables and frees
+ * the events).  lora_trace_read synchronises the
  * recorded events, fills kind[] and ms[] (kernel kinds below) for up to `max`
  * launches, and restarts the trace; it returns the number filled or -1 on error. */
 enum {
   LORA_KIND_PACK = 0,        /* adapter packing */
-  LORA_KIND_REDUCE = 1,      /* split-K reduction of the rank-r products */
+  LORA_KIND_REDUCE = 1,      /* split-K sums of the rank-r products; per-example norms */
   LORA_KIND_RANK_PROJ = 2,   /* token-major rank-r projections (x A^T, dy B, dg B) */
   LORA_KIND_RANK_GRAD = 3,   /* reductions over tokens (dA, dB) */
   LORA_KIND_GATE_UP = 4,     /* gate/up GEMM with the activation epilogue */
