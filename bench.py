@@ -266,13 +266,14 @@ def oracle_step_fn(cfg, tokens: int, host):
     return step
 
 
-def host_inputs(cfg, max_tokens: int):
-    """Float64 copies of the workload's bf16 inputs (tokens truncated)."""
+def host_inputs(cfg, max_tokens: int, seed: int = 0):
+    """Float64 copies of the workload's bf16 inputs (tokens truncated; the generator's
+    streams do not depend on the token count, so these are the workload's first rows)."""
     import torch
     import synth
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     c = cfg.replace(M=max_tokens)
-    t = synth.make_mlp_inputs(c, seed=0, device=dev)
+    t = synth.make_mlp_inputs(c, seed=seed, device=dev)
     return {k: synth.bf16_to_f64(x) for k, x in t.items()}
 
 
@@ -287,12 +288,12 @@ def parity_errors(got, ref) -> dict:
             "max_abs_over_max_ref": float(np.abs(g - ref).max() / np.abs(ref).max())}
 
 
-def cpu_baseline(cfg, budget_s: float = 15.0, got=None):
+def cpu_baseline(cfg, budget_s: float = 15.0, got=None, seed: int = 0):
     """Times the oracle as it stands on a sample of tokens sized for ~budget_s.  got:
     the GPU's results for the first tokens ({"y": ..., "dx": ...}, bf16 on the host):
     the sample's oracle results then also give the parity errors of those rows."""
     probe = 64
-    host = host_inputs(cfg, 4096)
+    host = host_inputs(cfg, 4096, seed)
     t0 = time.perf_counter()
     oracle_step_fn(cfg, probe, host)()
     per_tok = (time.perf_counter() - t0) / probe
@@ -322,7 +323,7 @@ def run_reference(args):
         return 0
     import synth
     cfg = synth.MLP_CONFIGS[args.workload]
-    host = host_inputs(cfg, 4096)
+    host = host_inputs(cfg, 4096, args.seed)
     probe = 32
     t0 = time.perf_counter()
     oracle_step_fn(cfg, probe, host)()
@@ -371,7 +372,7 @@ def run_ours(args):
     if args.act:
         cfg = cfg.replace(act=args.act)
     M, h, i, r = cfg.M, cfg.h, cfg.i, cfg.r
-    t = synth.make_mlp_inputs(cfg, seed=0, device=device)
+    t = synth.make_mlp_inputs(cfg, seed=args.seed, device=device)
     lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
     gate, up, down = lin("gate"), lin("up"), lin("down")
     saved_b, ws_b = lib.mlp_sizes(M, h, i, r)
@@ -495,7 +496,7 @@ def run_ours(args):
             got["dx"] = dx[:4096].cpu()
         del t
         torch.cuda.empty_cache()
-        cpu = cpu_baseline(cfg, got=got)
+        cpu = cpu_baseline(cfg, got=got, seed=args.seed)
     traffic = ncu_traffic(dom)
     line = {
         "metric": METRIC, "value": world * M * args.steps / secs, "unit": "tokens/s", "n_gpus": world,
@@ -503,7 +504,8 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded generator: x, dy ~ N(0,1), W ~ N(0,1/fan_in), A ~ U(+-1/sqrt(fan_in)), "
                 "B ~ N(0,0.02))",
-        "config": {"workload": workload_name(cfg) + (f", per-example adapter gradients of {n_ex} examples"
+        "config": {"seed": args.seed,
+                   "workload": workload_name(cfg) + (f", per-example adapter gradients of {n_ex} examples"
                                                       if n_ex else ""),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (weights 352 MB + activations per step)"},
@@ -543,7 +545,7 @@ def run_qkvo(args):
     dist_init("nccl")
     lib.load()
     cfg = synth.QKVO_CONFIGS[args.workload]
-    t = synth.make_qkvo_inputs(cfg, seed=0, device=device)
+    t = synth.make_qkvo_inputs(cfg, seed=args.seed, device=device)
     lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
     rope = None
     if args.rope:
@@ -617,12 +619,21 @@ def main(argv=None):
     ap.add_argument("--per-example", type=int, default=0, metavar="N",
                     help="backward with per-example adapter gradients of N examples (DP-SGD)")
     ap.add_argument("--rope", action="store_true", help="Q/K/V+O workloads: RoPE on q and k")
+    ap.add_argument("--seed", type=int, default=0, help="seed of the synthetic inputs")
+    ap.add_argument("--list", action="store_true", help="list the workloads and exit")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     import synth
+    if args.list:
+        for name, c in synth.MLP_CONFIGS.items():
+            print(f"{name:10s} LoRA-MLP fwd+bwd  M={c.M} h={c.h} i={c.i} r={c.r} alpha={c.alpha:g} {c.act}")
+        for name, c in synth.QKVO_CONFIGS.items():
+            print(f"{name:10s} LoRA Q/K/V+O fwd+bwd  M={c.M} h={c.h} heads {c.heads_q}/{c.heads_kv} x "
+                  f"{c.head_dim} r={c.r} alpha={c.alpha:g}  (--rope: RoPE on q and k)")
+        return 0
     if args.workload not in synth.MLP_CONFIGS and args.workload not in synth.QKVO_CONFIGS:
         ap.error(f"unknown workload {args.workload}")
     if args.impl == "reference":
