@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_NAME = "liblora_gb300.so"
-SOURCES = ("lora_api.cu", "gemm_big.cu", "gemm_skinny.cu", "noalloc.cu")
+SOURCES = ("lora_api.cu", "lora_linear.cu", "lora_mlp.cu", "lora_qkvo.cu", "gemm_big.cu", "gemm_skinny.cu",
+           "noalloc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "--expt-relaxed-constexpr", "-I" + INCLUDE, "-diag-suppress", "1160"]

@@ -1,0 +1,88 @@
+// Declarations shared by the entry-point files (lora_linear.cu, lora_mlp.cu,
+// lora_qkvo.cu); lora_api.cu defines them.
+#pragma once
+
+#include <nvtx3/nvToolsExt.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "host.cuh"
+
+namespace lgb {
+
+#define LGB_TRY(expr)                       \
+  do {                                      \
+    lora_status_t _st = (expr);             \
+    if (_st != LORA_OK) return _st;         \
+  } while (0)
+
+typedef __nv_bfloat16 bf16;
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+inline bool lin_ok(const lora_linear_t& l) { return l.W && l.A && l.B; }
+inline bool lin_aligned(const lora_linear_t& l) { return aligned(l.W, 16) && aligned(l.A, 2) && aligned(l.B, 2); }
+inline static void check_size(int64_t v, lora_status_t& st) {
+  if (v <= 0) st = LORA_ERR_INVALID_ARG;
+}
+
+// M >= 0, r >= 1, s finite.
+lora_status_t check_common(int64_t M, int r, float s);
+
+// An NVTX range around each entry point, so that profilers can attribute the launches
+// to the call (no cost beyond a pointer test when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// Adapter packing: block `src` (row stride lds) lands at (ro, co) of job J's dense
+// destination, optionally transposed and scaled.
+void pack_block(PackJob& J, const void* src, int64_t lds, int ro, int co, int R, int C, int trans, float scale);
+PackJob& pack_job(PackParams& P, void* dst, int64_t rows, int64_t cols);
+
+// C[M x kf] = src[M x K] * P^T with P [kf x K] packed (token-major rank-r
+// projection), written as bf16 into dst [M x kf].  `extra` adds more (src, P, K)
+// segments summed into the same output.
+struct ProjSeg {
+  const void* src;
+  const void* P;
+  int64_t K;
+};
+lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int nseg, void* dst, float* part,
+                              unsigned* status, cudaStream_t st);
+// f32 slab elements of a rank-r projection over ktotal_blocks 64-wide k-blocks.
+int64_t rank_projection_part(int64_t M, int kf, int64_t ktotal_blocks);
+
+// Reductions over tokens: for each job j, D_j[f x kf] = Q_j[tokens x f]^T * T[tokens x kf],
+// then out = s * D_j[:, col0 .. col0+r) written as [f x r] (dB) or transposed [r x f] (dA).
+struct GradJob {
+  const void* Q;      // [M x f] token-major
+  int64_t f;
+  int col0;           // rank slot inside T
+  void* dst;
+  int trans;          // 1: dst is [r x f] (dA), 0: dst is [f x r] (dB)
+};
+// f32 slab elements of the token reductions of n products (fs[j] features each).
+// n_ex > 0: per-example mode, one slab per example.
+int64_t token_grad_part(int64_t M, int kf, const int64_t* fs, int n, int64_t n_ex = 0);
+
+// Reductions over tokens whose results no later launch of a call reads (the dA, dB
+// outputs): each keeps its own f32 slabs, and one reduce launch at the end of the call
+// sums them all.
+struct Deferred {
+  RedParams rp;
+  float* cursor;      // next free slab element
+};
+void defer_init(Deferred& d, float* slabs);
+lora_status_t defer_flush(Deferred& d, cudaStream_t st);
+// Reductions over tokens of the jobs (see lora_api.cu); late: the launch reads nothing
+// the previous kernel writes and writes nothing it reads (pdl_late).
+lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* T, const GradJob* jobs, int njobs,
+                          Deferred& defer, unsigned* status, cudaStream_t st, int64_t n_ex = 0, bool late = false);
+
+lora_status_t launch_rope(const RopeParams& p, cudaStream_t st);
+
+}  // namespace lgb
