@@ -189,20 +189,24 @@ constexpr float kSqrtHalf = 0.7071067811865476f;
 constexpr float kInvSqrt2Pi = 0.3989422804014327f;
 
 // act(g): silu, tanh-GELU or exact GELU ("Model Patches and Kernels", activation table).
-__device__ __forceinline__ float act_fwd(float g, int act) {
-  if (act == ACT_SWIGLU) return __fdividef(g, 1.0f + __expf(-g));
-  if (act == ACT_GEGLU_ERF) return 0.5f * g * (1.0f + erff(g * kSqrtHalf));
+// The activation is a template argument: the act epilogue picks it once per 32-column
+// chunk (act_chunk below), so its unrolled per-element loop carries no branch on it.
+template <int ACT>
+__device__ __forceinline__ float act_fwd(float g) {
+  if (ACT == ACT_SWIGLU) return __fdividef(g, 1.0f + __expf(-g));
+  if (ACT == ACT_GEGLU_ERF) return 0.5f * g * (1.0f + erff(g * kSqrtHalf));
   const float t = tanh_approx(kSqrt2OverPi * (g + kGeluC * g * g * g));
   return 0.5f * g * (1.0f + t);
 }
 
 // act(g) and act'(g) together.
-__device__ __forceinline__ void act_fwd_bwd(float g, int act, float& a, float& ap) {
-  if (act == ACT_SWIGLU) {
+template <int ACT>
+__device__ __forceinline__ void act_fwd_bwd(float g, float& a, float& ap) {
+  if (ACT == ACT_SWIGLU) {
     const float sg = __fdividef(1.0f, 1.0f + __expf(-g));
     a = g * sg;
     ap = sg * (1.0f + g * (1.0f - sg));
-  } else if (act == ACT_GEGLU_ERF) {
+  } else if (ACT == ACT_GEGLU_ERF) {
     const float cdf = 0.5f * (1.0f + erff(g * kSqrtHalf));
     a = g * cdf;
     ap = cdf + g * kInvSqrt2Pi * __expf(-0.5f * g * g);
@@ -210,6 +214,36 @@ __device__ __forceinline__ void act_fwd_bwd(float g, int act, float& a, float& a
     const float t = tanh_approx(kSqrt2OverPi * (g + kGeluC * g * g * g));
     a = 0.5f * g * (1.0f + t);
     ap = 0.5f * (1.0f + t) + 0.5f * g * (1.0f - t * t) * kSqrt2OverPi * (1.0f + 3.0f * kGeluC * g * g);
+  }
+}
+
+// The same with the activation chosen at run time, per element.  The act' epilogue
+// uses this form: with one compiled copy per activation its 8-warp kernels (at most 168
+// registers a thread) spill, and that costs more than the per-element branch.
+__device__ __forceinline__ void act_fwd_bwd_rt(float g, int act, float& a, float& ap) {
+  if (act == ACT_SWIGLU) {
+    act_fwd_bwd<ACT_SWIGLU>(g, a, ap);
+  } else if (act == ACT_GEGLU_ERF) {
+    act_fwd_bwd<ACT_GEGLU_ERF>(g, a, ap);
+  } else {
+    act_fwd_bwd<ACT_GEGLU_TANH>(g, a, ap);
+  }
+}
+
+// Calls f(tag) with tag's `value` the activation, so f is compiled once per activation
+// and the branch is taken once per call instead of once per element.
+template <int ACT>
+struct ActTag {
+  static constexpr int value = ACT;
+};
+template <typename F>
+__device__ __forceinline__ void act_chunk(int act, F&& f) {
+  if (act == ACT_SWIGLU) {
+    f(ActTag<ACT_SWIGLU>{});
+  } else if (act == ACT_GEGLU_ERF) {
+    f(ActTag<ACT_GEGLU_ERF>{});
+  } else {
+    f(ActTag<ACT_GEGLU_TANH>{});
   }
 }
 
@@ -296,12 +330,15 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
       if (row_ok) {
         const long long off = static_cast<long long>(row) * G.ldo + col0;
         uint32_t w[16];
+        act_chunk(p.act, [&](auto tag) {
+          constexpr int ACT = decltype(tag)::value;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float h0 = act_fwd(__uint_as_float(vg[2 * e]), p.act) * __uint_as_float(vu[2 * e]);
-          const float h1 = act_fwd(__uint_as_float(vg[2 * e + 1]), p.act) * __uint_as_float(vu[2 * e + 1]);
-          w[e] = pack_bf16x2(h0, h1);
-        }
+          for (int e = 0; e < 16; ++e) {
+            const float h0 = act_fwd<ACT>(__uint_as_float(vg[2 * e])) * __uint_as_float(vu[2 * e]);
+            const float h1 = act_fwd<ACT>(__uint_as_float(vg[2 * e + 1])) * __uint_as_float(vu[2 * e + 1]);
+            w[e] = pack_bf16x2(h0, h1);
+          }
+        });
         store_row32_bf16(hout + off, w, col0, G.N, v8);
         if (gout != nullptr) {
 #pragma unroll
@@ -359,8 +396,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
             float a0, ap0, a1, ap1;
             const float g0 = bf16_lo(gg[e]), g1 = bf16_hi(gg[e]);
             const float u0 = bf16_lo(uu[e]), u1 = bf16_hi(uu[e]);
-            act_fwd_bwd(g0, p.act, a0, ap0);
-            act_fwd_bwd(g1, p.act, a1, ap1);
+            act_fwd_bwd_rt(g0, p.act, a0, ap0);
+            act_fwd_bwd_rt(g1, p.act, a1, ap1);
             const float d0 = __uint_as_float(v[8 * j + 2 * e]);
             const float d1 = __uint_as_float(v[8 * j + 2 * e + 1]);
             og[4 * j + e] = pack_bf16x2(d0 * u0 * ap0, d1 * u1 * ap1);
