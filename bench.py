@@ -194,15 +194,21 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from profiles/traffic.md, if that capture
-    was taken on the current kernel source; else None."""
+def traffic_workload_key(cfg) -> str:
+    """The workload column of profiles/traffic.md for an MLP config."""
+    return f"{cfg.name} M={cfg.M} h={cfg.h} i={cfg.i} r={cfg.r}"
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` (traffic_workload_key) from
+    profiles/traffic.md, if that capture was taken on the current kernel source; else
+    None."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
     try:
         sha = kernel_source_sha()
         for line in open(path):
             cells = [c.strip() for c in line.strip().strip("|").split("|")]
-            if len(cells) >= 4 and cells[0] == kernel and cells[2] == sha:
+            if len(cells) >= 4 and cells[0] == kernel and cells[1] == workload and cells[2] == sha:
                 return float(cells[3])
     except (OSError, ValueError):
         pass
@@ -322,7 +328,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import synth
-    cfg = synth.MLP_CONFIGS[args.workload]
+    cfg = mlp_config(args)
     host = host_inputs(cfg, 4096, args.seed)
     probe = 32
     t0 = time.perf_counter()
@@ -353,6 +359,18 @@ def run_reference(args):
     return 0
 
 
+def mlp_config(args):
+    """The MLP workload with the command line's activation and rank overrides (a rank
+    override keeps the scale s = alpha / r)."""
+    import synth
+    cfg = synth.MLP_CONFIGS[args.workload]
+    if args.act:
+        cfg = cfg.replace(act=args.act)
+    if args.rank:
+        cfg = cfg.replace(r=args.rank, alpha=cfg.s * args.rank)
+    return cfg
+
+
 def workload_name(cfg):
     return (f"{cfg.name}-shaped LoRA-MLP fwd+bwd: M={cfg.M} tokens ({cfg.batch}x{cfg.seq}), h={cfg.h}, "
             f"i={cfg.i}, r={cfg.r}, alpha={cfg.alpha:g}, {cfg.act}")
@@ -368,9 +386,7 @@ def run_ours(args):
     torch.cuda.set_device(device)
     dist_init("nccl")
     lib.load()
-    cfg = synth.MLP_CONFIGS[args.workload]
-    if args.act:
-        cfg = cfg.replace(act=args.act)
+    cfg = mlp_config(args)
     M, h, i, r = cfg.M, cfg.h, cfg.i, cfg.r
     t = synth.make_mlp_inputs(cfg, seed=args.seed, device=device)
     lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
@@ -497,7 +513,7 @@ def run_ours(args):
         del t
         torch.cuda.empty_cache()
         cpu = cpu_baseline(cfg, got=got, seed=args.seed)
-    traffic = ncu_traffic(dom)
+    traffic = ncu_traffic(dom, traffic_workload_key(cfg))
     line = {
         "metric": METRIC, "value": world * M * args.steps / secs, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -545,6 +561,8 @@ def run_qkvo(args):
     dist_init("nccl")
     lib.load()
     cfg = synth.QKVO_CONFIGS[args.workload]
+    if args.rank:
+        cfg = cfg.replace(r=args.rank, alpha=cfg.s * args.rank)
     t = synth.make_qkvo_inputs(cfg, seed=args.seed, device=device)
     lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
     rope = None
@@ -616,6 +634,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--act", choices=("swiglu", "geglu_tanh", "geglu_erf"), default=None,
                     help="override the workload's activation")
+    ap.add_argument("--rank", type=int, default=0, metavar="R",
+                    help="override the workload's adapter rank (keeping s = alpha / r)")
     ap.add_argument("--per-example", type=int, default=0, metavar="N",
                     help="backward with per-example adapter gradients of N examples (DP-SGD)")
     ap.add_argument("--rope", action="store_true", help="Q/K/V+O workloads: RoPE on q and k")
@@ -626,6 +646,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.rank < 0:
+        ap.error("--rank must be positive")
     import synth
     if args.list:
         for name, c in synth.MLP_CONFIGS.items():

@@ -77,6 +77,20 @@ def test_mlp_tiny(lib, act, M):
         parity(k, g[k], b[k])
 
 
+@pytest.mark.parametrize("act", ["swiglu", "geglu_tanh", "geglu_erf"])
+def test_mlp_long_k_activations(lib, act):
+    """h = 2304 gives the gate/up GEMM 37 k-blocks (> 32), so the forward runs the
+    4-epilogue-warp pair kernel (the tiny cases take the 8-warp short-K one); each
+    activation's compiled copy of the act epilogue is checked on both."""
+    cfg = synth.MLP_CONFIGS["tiny"].replace(M=260, h=2304, i=520, r=16, alpha=32, act=act)
+    t, v = _mlp_inputs(cfg, seed=7)
+    y, g = mlp_gpu(lib, t, cfg)
+    f, b = mlp_oracle(v, cfg)
+    parity("y", y, f["y"])
+    for k in MLP_GRADS:
+        parity(k, g[k], b[k])
+
+
 @pytest.mark.parametrize("r", [1, 8, 64, 128])
 def test_mlp_ranks(lib, r):
     cfg = synth.MLP_CONFIGS["tiny"].replace(M=200, h=256, i=520, r=r, alpha=2 * r)
