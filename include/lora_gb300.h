@@ -47,7 +47,8 @@
  *   alignment beyond their element size.  Violations return LORA_ERR_ALIGNMENT.
  * - Rank limits: 1 <= r, and (number of adapters sharing one input) * r <= 256,
  *   i.e. r <= 128 for the MLP's gate/up pair and r <= 85 for q/k/v; otherwise
- *   LORA_ERR_UNSUPPORTED.
+ *   LORA_ERR_UNSUPPORTED.  Size limits: M and every feature size at most 2^31 - 1
+ *   (32-bit row, column and tile indices); otherwise LORA_ERR_UNSUPPORTED.
  * - Every argument error returns before anything is enqueued.  No entry point
  *   aborts, throws or prints.
  * - `ws` must hold lora_*_workspace_bytes(...) bytes; its first 256 bytes hold the
@@ -78,7 +79,7 @@ typedef enum {
   LORA_OK = 0,
   LORA_ERR_INVALID_ARG = 1,   /* NULL pointer, negative size, bad enum, non-finite s */
   LORA_ERR_ALIGNMENT = 2,     /* pointer or feature size violates the alignment rules */
-  LORA_ERR_UNSUPPORTED = 3,   /* rank beyond the limits above */
+  LORA_ERR_UNSUPPORTED = 3,   /* rank or size beyond the limits above */
   LORA_ERR_WORKSPACE = 4,     /* ws_bytes below the workspace query */
   LORA_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
   LORA_ERR_TIMEOUT = 6,       /* a kernel's bounded wait expired (read by lora_poll_status) */

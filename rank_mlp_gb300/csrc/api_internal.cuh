@@ -23,10 +23,14 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 inline bool lin_ok(const lora_linear_t& l) { return l.W && l.A && l.B; }
 inline bool lin_aligned(const lora_linear_t& l) { return aligned(l.W, 16) && aligned(l.A, 2) && aligned(l.B, 2); }
 inline static void check_size(int64_t v, lora_status_t& st) {
-  if (v <= 0) st = LORA_ERR_INVALID_ARG;
+  if (v <= 0) {
+    st = LORA_ERR_INVALID_ARG;
+  } else if (v > kMaxExtent && st == LORA_OK) {
+    st = LORA_ERR_UNSUPPORTED;
+  }
 }
 
-// M >= 0, r >= 1, s finite.
+// M >= 0 (LORA_ERR_UNSUPPORTED above kMaxExtent), r >= 1, s finite.
 lora_status_t check_common(int64_t M, int r, float s);
 
 // An NVTX range around each entry point, so that profilers can attribute the launches

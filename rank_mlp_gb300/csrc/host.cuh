@@ -36,6 +36,10 @@ enum Variant : int {
 // epilogue of the previous tile (~8 us for gate/up with SwiGLU).
 constexpr int kShortKBlocks = 32;
 
+// Largest token count or feature size: the kernels index rows, columns and tiles with
+// 32-bit integers and TMA coordinates are 32-bit.
+constexpr int64_t kMaxExtent = 0x7fffffff;
+
 constexpr bool variant_pair(int v) { return v == VP_KK || v == VP_KMN || v == VP_KK8; }
 constexpr int variant_bn(int v) { return variant_pair(v) ? 256 : (v <= V64_MNMN ? 64 : 128); }
 constexpr bool variant_a_mn(int v) { return v == V64_MNMN || v == V128_MNMN; }

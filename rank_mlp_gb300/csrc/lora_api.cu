@@ -359,6 +359,7 @@ lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* T, cons
 
 lora_status_t check_common(int64_t M, int r, float s) {
   if (M < 0 || r < 1 || !std::isfinite(s)) return LORA_ERR_INVALID_ARG;
+  if (M > kMaxExtent) return LORA_ERR_UNSUPPORTED;
   return LORA_OK;
 }
 

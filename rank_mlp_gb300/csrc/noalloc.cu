@@ -43,7 +43,7 @@ extern "C" lora_status_t lora_linear_forward_noalloc(int64_t M, int64_t in, int6
   auto al = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
   if (M < 0 || in <= 0 || out <= 0 || r < 1 || !std::isfinite(s)) return LORA_ERR_INVALID_ARG;
   if ((M > 0 && (x == nullptr || y == nullptr)) || !lin.W || !lin.A || !lin.B) return LORA_ERR_INVALID_ARG;
-  if (r > 256) return LORA_ERR_UNSUPPORTED;
+  if (r > 256 || M > lgb::kMaxExtent || in > lgb::kMaxExtent || out > lgb::kMaxExtent) return LORA_ERR_UNSUPPORTED;
   if (in % 8 || out % 8 || !al(x, 16) || !al(y, 16) || !al(lin.W, 16) || !al(lin.A, 2) || !al(lin.B, 2))
     return LORA_ERR_ALIGNMENT;
   if (lora_linear_workspace_bytes(M, in, out, r) > kNoAllocScratchBytes) return LORA_ERR_WORKSPACE;

@@ -161,6 +161,20 @@ def test_backward_needs_saved(L):
                                g, g, g, ALIGNED, ws, None) == 1
 
 
+def test_sizes_beyond_32_bit_indices_are_unsupported(L):
+    """M or a feature size above 2^31 - 1 is rejected (LORA_ERR_UNSUPPORTED) before any
+    pointer is touched: the kernels index rows, columns and tiles with 32-bit ints."""
+    big = 1 << 31
+    assert _mlp_fwd(L, M=big, ws_bytes=1 << 62) == 3
+    assert _mlp_fwd(L, h=big, ws_bytes=1 << 62) == 3
+    assert _mlp_fwd(L, i=big, ws_bytes=1 << 62) == 3
+    assert _mlp_fwd(L, M=big - 1, h=big - 1, r=0) == 1          # invalid arguments still win
+    lin = _lin(L)
+    assert L.lora_linear_forward(big, 128, 256, 8, 1.0, ALIGNED, lin, ALIGNED, None, ALIGNED, 1 << 62,
+                                 None) == 3
+    assert L.lora_linear_forward_noalloc(64, 128, big, 8, 1.0, ALIGNED, lin, ALIGNED, None) == 3
+
+
 def test_linear_rejects(L):
     lin = _lin(L)
     ws = L.lora_linear_workspace_bytes(64, 128, 256, 8)
