@@ -370,6 +370,41 @@ def test_per_example_grads_sum_to_the_batch_gradient():
     assert math.isclose(per["sq_norms"][1], e1, rel_tol=1e-12)
 
 
+@pytest.mark.parametrize("kind", ["swiglu", "geglu_tanh", "geglu_erf"])
+def test_tokens_are_independent_rows(kind):
+    """The block acts on each token row on its own and the adapter gradients are sums
+    over tokens: permuting the tokens (x and dy together) permutes y and dx the same
+    way and leaves every dA, dB unchanged.  A token index mixed into another operand
+    (a transposed x, dy or saved tensor) breaks this."""
+    p, dy = _mlp_params(M=7, h=8, i=12, r=3, seed=19)
+    perm = np.random.default_rng(3).permutation(7)
+    args = lambda x: (x, p["Wg"], p["Ag"], p["Bg"], p["Wu"], p["Au"], p["Bu"],  # noqa: E731
+                      p["Wd"], p["Ad"], p["Bd"], 1.25, kind)
+    y = oracle.mlp_forward(*args(p["x"]))["y"]
+    yp = oracle.mlp_forward(*args(p["x"][perm]))["y"]
+    np.testing.assert_allclose(yp, y[perm], rtol=1e-13, atol=1e-13)
+    g = oracle.mlp_backward(*args(p["x"]), dy)
+    gp = oracle.mlp_backward(*args(p["x"][perm]), dy[perm])
+    np.testing.assert_allclose(gp["dx"], g["dx"][perm], rtol=1e-12, atol=1e-12)
+    for k in ("dA_gate", "dB_gate", "dA_up", "dB_up", "dA_down", "dB_down"):
+        np.testing.assert_allclose(gp[k], g[k], rtol=1e-12, atol=1e-12)
+
+
+def test_per_example_grads_follow_their_examples():
+    """Reordering whole examples (blocks of seq consecutive tokens) reorders the
+    per-example gradients and squared norms the same way."""
+    p, dy = _mlp_params(M=8, h=8, i=12, r=2, seed=23)
+    blocks = np.array([2, 0, 3, 1])
+    rows = (blocks[:, None] * 2 + np.arange(2)[None, :]).reshape(-1)
+    args = lambda x: (x, p["Wg"], p["Ag"], p["Bg"], p["Wu"], p["Au"], p["Bu"],  # noqa: E731
+                      p["Wd"], p["Ad"], p["Bd"], 0.75, "geglu_tanh")
+    a = oracle.mlp_backward_per_example(*args(p["x"]), dy, 4)
+    b = oracle.mlp_backward_per_example(*args(p["x"][rows]), dy[rows], 4)
+    for k in ("dA_gate", "dB_gate", "dA_up", "dB_up", "dA_down", "dB_down"):
+        np.testing.assert_allclose(b[k], a[k][blocks], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(b["sq_norms"], a["sq_norms"][blocks], rtol=1e-12)
+
+
 # ---------------------------------------------------------------- RoPE
 
 def _rope(M=4, n_pos=40, head_dim=4, seed=2, base=10000.0):
