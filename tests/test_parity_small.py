@@ -220,6 +220,8 @@ def test_qkvo_frozen_bias(lib):
     ("qwen05b", {"M": 2048}, 4),                    # seq 512
     ("tiny", {"M": 256, "i": 520, "h": 256, "act": "geglu_tanh"}, 4),
     ("tiny", {"M": 192, "i": 344, "h": 128, "act": "geglu_erf", "r": 64, "alpha": 128}, 3),
+    ("tiny", {"M": 24}, 24),                        # seq 1: one token per example
+    ("tiny", {"M": 35, "i": 520}, 5),               # seq 7: odd
 ])
 def test_mlp_per_example_grads(lib, name, over, n_ex):
     """DP-SGD per-example adapter gradients and their squared norms."""
