@@ -2,7 +2,7 @@
 backward, against the CPU float64 oracle ("Model Patches and Kernels", RoPE).
 
 Head sizes 64, 128 and 256 (one, two or four heads per 256-column tile), GQA head
-ratios 2 and 4, q widths that end inside a tile, equal and packed sequences,
+ratios 2, 4 and 8, q widths that end inside a tile, equal and packed sequences,
 positions far into a long context, frozen biases before the rotation, and a
 position outside the table (reported, not read).
 """
@@ -58,6 +58,7 @@ def _case(lib, M, h, hq, hkv, d, pos, n_pos, base=10000.0, bias=False, seed=0):
     (200, 512, 4, 1, 128, [17, 150, 33], True),      # packed sequences, GQA 4:1, bias
     (129, 512, 2, 1, 256, [64, 65], True),           # one head per tile
     (260, 384, 6, 2, 64, [260], False),              # q ends half-way into its second tile
+    (192, 256, 8, 1, 64, [96, 96], True),            # GQA 8:1: k and v are 64 of a 256-wide tile
 ])
 def test_qkvo_rope(lib, M, h, hq, hkv, d, lengths, bias):
     _case(lib, M, h, hq, hkv, d, synth.positions(M, lengths=lengths), n_pos=max(lengths), bias=bias)
