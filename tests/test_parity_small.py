@@ -41,6 +41,8 @@ def _linear(M, fin, fout, r, seed):
     (127, 520, 136, 16),     # K not a multiple of 64, N < one tile
     (200, 512, 384, 128),    # the widest fold of one adapter (128-column rank tiles)
     (1031, 896, 4864, 16),   # a prime token count at the Qwen-0.5B width
+    (3, 8, 8, 1),            # the smallest feature sizes: every box wider than its tensor
+    (70, 24, 40, 3),         # K and N below one 64-wide block, not powers of two
 ])
 def test_linear_forward_backward(lib, M, fin, fout, r):
     s = 2.0
@@ -84,6 +86,19 @@ def test_mlp_long_k_activations(lib, act):
     activation's compiled copy of the act epilogue is checked on both."""
     cfg = synth.MLP_CONFIGS["tiny"].replace(M=260, h=2304, i=520, r=16, alpha=32, act=act)
     t, v = _mlp_inputs(cfg, seed=7)
+    y, g = mlp_gpu(lib, t, cfg)
+    f, b = mlp_oracle(v, cfg)
+    parity("y", y, f["y"])
+    for k in MLP_GRADS:
+        parity(k, g[k], b[k])
+
+
+@pytest.mark.parametrize("M,h,i,r", [(5, 8, 16, 1), (33, 16, 8, 2)])
+def test_mlp_smallest_features(lib, M, h, i, r):
+    """Feature sizes of 8 and 16 (the alignment minimum): every tile and TMA box is
+    mostly outside the tensors and reads zeros there."""
+    cfg = synth.MLP_CONFIGS["tiny"].replace(M=M, h=h, i=i, r=r, alpha=2.0 * r)
+    t, v = _mlp_inputs(cfg, seed=M)
     y, g = mlp_gpu(lib, t, cfg)
     f, b = mlp_oracle(v, cfg)
     parity("y", y, f["y"])
