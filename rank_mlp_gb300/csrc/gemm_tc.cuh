@@ -131,37 +131,32 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   return U;
 }
 
-// Wait limit in SM cycles: timeout_ns at up to 2.5 GHz (longer at lower clocks).
-// The SM cycle counter is a register read; the global nanosecond timer is not.
-__device__ __forceinline__ long long timeout_cycles(const TcParams& p) {
-  return static_cast<long long>(p.timeout_ns) * 5 / 2;
-}
-
 // Bounded wait: true when the phase completed, false on abort (flag set by another
-// role, or this wait timed out, which sets the flag and the status word).
+// role, or this wait timed out, which sets the flag and the status word).  The limit
+// is wall-clock time (the global nanosecond timer, read after every failed poll from
+// the first failed one on), so it holds at any SM clock; a poll sleeps at most the
+// suspend-time hint, so the limit is seen at most two hints late.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            const TcParams& p) {
   if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (uint32_t n = 1;; ++n) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 15u) == 0) {
-      if (*abort_flag) return false;
-      if (clock64() - t0 > timeout_cycles(p)) {
-        *abort_flag = 1;
-        if (p.status) atomicOr(p.status, kStatusTimeout);
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > p.timeout_ns) {
+      *abort_flag = 1;
+      if (p.status) atomicOr(p.status, kStatusTimeout);
+      return false;
     }
   }
 }
 
 // Drain wait after an abort (this CTA's own copies or MMAs, which finish in
-// microseconds): bounded by a fixed 20 ms at up to 2.5 GHz, whatever timeout_ns is.
+// microseconds): bounded by a fixed 20 ms of wall-clock time, whatever timeout_ns is.
 __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity, const TcParams& p) {
-  const long long t0 = clock64();
+  const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > 50000000ll) {
+    if (global_timer_ns() - t0 > 20000000ull) {
       if (p.status) atomicOr(p.status, kStatusTimeout);
       return;
     }

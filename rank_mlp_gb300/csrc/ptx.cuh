@@ -40,8 +40,8 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 // True once the phase with the given parity has completed.  The thread may sleep in
-// the instruction until then (at most the suspend-time hint, 10 ms), which wakes it
-// sooner and costs the SM less than polling.
+// the instruction until then (at most the suspend-time hint, 200 us), which costs the
+// SM less than polling; the hint also bounds how late a caller's time limit is seen.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -49,7 +49,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(10000000u)
+      : "r"(bar), "r"(parity), "r"(200000u)
       : "memory");
   return ok != 0;
 }
