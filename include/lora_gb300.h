@@ -124,11 +124,16 @@ lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out, int r, fl
  * output buffers, or a latency-critical loop that must never call cudaMalloc (which
  * can synchronise the device).  Scratch comes from a fixed 32 MiB array inside the
  * library, which every GPU that loads the library holds until the process exits.
- * - Problems with lora_linear_workspace_bytes(M, in, out, r) > 32 MiB are rejected with
- *   LORA_ERR_WORKSPACE before anything is enqueued; other argument rules and results
- *   are those of lora_linear_forward with saved == NULL.
- * - The first call on a device looks up the array's device address (a one-time set-up
- *   per device); make that first call before any stream capture.
+ * - Problems whose forward needs more than 32 MiB of scratch (the forward's share of
+ *   lora_linear_workspace_bytes(M, in, out, r), which also counts the backward's) are
+ *   rejected with LORA_ERR_WORKSPACE before anything is enqueued; other argument rules
+ *   and results are those of lora_linear_forward with saved == NULL.
+ * - Asynchronous errors (an expired bounded wait) set the status word at the front of
+ *   the array; lora_poll_status(NULL, stream) reads and clears it.  It stays set across
+ *   calls until polled.
+ * - The first call on a device, and the first after the device's context was
+ *   destroyed and created again (cudaDeviceReset), looks up the array's device address;
+ *   make that first call before any stream capture.
  * - Every call on a device shares the one array and leaves its contents behind; calls
  *   whose GPU work overlaps (other streams, other threads) race and corrupt each
  *   other's results.  Calls in order on one stream are safe. */
@@ -236,7 +241,8 @@ lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv
  * lora_poll_status: synchronises `stream`, reads the asynchronous status word in
  * ws, clears it, and returns LORA_OK, LORA_ERR_TIMEOUT or LORA_ERR_DEVICE_INPUT
  * (timeout first when both are set; LORA_ERR_CUDA if the synchronisation itself
- * fails). */
+ * fails).  ws == NULL reads and clears the status word of the current device's
+ * lora_linear_forward_noalloc scratch instead (the word that call's kernels set). */
 lora_status_t lora_poll_status(void* ws, cudaStream_t stream);
 const char* lora_status_string(lora_status_t status);
 /* Kernels this library has launched in this process (all entry points). */
@@ -254,8 +260,7 @@ uint64_t lora_launch_count(void);
  * Accepted range 1 ms .. 60 s, else LORA_ERR_INVALID_ARG.  A limit shorter than
  * the slowest tile of a workload (tens of microseconds for the shapes here, longer
  * when the GPU is time-sliced with other processes) makes healthy calls fail.
- * The limit is counted in SM cycles at 2.5 GHz, so at a lower clock the wait lasts
- * proportionally longer.
+ * The limit is wall-clock time (the GPU's nanosecond timer), whatever the SM clock.
  * lora_wait_timeout: the current limit in nanoseconds. */
 lora_status_t lora_set_wait_timeout(uint64_t ns);
 uint64_t lora_wait_timeout(void);

@@ -164,6 +164,12 @@ def poll_status(ws: torch.Tensor | None = None) -> int:
     return lib.lora_poll_status(ctypes.c_void_p(ws.data_ptr()), _stream(ws.device))
 
 
+def poll_noalloc_status() -> int:
+    """Reads and clears the status word of lora_linear_forward_noalloc's scratch on the
+    current device (lora_poll_status with ws = NULL); syncs the current stream."""
+    return load().lora_poll_status(None, _stream(torch.cuda.current_device()))
+
+
 def launch_count() -> int:
     return int(load().lora_launch_count())
 

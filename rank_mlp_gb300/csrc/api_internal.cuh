@@ -89,4 +89,12 @@ lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* T, cons
 
 lora_status_t launch_rope(const RopeParams& p, cudaStream_t st);
 
+// Workspace bytes lora_linear_forward needs (its share of lora_linear_workspace_bytes,
+// which also covers the backward); 0 for invalid sizes.  Defined in lora_linear.cu.
+size_t linear_forward_workspace_bytes(int64_t M, int64_t in, int64_t out, int r);
+// Device address of lora_linear_forward_noalloc's fixed scratch on the current device
+// (its first 256 bytes are that call's status word), or NULL on a CUDA error.
+// Defined in noalloc.cu.
+void* noalloc_scratch();
+
 }  // namespace lgb

@@ -370,7 +370,11 @@ using namespace lgb;
 // ================================================================ status and trace
 
 extern "C" lora_status_t lora_poll_status(void* ws, cudaStream_t stream) {
-  if (ws == nullptr || !aligned(ws, 256)) return LORA_ERR_INVALID_ARG;
+  if (ws == nullptr) {
+    ws = noalloc_scratch();     // the no-allocation forward's status word on this device
+    if (ws == nullptr) return LORA_ERR_CUDA;
+  }
+  if (!aligned(ws, 256)) return LORA_ERR_INVALID_ARG;
   unsigned host = 0;
   if (cudaMemcpyAsync(&host, ws, sizeof(unsigned), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return LORA_ERR_CUDA;

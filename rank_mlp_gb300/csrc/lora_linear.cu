@@ -60,6 +60,11 @@ extern "C" size_t lora_linear_workspace_bytes(int64_t M, int64_t in, int64_t out
   return L.ws_fwd > L.ws_bwd ? L.ws_fwd : L.ws_bwd;
 }
 
+size_t lgb::linear_forward_workspace_bytes(int64_t M, int64_t in, int64_t out, int r) {
+  if (M < 0 || in <= 0 || out <= 0 || r < 1) return 0;
+  return linear_layout(M, in, out, r).ws_fwd;
+}
+
 extern "C" lora_status_t lora_linear_forward(int64_t M, int64_t in, int64_t out, int r, float s, const void* x,
                                              lora_linear_t lin, void* y, void* saved, void* ws, size_t ws_bytes,
                                              cudaStream_t stream) {

@@ -182,7 +182,7 @@ def test_linear_rejects(L):
     assert L.lora_linear_forward(64, 128, 256, 8, 1.0, ALIGNED, _lin(L, w=ALIGNED + 8), ALIGNED, None,
                                  ALIGNED, ws, None) == 2
     assert L.lora_linear_forward(64, 128, 256, 8, 1.0, ALIGNED, lin, ALIGNED, None, ALIGNED, 10, None) == 4
-    assert L.lora_poll_status(None, None) == 1
+    assert L.lora_poll_status(ALIGNED + 16, None) == 1      # ws not 256-byte aligned
 
 
 def test_wait_limit_range(L):
