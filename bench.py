@@ -25,6 +25,7 @@ import subprocess
 import sys
 import tempfile
 import time
+import types
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -184,6 +185,40 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+# The sustained peak is a cuBLAS loop run back to back for about 4 s under the power
+# cap; a shorter timed region runs at burst clocks and is held to the burst peak.
+SUSTAINED_REGION_S = 4.0
+# Nominal dense bf16 tensor rate of a GB300 (context only: the measured peaks are the
+# denominators).
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def choose_peak(region_s: float, peaks: dict):
+    """(key, TFLOP/s) of the measured bf16 peak that applies to a timed region of
+    region_s seconds: the burst peak unless the region is as long as the loop the
+    sustained peak was measured over."""
+    if region_s >= SUSTAINED_REGION_S and "bf16_tflops_sustained" in peaks:
+        return "bf16_tflops_sustained", float(peaks["bf16_tflops_sustained"])
+    return "bf16_tflops", float(peaks["bf16_tflops"])
+
+
+def peak_fields(tflops: float, region_s: float):
+    """The line's peak fields for a whole-step rate: the fraction against the peak
+    that applies to the region, plus the other measured peak and the nominal rate,
+    each labelled."""
+    peaks, src = measured_peaks()
+    key, peak = choose_peak(region_s, peaks)
+    out = {"tflops": tflops, "pct_of_peak": 100.0 * tflops / peak, "peak_tflops": peak,
+           "peak_source": f"{src} {key} (timed region {region_s:.3f} s; the sustained peak applies from "
+                          f"{SUSTAINED_REGION_S:g} s)",
+           "timed_region_s": region_s,
+           "pct_of_nominal_dense_bf16": 100.0 * tflops / NOMINAL_BF16_TFLOPS}
+    if "bf16_tflops_sustained" in peaks:
+        out["pct_of_sustained_peak"] = 100.0 * tflops / float(peaks["bf16_tflops_sustained"])
+    out["pct_of_burst_peak"] = 100.0 * tflops / float(peaks["bf16_tflops"])
+    return out, peak, f"{src} {key}"
+
+
 def kernel_source_sha() -> str:
     """sha256[:16] over the GEMM kernels' sources (ptx.cuh, gemm_tc.cuh, gemm_pair.cuh)."""
     import hashlib
@@ -234,13 +269,11 @@ def kernel_breakdown(lib, step, steps: int) -> dict:
     return per_kind
 
 
-def timed_with_kind(lib, step, steps, world, device, stream, kind):
-    """The timed region: `steps` steps, CUDA events around the launches of `kind` only
-    (the dominant kernel), clocks sampled meanwhile.  Returns (seconds over ranks,
-    clocks, launches of the library's kernels, [ms of each traced launch])."""
+def timed_region(lib, step, steps, world, device, stream):
+    """The timed region: `steps` untraced steps (no events between launches, so the
+    kernels overlap as they do in use), clocks sampled meanwhile.  Returns (seconds,
+    max over ranks; clocks; launches of the library's kernels)."""
     import torch
-    lib.trace_kinds([kind])
-    lib.trace_enable(16 * steps + 16)
     n0 = lib.launch_count()
     rank = dist_env()[0]
     clocks = ClockSampler()
@@ -248,11 +281,22 @@ def timed_with_kind(lib, step, steps, world, device, stream, kind):
         clocks.start()
     secs = timed_steps(step, steps, world, device, torch.cuda.synchronize, cuda_timer(torch, stream))
     clk = clocks.stop() if rank == 0 else None
-    launches = lib.launch_count() - n0
+    return secs, clk, lib.launch_count() - n0
+
+
+def kernel_launch_ms(lib, step, steps, kind):
+    """A separate pass of `steps` steps with CUDA events around the launches of `kind`
+    only (the dominant kernel); returns the duration of each of its launches (ms)."""
+    import torch
+    torch.cuda.synchronize()
+    lib.trace_kinds([kind])
+    lib.trace_enable(16 * steps + 16)
+    for _ in range(steps):
+        step()
     trace = lib.trace_read(16 * steps + 16)
     lib.trace_enable(0)
     lib.trace_kinds(None)
-    return secs, clk, launches, [ms for k, ms in trace if k == kind]
+    return [ms for k, ms in trace if k == kind]
 
 
 # ---------------------------------------------------------------------------- oracle
@@ -368,6 +412,8 @@ def mlp_config(args):
         cfg = cfg.replace(act=args.act)
     if args.rank:
         cfg = cfg.replace(r=args.rank, alpha=cfg.s * args.rank)
+    if getattr(args, "tokens", 0):
+        cfg = cfg.replace(M=args.tokens)
     return cfg
 
 
@@ -376,9 +422,166 @@ def workload_name(cfg):
             f"i={cfg.i}, r={cfg.r}, alpha={cfg.alpha:g}, {cfg.act}")
 
 
-def run_ours(args):
+def mlp_workload(lib, cfg, device, seed, n_ex=0):
+    """Device-resident inputs, outputs, saved blob and workspace of one MLP workload
+    and its fwd+bwd step."""
     import torch
     import synth
+    M, h, i, r = cfg.M, cfg.h, cfg.i, cfg.r
+    t = synth.make_mlp_inputs(cfg, seed=seed, device=device)
+    lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
+    gate, up, down = lin("gate"), lin("up"), lin("down")
+    saved_b, ws_b = lib.mlp_sizes(M, h, i, r)
+    if n_ex:
+        ws_b = max(ws_b, lib.load().lora_mlp_per_example_workspace_bytes(M, h, i, r, n_ex))
+    w = types.SimpleNamespace(cfg=cfg, t=t, gate=gate, up=up, down=down, n_ex=n_ex)
+    w.saved = torch.empty(saved_b, dtype=torch.uint8, device=device)
+    w.ws = torch.zeros(ws_b, dtype=torch.uint8, device=device)
+    w.y = torch.empty(M, h, dtype=torch.bfloat16, device=device)
+    w.dx = torch.empty(M, h, dtype=torch.bfloat16, device=device)
+    e = lambda *sh: torch.empty(*sh, dtype=torch.bfloat16, device=device)  # noqa: E731
+    w.grads = {"dA_gate": e(r, h), "dB_gate": e(i, r), "dA_up": e(r, h), "dB_up": e(i, r),
+               "dA_down": e(r, i), "dB_down": e(h, r)}
+
+    def step():
+        lib.mlp_forward(t["x"], gate, up, down, cfg.s, cfg.act, y=w.y, saved=w.saved, ws=w.ws)
+        if n_ex:
+            lib.mlp_backward_per_example(t["x"], gate, up, down, cfg.s, cfg.act, w.saved, t["dy"], n_ex, ws=w.ws)
+        else:
+            lib.mlp_backward(t["x"], gate, up, down, cfg.s, cfg.act, w.saved, t["dy"], dx=w.dx, grads=w.grads,
+                             ws=w.ws)
+    w.step = step
+    w.flops = kernel_flops(cfg)
+    w.total_flops = cfg.flops()
+    w.M = M
+    return w
+
+
+def qkvo_workload(lib, cfg, device, seed, rope=False):
+    """The same for the Q/K/V + O projections (optionally with RoPE on q and k)."""
+    import torch
+    import synth
+    t = synth.make_qkvo_inputs(cfg, seed=seed, device=device)
+    lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
+    rp = None
+    if rope:
+        cos, sin = lib.rope_table(cfg.seq, cfg.head_dim, 10000.0, device=device)
+        rp = {"cos": cos, "sin": sin, "pos": synth.positions(cfg.M, seq=cfg.seq, device=device),
+              "head_dim": cfg.head_dim}
+    M, h, r = cfg.M, cfg.h, cfg.r
+    w = types.SimpleNamespace(cfg=cfg, t=t)
+    w.ws = torch.zeros(lib.load().lora_qkvo_workspace_bytes(M, h, cfg.n_q, cfg.n_kv, r), dtype=torch.uint8,
+                       device=device)
+    w.saved = torch.empty(lib.load().lora_qkvo_saved_bytes(M, h, cfg.n_q, cfg.n_kv, r), dtype=torch.uint8,
+                          device=device)
+
+    def step():
+        lib.qkvo_forward(t["x"], lin("q"), lin("k"), lin("v"), t["o_in"], lin("o"), cfg.s, rope=rp,
+                         saved=w.saved, ws=w.ws)
+        lib.qkvo_backward(t["x"], lin("q"), lin("k"), lin("v"), t["o_in"], lin("o"), cfg.s, w.saved,
+                          t["dy_q"], t["dy_k"], t["dy_v"], t["dy_o"], rope=rp, ws=w.ws)
+    w.step = step
+    w.flops = qkvo_kernel_flops(cfg)
+    w.total_flops = cfg.flops()
+    w.M = M
+    return w
+
+
+def measure(lib, w, steps, warmup, world, device, stream, breakdown_steps):
+    """Warm-up, the per-kernel breakdown (every launch traced), the untraced timed
+    region and the dominant kernel's separate traced pass.  Raises if a kernel reports
+    an asynchronous error."""
+    import torch
+    for _ in range(warmup):
+        w.step()
+    torch.cuda.synchronize()
+    per_kind = kernel_breakdown(lib, w.step, breakdown_steps) if breakdown_steps else {}
+    secs, clk, launches = timed_region(lib, w.step, steps, world, device, stream)
+    status = lib.poll_status(w.ws)
+    if status != 0:
+        raise RuntimeError(f"kernel status {status} after the timed region")
+    m = types.SimpleNamespace(secs=secs, clk=clk, launches=launches, per_kind=per_kind,
+                              ms_step=secs / steps * 1e3)
+    m.tflops = w.total_flops / (m.ms_step * 1e-3) / 1e12
+    if per_kind:
+        m.dom = max((k for k in per_kind if k in w.flops), key=lambda k: per_kind[k][1])
+        m.dom_launch_ms = kernel_launch_ms(lib, w.step, steps, m.dom)
+    return m
+
+
+def roofline_obj(w, m, peak, peak_key, traffic):
+    """The dominant kernel against the bf16 peak: algorithmic FLOPs per launch over its
+    average launch duration from the separate traced pass."""
+    launches_per_step = _launches_per_step(w, m)
+    dom_ms = sum(m.dom_launch_ms) / len(m.dom_launch_ms)
+    flops_launch = w.flops[m.dom] / launches_per_step
+    achieved = flops_launch / (dom_ms * 1e-3) / 1e12
+    peaks, _ = measured_peaks()
+    out = {"bound": "tensor", "kernel": m.dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+           "frac": achieved / peak, "peak_key": peak_key, "traffic": traffic, "launch_ms": dom_ms,
+           "flops_per_launch": flops_launch,
+           "duration_source": "average launch of a separate pass of the same number of steps, CUDA events "
+                              "around this kernel's launches only"}
+    if "bf16_tflops_sustained" in peaks:
+        out["frac_of_sustained"] = achieved / float(peaks["bf16_tflops_sustained"])
+    out["frac_of_burst"] = achieved / float(peaks["bf16_tflops"])
+    return out
+
+
+def _launches_per_step(w, m):
+    """Launches of the dominant kind per step (w.flops counts a kind's FLOPs per step)."""
+    return max(1, round(m.per_kind[m.dom][0] / max(1, m.breakdown_steps)))
+
+
+OTHER_WORKLOADS = (
+    ("gemma7b_r8", "mlp", "gemma7b", {}),
+    ("gemma7b_r64", "mlp", "gemma7b", {"r": 64}),
+    ("gqa7b", "qkvo", "gqa7b", {}),
+    ("gqa7b_rope", "qkvo", "gqa7b", {"rope": True}),
+    ("qwen05b_m4096", "mlp", "qwen05b", {}),
+    ("qwen05b_m4095", "mlp", "qwen05b", {"M": 4095}),
+)
+
+
+def other_workloads(lib, args, world, device, stream):
+    """Device-timed fwd+bwd of the other workloads (no oracle, no end-to-end copies),
+    each with its own untraced timed region, under one clock record."""
+    import torch
+    import synth
+    steps = max(10, min(args.steps, 30))
+    rank = dist_env()[0]
+    clocks = ClockSampler()
+    if rank == 0:
+        clocks.start()
+    out = {}
+    for label, kind, name, over in OTHER_WORKLOADS:
+        if kind == "mlp":
+            cfg = synth.MLP_CONFIGS[name]
+            if "r" in over:
+                cfg = cfg.replace(r=over["r"], alpha=cfg.s * over["r"])
+            if "M" in over:
+                cfg = cfg.replace(M=over["M"])
+            w = mlp_workload(lib, cfg, device, args.seed)
+            desc = workload_name(cfg)
+        else:
+            cfg = synth.QKVO_CONFIGS[name]
+            w = qkvo_workload(lib, cfg, device, args.seed, rope=over.get("rope", False))
+            desc = qkvo_name(cfg, over.get("rope", False))
+        m = measure(lib, w, steps, 3, world, device, stream, 0)
+        pf, _, _ = peak_fields(m.tflops, m.secs)
+        out[label] = {"workload": desc, "ms_per_step": m.ms_step, "tokens_per_s": world * w.M / (m.ms_step * 1e-3),
+                      "tflops": m.tflops, "pct_of_peak": pf["pct_of_peak"], "peak_tflops": pf["peak_tflops"],
+                      "steps": steps, "gpu_launches": m.launches}
+        del w
+        torch.cuda.empty_cache()
+    out["clocks"] = clocks.stop() if rank == 0 else None
+    out["note"] = (f"each: 3 warm-up and {steps} untraced timed steps on device-resident inputs; pct_of_peak "
+                   "against the measured bf16 peak that applies to its timed region")
+    return out
+
+
+def run_ours(args):
+    import torch
     from rank_mlp_gb300 import binding as lib
 
     rank, world, local = dist_env()
@@ -387,53 +590,17 @@ def run_ours(args):
     dist_init("nccl")
     lib.load()
     cfg = mlp_config(args)
-    M, h, i, r = cfg.M, cfg.h, cfg.i, cfg.r
-    t = synth.make_mlp_inputs(cfg, seed=args.seed, device=device)
-    lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
-    gate, up, down = lin("gate"), lin("up"), lin("down")
-    saved_b, ws_b = lib.mlp_sizes(M, h, i, r)
-    saved = torch.empty(saved_b, dtype=torch.uint8, device=device)
-    ws = torch.zeros(ws_b, dtype=torch.uint8, device=device)
-    y = torch.empty(M, h, dtype=torch.bfloat16, device=device)
-    dx = torch.empty(M, h, dtype=torch.bfloat16, device=device)
-    e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=device)  # noqa: E731
-    grads = {"dA_gate": e(r, h), "dB_gate": e(i, r), "dA_up": e(r, h), "dB_up": e(i, r),
-             "dA_down": e(r, i), "dB_down": e(h, r)}
-    x, dy = t["x"], t["dy"]
-
+    M, h = cfg.M, cfg.h
     n_ex = args.per_example
-    if n_ex:
-        ws = torch.zeros(max(ws_b, lib.load().lora_mlp_per_example_workspace_bytes(M, h, i, r, n_ex)),
-                         dtype=torch.uint8, device=device)
-
-    def step():
-        lib.mlp_forward(x, gate, up, down, cfg.s, cfg.act, y=y, saved=saved, ws=ws)
-        if n_ex:
-            lib.mlp_backward_per_example(x, gate, up, down, cfg.s, cfg.act, saved, dy, n_ex, ws=ws)
-        else:
-            lib.mlp_backward(x, gate, up, down, cfg.s, cfg.act, saved, dy, dx=dx, grads=grads, ws=ws)
-
+    w = mlp_workload(lib, cfg, device, args.seed, n_ex)
     stream = torch.cuda.current_stream(device)
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
 
-    # ---- per-kernel breakdown (every launch traced), then the device-resident timed
-    # region with events around the dominant kernel's launches only
+    # ---- warm-up, per-kernel breakdown (every launch traced), then the untraced timed
+    # region, then a separate pass timing the dominant kernel's launches
     nb = max(1, min(args.steps, 20))
-    per_kind = kernel_breakdown(lib, step, nb)
-    flops = kernel_flops(cfg)
-    dom = max((k for k in per_kind if k in flops), key=lambda k: per_kind[k][1])
-    secs, clk, launches, dom_trace = timed_with_kind(lib, step, args.steps, world, device, stream, dom)
-    status = lib.poll_status(ws)
-    if status != 0:
-        raise RuntimeError(f"kernel status {status} after the timed region")
-    dom_ms = sum(dom_trace) / len(dom_trace)
-    peaks, peak_src = measured_peaks()
-    peak = float(peaks["bf16_tflops_sustained"])
-    achieved = flops[dom] / (dom_ms * 1e-3) / 1e12
-    ms_step = secs / args.steps * 1e3
-    tflops = cfg.flops() / (ms_step * 1e-3) / 1e12
+    m = measure(lib, w, args.steps, args.warmup, world, device, stream, nb)
+    m.breakdown_steps = nb
+    pf, peak, peak_key = peak_fields(m.tflops, m.secs)
 
     # ---- end to end through host buffers: every step copies its x, dy from pinned host
     # memory and its y, dx, dA, dB back.  Double-buffered, as a training loop would:
@@ -441,82 +608,26 @@ def run_ours(args):
     # compute stream runs step k.
     e2e = None
     if not args.no_e2e and not n_ex:
-        cs = torch.cuda.Stream(device)
-        xh = x.cpu().pin_memory()
-        dyh = dy.cpu().pin_memory()
-        xd = [torch.empty_like(x) for _ in range(2)]
-        dyd = [torch.empty_like(dy) for _ in range(2)]
-        yd = [torch.empty_like(y) for _ in range(2)]
-        dxd = [torch.empty_like(dx) for _ in range(2)]
-        gd = [{k: torch.empty_like(v) for k, v in grads.items()} for _ in range(2)]
-        yh = torch.empty(M, h, dtype=torch.bfloat16).pin_memory()
-        dxh = torch.empty(M, h, dtype=torch.bfloat16).pin_memory()
-        gh = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in grads.items()}
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_done = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
+        e2e = run_e2e(lib, w, args, world, device, stream)
 
-        def e2e_run(steps):
-            """steps fwd+bwd through host buffers; returns seconds (CUDA events)."""
-            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            t0.record(cs)
-            with torch.cuda.stream(cs):
-                xd[0].copy_(xh, non_blocking=True)
-                dyd[0].copy_(dyh, non_blocking=True)
-                ev_in[0].record(cs)
-            for k in range(steps):
-                b = k & 1
-                stream.wait_event(ev_in[b])
-                if k >= 2:
-                    stream.wait_event(ev_out[b])              # step k-2's results have left buffers b
-                lib.mlp_forward(xd[b], gate, up, down, cfg.s, cfg.act, y=yd[b], saved=saved, ws=ws)
-                lib.mlp_backward(xd[b], gate, up, down, cfg.s, cfg.act, saved, dyd[b], dx=dxd[b], grads=gd[b],
-                                 ws=ws)
-                ev_done[b].record(stream)
-                with torch.cuda.stream(cs):
-                    if k + 1 < steps:
-                        if k >= 1:
-                            cs.wait_event(ev_done[1 - b])     # step k-1 finished reading buffers 1-b
-                        xd[1 - b].copy_(xh, non_blocking=True)
-                        dyd[1 - b].copy_(dyh, non_blocking=True)
-                        ev_in[1 - b].record(cs)
-                    cs.wait_event(ev_done[b])
-                    yh.copy_(yd[b], non_blocking=True)
-                    dxh.copy_(dxd[b], non_blocking=True)
-                    for n in grads:
-                        gh[n].copy_(gd[b][n], non_blocking=True)
-                    ev_out[b].record(cs)
-            t1.record(cs)
-            t1.synchronize()
-            return t0.elapsed_time(t1) / 1e3
-
-        e2e_run(3)
-        ke = max(1, min(args.steps, 50))
-        barrier(world, device)
-        torch.cuda.synchronize()
-        esecs = max_over_ranks(e2e_run(ke), world, device)
-        barrier(world, device)
-        h2d = 2 * M * h * 2
-        d2h = 2 * M * h * 2 + sum(v.numel() * 2 for v in grads.values())
-        e2e = {"value": world * M * ke / esecs, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": ke,
-               "path": "pinned host x, dy -> device; lora_mlp_forward + lora_mlp_backward; y, dx, dA, dB -> "
-                       "host; copies of step k+1 / k overlap step k's compute (copy stream, double buffers)"}
+    others = None
+    if not args.no_other and not n_ex:
+        others = other_workloads(lib, args, world, device, stream)
 
     if rank != 0:
         return 0
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        got = {"y": y[:4096].cpu()}
+        got = {"y": w.y[:4096].cpu()}
         if not n_ex:
-            got["dx"] = dx[:4096].cpu()
-        del t
+            got["dx"] = w.dx[:4096].cpu()
+        del w.t
         torch.cuda.empty_cache()
         cpu = cpu_baseline(cfg, got=got, seed=args.seed)
-    traffic = ncu_traffic(dom, traffic_workload_key(cfg))
+    traffic = ncu_traffic(m.dom, traffic_workload_key(cfg))
     line = {
-        "metric": METRIC, "value": world * M * args.steps / secs, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "metric": METRIC, "value": world * M * args.steps / m.secs, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": m.ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded generator: x, dy ~ N(0,1), W ~ N(0,1/fan_in), A ~ U(+-1/sqrt(fan_in)), "
                 "B ~ N(0,0.02))",
@@ -525,20 +636,87 @@ def run_ours(args):
                                                       if n_ex else ""),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (weights 352 MB + activations per step)"},
-        "tflops": tflops, "pct_of_peak": 100.0 * tflops / peak, "peak_tflops": peak,
-        "peak_source": f"{peak_src} bf16_tflops_sustained",
-        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None if traffic is None else traffic / 1.0,
-                     "launch_ms": dom_ms, "flops_per_launch": flops[dom]},
-        "kernels_ms_per_step": {k: v[1] / nb for k, v in sorted(per_kind.items())},
+        **pf,
+        "roofline": roofline_obj(w, m, peak, peak_key, traffic),
+        "kernels_ms_per_step": {k: v[1] / nb for k, v in sorted(m.per_kind.items())},
         "kernels_ms_per_step_note": f"every launch traced over {nb} separate steps (serialised by the events)",
-        "gpu_launches": launches,
-        "clocks": clk,
+        "gpu_launches": m.launches,
+        "clocks": m.clk,
         "e2e": e2e,
+        "other_workloads": others,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def run_e2e(lib, w, args, world, device, stream):
+    """fwd+bwd through pinned host buffers, double-buffered; returns the e2e object."""
+    import torch
+    cfg, t = w.cfg, w.t
+    M, h = cfg.M, cfg.h
+    x, dy, y, dx, grads = t["x"], t["dy"], w.y, w.dx, w.grads
+    cs = torch.cuda.Stream(device)
+    xh = x.cpu().pin_memory()
+    dyh = dy.cpu().pin_memory()
+    xd = [torch.empty_like(x) for _ in range(2)]
+    dyd = [torch.empty_like(dy) for _ in range(2)]
+    yd = [torch.empty_like(y) for _ in range(2)]
+    dxd = [torch.empty_like(dx) for _ in range(2)]
+    gd = [{k: torch.empty_like(v) for k, v in grads.items()} for _ in range(2)]
+    yh = torch.empty(M, h, dtype=torch.bfloat16).pin_memory()
+    dxh = torch.empty(M, h, dtype=torch.bfloat16).pin_memory()
+    gh = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in grads.items()}
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_run(steps):
+        """steps fwd+bwd through host buffers; returns seconds (CUDA events)."""
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(cs)
+        with torch.cuda.stream(cs):
+            xd[0].copy_(xh, non_blocking=True)
+            dyd[0].copy_(dyh, non_blocking=True)
+            ev_in[0].record(cs)
+        for k in range(steps):
+            b = k & 1
+            stream.wait_event(ev_in[b])
+            if k >= 2:
+                stream.wait_event(ev_out[b])              # step k-2's results have left buffers b
+            lib.mlp_forward(xd[b], w.gate, w.up, w.down, cfg.s, cfg.act, y=yd[b], saved=w.saved, ws=w.ws)
+            lib.mlp_backward(xd[b], w.gate, w.up, w.down, cfg.s, cfg.act, w.saved, dyd[b], dx=dxd[b],
+                             grads=gd[b], ws=w.ws)
+            ev_done[b].record(stream)
+            with torch.cuda.stream(cs):
+                if k + 1 < steps:
+                    if k >= 1:
+                        cs.wait_event(ev_done[1 - b])     # step k-1 finished reading buffers 1-b
+                    xd[1 - b].copy_(xh, non_blocking=True)
+                    dyd[1 - b].copy_(dyh, non_blocking=True)
+                    ev_in[1 - b].record(cs)
+                cs.wait_event(ev_done[b])
+                yh.copy_(yd[b], non_blocking=True)
+                dxh.copy_(dxd[b], non_blocking=True)
+                for n in grads:
+                    gh[n].copy_(gd[b][n], non_blocking=True)
+                ev_out[b].record(cs)
+        t1.record(cs)
+        t1.synchronize()
+        return t0.elapsed_time(t1) / 1e3
+
+    e2e_run(3)
+    ke = max(1, min(args.steps, 50))
+    barrier(world, device)
+    torch.cuda.synchronize()
+    esecs = max_over_ranks(e2e_run(ke), world, device)
+    barrier(world, device)
+    h2d = 2 * M * h * 2
+    d2h = 2 * M * h * 2 + sum(v.numel() * 2 for v in grads.values())
+    return {"value": world * M * ke / esecs, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": ke,
+            "path": "pinned host x, dy -> device; lora_mlp_forward + lora_mlp_backward; y, dx, dA, dB -> "
+                    "host; copies of step k+1 / k overlap step k's compute (copy stream, double buffers)"}
 
 
 def qkvo_kernel_flops(cfg):
@@ -547,6 +725,12 @@ def qkvo_kernel_flops(cfg):
     M, h, r, nq, nkv = cfg.M, cfg.h, cfg.r, cfg.n_q, cfg.n_kv
     return {"proj": 2.0 * M * ((nq + 2 * nkv) * (h + r) + h * (nq + r)),
             "dgrad": 2.0 * M * (h * (nq + 2 * nkv + 3 * r) + nq * (h + r))}
+
+
+def qkvo_name(cfg, rope):
+    return (f"{cfg.name}-shaped LoRA Q/K/V+O fwd+bwd: M={cfg.M} tokens ({cfg.batch}x{cfg.seq}), h={cfg.h}, "
+            f"{cfg.heads_q}/{cfg.heads_kv} heads x {cfg.head_dim}, r={cfg.r}, alpha={cfg.alpha:g}"
+            + (", RoPE on q and k (base 10000, positions restart per sequence)" if rope else ""))
 
 
 def run_qkvo(args):
@@ -563,63 +747,28 @@ def run_qkvo(args):
     cfg = synth.QKVO_CONFIGS[args.workload]
     if args.rank:
         cfg = cfg.replace(r=args.rank, alpha=cfg.s * args.rank)
-    t = synth.make_qkvo_inputs(cfg, seed=args.seed, device=device)
-    lin = lambda n: (t["W_" + n], t["A_" + n], t["B_" + n])  # noqa: E731
-    rope = None
-    if args.rope:
-        cos, sin = lib.rope_table(cfg.seq, cfg.head_dim, 10000.0, device=device)
-        rope = {"cos": cos, "sin": sin, "pos": synth.positions(cfg.M, seq=cfg.seq, device=device),
-                "head_dim": cfg.head_dim}
-    M, h, r = cfg.M, cfg.h, cfg.r
-    ws = torch.zeros(lib.load().lora_qkvo_workspace_bytes(M, h, cfg.n_q, cfg.n_kv, r), dtype=torch.uint8,
-                     device=device)
-    saved = torch.empty(lib.load().lora_qkvo_saved_bytes(M, h, cfg.n_q, cfg.n_kv, r), dtype=torch.uint8,
-                        device=device)
-
-    def step():
-        lib.qkvo_forward(t["x"], lin("q"), lin("k"), lin("v"), t["o_in"], lin("o"), cfg.s, rope=rope,
-                         saved=saved, ws=ws)
-        lib.qkvo_backward(t["x"], lin("q"), lin("k"), lin("v"), t["o_in"], lin("o"), cfg.s, saved,
-                          t["dy_q"], t["dy_k"], t["dy_v"], t["dy_o"], rope=rope, ws=ws)
-
+    if args.tokens:
+        cfg = cfg.replace(M=args.tokens)
+    w = qkvo_workload(lib, cfg, device, args.seed, rope=args.rope)
     stream = torch.cuda.current_stream(device)
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
     nb = max(1, min(args.steps, 20))
-    per_kind = kernel_breakdown(lib, step, nb)
-    flops = qkvo_kernel_flops(cfg)
-    dom = max((k for k in per_kind if k in flops), key=lambda k: per_kind[k][1])
-    secs, clk, launches, dom_trace = timed_with_kind(lib, step, args.steps, world, device, stream, dom)
-    status = lib.poll_status(ws)
-    if status != 0:
-        raise RuntimeError(f"kernel status {status} after the timed region")
+    m = measure(lib, w, args.steps, args.warmup, world, device, stream, nb)
+    m.breakdown_steps = nb
     if rank != 0:
         return 0
-    dom_ms_step = sum(dom_trace) / args.steps
-    peaks, peak_src = measured_peaks()
-    peak = float(peaks["bf16_tflops_sustained"])
-    achieved = flops[dom] / (dom_ms_step * 1e-3) / 1e12
-    ms_step = secs / args.steps * 1e3
-    tflops = cfg.flops() / (ms_step * 1e-3) / 1e12
-    name = (f"{cfg.name}-shaped LoRA Q/K/V+O fwd+bwd: M={cfg.M} tokens ({cfg.batch}x{cfg.seq}), h={h}, "
-            f"{cfg.heads_q}/{cfg.heads_kv} heads x {cfg.head_dim}, r={r}, alpha={cfg.alpha:g}"
-            + (", RoPE on q and k (base 10000, positions restart per sequence)" if args.rope else ""))
+    pf, peak, peak_key = peak_fields(m.tflops, m.secs)
     line = {
-        "metric": "LoRA Q/K/V+O fwd+bwd tokens/s", "value": world * M * args.steps / secs, "unit": "tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded generator)",
-        "config": {"workload": name, "parallelism": "replicas" if world > 1 else "single GPU",
+        "metric": "LoRA Q/K/V+O fwd+bwd tokens/s", "value": world * cfg.M * args.steps / m.secs,
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": m.ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded generator)",
+        "config": {"workload": qkvo_name(cfg, args.rope), "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2"},
-        "tflops": tflops, "pct_of_peak": 100.0 * tflops / peak, "peak_tflops": peak,
-        "peak_source": f"{peak_src} bf16_tflops_sustained",
-        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "ms_per_step": dom_ms_step,
-                     "flops_per_step": flops[dom]},
-        "kernels_ms_per_step": {k: v[1] / nb for k, v in sorted(per_kind.items())},
+        **pf,
+        "roofline": roofline_obj(w, m, peak, peak_key, None),
+        "kernels_ms_per_step": {k: v[1] / nb for k, v in sorted(m.per_kind.items())},
         "kernels_ms_per_step_note": f"every launch traced over {nb} separate steps (serialised by the events)",
-        "gpu_launches": launches, "clocks": clk, "e2e": None, "cpu_baseline": None,
+        "gpu_launches": m.launches, "clocks": m.clk, "e2e": None, "cpu_baseline": None,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -636,6 +785,8 @@ def main(argv=None):
                     help="override the workload's activation")
     ap.add_argument("--rank", type=int, default=0, metavar="R",
                     help="override the workload's adapter rank (keeping s = alpha / r)")
+    ap.add_argument("--tokens", type=int, default=0, metavar="M",
+                    help="override the workload's token count (small cases for profiler captures)")
     ap.add_argument("--per-example", type=int, default=0, metavar="N",
                     help="backward with per-example adapter gradients of N examples (DP-SGD)")
     ap.add_argument("--rope", action="store_true", help="Q/K/V+O workloads: RoPE on q and k")
@@ -643,11 +794,14 @@ def main(argv=None):
     ap.add_argument("--list", action="store_true", help="list the workloads and exit")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other", action="store_true", help="skip the other workloads' device-timed lines")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.rank < 0:
         ap.error("--rank must be positive")
+    if args.tokens < 0:
+        ap.error("--tokens must be positive")
     import synth
     if args.list:
         for name, c in synth.MLP_CONFIGS.items():
