@@ -127,7 +127,9 @@ lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out, int r, fl
  * - Problems whose forward needs more than 32 MiB of scratch (the forward's share of
  *   lora_linear_workspace_bytes(M, in, out, r), which also counts the backward's) are
  *   rejected with LORA_ERR_WORKSPACE before anything is enqueued; other argument rules
- *   and results are those of lora_linear_forward with saved == NULL.
+ *   are those of lora_linear_forward with saved == NULL, and so is the result, up to
+ *   the order of the f32 sums (this call always gives each 256 x 256 output tile to
+ *   one CTA pair).
  * - Asynchronous errors (an expired bounded wait) set the status word at the front of
  *   the array; lora_poll_status(NULL, stream) reads and clears it.  It stays set across
  *   calls until polled.
@@ -264,6 +266,26 @@ uint64_t lora_launch_count(void);
  * lora_wait_timeout: the current limit in nanoseconds. */
 lora_status_t lora_set_wait_timeout(uint64_t ns);
 uint64_t lora_wait_timeout(void);
+
+/* ---------------------------------------------------------------- split tail
+ * The projection GEMMs deal whole 256 x 256 output tiles round-robin to pairs of SMs.
+ * When the last wave would leave pairs idle, the tiles of that wave (all tiles, when
+ * there are fewer than pairs) can each be cut into 2 to 4 equal k-ranges computed by
+ * different pairs; the last piece of a tile to finish adds the others' f32 partial
+ * sums, in a fixed order, before the epilogue, so results stay deterministic for a
+ * given device and mode (and match the whole-tile schedule up to the order of the f32
+ * sums).  The partial sums live in the call's workspace (the size queries include
+ * them).  Not from the pages: a scheduling choice of this library.
+ *
+ * lora_set_split_tail: 0 (default) cuts the tail into the number of pieces (2 to 4)
+ * for which a cost model of the partial sums expects the launch to gain most, if at
+ * least 2%; 1 never cuts; 2, 3 or 4 cuts every tail into that many pieces whenever the
+ * launch allows it (every group with the same k-extent, at least 8 k-blocks per tile
+ * and two per piece, a tail of at most 128 tiles).  Process-wide, for launches enqueued
+ * after the call; the environment variable LORA_SPLIT_TAIL=1..4 sets the initial mode.
+ * Other values return LORA_ERR_INVALID_ARG.  lora_split_tail: the current mode. */
+lora_status_t lora_set_split_tail(int mode);
+int lora_split_tail(void);
 
 /* Test hook for the failure path (no counterpart in the pages): the next `launches`
  * GEMM launches (0 .. 64; 0 cancels) each leave the first pipeline stage of every

@@ -82,6 +82,8 @@ _SIGS = {
     "lora_set_wait_timeout": (_INT, [ctypes.c_uint64]),
     "lora_wait_timeout": (ctypes.c_uint64, []),
     "lora_test_expire_waits": (_INT, [_INT]),
+    "lora_set_split_tail": (_INT, [_INT]),
+    "lora_split_tail": (_INT, []),
     "lora_trace_enable": (_INT, [_INT]),
     "lora_trace_kinds": (None, [ctypes.c_uint]),
     "lora_trace_read": (_INT, [ctypes.POINTER(_INT), ctypes.POINTER(_F32), _INT]),
@@ -181,6 +183,16 @@ def set_wait_timeout(ns: int):
 
 def wait_timeout() -> int:
     return int(load().lora_wait_timeout())
+
+
+def set_split_tail(mode: int):
+    """Split-tail mode of the projection GEMMs: 0 automatic, 1 never, 2..4 every tail
+    in that many pieces."""
+    _check(load().lora_set_split_tail(mode), "lora_set_split_tail")
+
+
+def split_tail() -> int:
+    return int(load().lora_split_tail())
 
 
 def test_expire_waits(launches: int):

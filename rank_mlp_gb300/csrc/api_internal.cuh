@@ -89,8 +89,12 @@ lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* T, cons
 
 lora_status_t launch_rope(const RopeParams& p, cudaStream_t st);
 
-// Workspace bytes lora_linear_forward needs (its share of lora_linear_workspace_bytes,
-// which also covers the backward); 0 for invalid sizes.  Defined in lora_linear.cu.
+// lora_linear_forward for inference with the projection on whole tiles only (no
+// split tail), and the workspace bytes that needs (less than
+// lora_linear_workspace_bytes, which also covers the backward and the tail's regions;
+// 0 for invalid sizes).  Defined in lora_linear.cu.
+lora_status_t linear_forward_whole_tiles(int64_t M, int64_t in, int64_t out, int r, float s, const void* x,
+                                         lora_linear_t lin, void* y, void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t linear_forward_workspace_bytes(int64_t M, int64_t in, int64_t out, int r);
 // Device address of lora_linear_forward_noalloc's fixed scratch on the current device
 // (its first 256 bytes are that call's status word), or NULL on a CUDA error.

@@ -33,6 +33,130 @@ struct PairCfg {
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
 
+// The 32-column accumulator chunks (bit k: columns 32k .. 32k + 31) that epilogue_tile
+// reads for the warp with share `part` of `nparts`: the warp's own columns for the
+// plain, derivative and partial epilogues; matching gate and up halves for the
+// activation epilogue; both chunks of each rotation pair it owns for RoPE.
+template <int BN>
+__device__ __forceinline__ unsigned epilogue_chunks(const TcParams& p, int epi, int part, int nparts) {
+  constexpr int kChunks = BN / 32;
+  unsigned m = 0;
+  if (epi == EPI_ACT_FWD) {
+    const int per = kChunks / 2 / nparts;
+    for (int j = 0; j < per; ++j) m |= (1u << (part * per + j)) | (1u << (kChunks / 2 + part * per + j));
+  } else if (epi == EPI_ROPE) {
+    const int half = p.rope_half, cph = half / 32;
+    for (int t = part; t < BN / 64; t += nparts) {
+      const int col = (t / cph) * 2 * half + (t % cph) * 32;
+      m |= (1u << (col / 32)) | (1u << ((col + half) / 32));
+    }
+  } else {
+    const int per = kChunks / nparts;
+    for (int j = 0; j < per; ++j) m |= 1u << (part * per + j);
+  }
+  return m;
+}
+
+// A split-tail piece's epilogue step, for one epilogue warp: its TMEM lane quarter
+// (rows `row` of the CTA's 128) and the column chunks its epilogue reads
+// (epilogue_chunks).  The warp stores the piece's partial sums for those rows and
+// columns, then counts its arrival on the word of (tile, CTA, warp).  Every piece's
+// warp with the same role covers the same rows and columns, so each warp's word counts
+// its own share of the tile, and a warp that finishes the tile has fixed up everything
+// its epilogue then reads.  The last arrival sums the pieces' partials in piece order
+// (its own from TMEM, bit-identical to what it stored), writes the total back to TMEM
+// and returns true: the caller then runs the epilogue on it.  Earlier arrivals return
+// false.
+//
+// Partial slots: piece s of tail tile t uses slot t * sk_splits + s, which holds
+// [2 CTAs][BN/32 column chunks][128 rows][32] f32.  Arrival words hold
+// (sk_epoch << 8) + arrivals: a word from another launch counts as zero arrivals, and
+// the last arrival resets it, so the same launch replayed (a CUDA graph) counts again
+// from zero.
+template <int BN>
+__device__ __forceinline__ bool sk_piece_arrive(const TcParams& p, const GroupDesc& G, const Unit& U, uint32_t tacc,
+                                                int cta, int row, int part, int nparts, int widx) {
+  const int lane = threadIdx.x & 31;
+  const unsigned mask = epilogue_chunks<BN>(p, G.epi, part, nparts);
+  auto chunk = [&](long long slot, int c) -> float* {
+    return p.sk_part + (((slot * 2 + cta) * (BN / 32) + c / 32) * kBM + row) * 32;
+  };
+  const long long slot0 = static_cast<long long>(U.sk_tile) * U.npieces;
+  // this piece's partial sums
+  const long long mine = slot0 + U.piece;
+#pragma unroll 1
+  for (int ch = 0; ch < BN / 32; ++ch) {
+    if (!((mask >> ch) & 1u)) continue;
+    const int c = ch * 32;
+    uint32_t v[32];
+    __syncwarp();
+    tmem_ld32(tacc + c, v);
+    tmem_ld_wait();
+    float* dst = chunk(mine, c);
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) st_global_v8(dst + j, v + j);
+  }
+  __threadfence();
+  __syncwarp();
+  // count the arrival
+  int last = 0;
+  if (lane == 0) {
+    unsigned long long* w = p.sk_flags + (static_cast<long long>(U.sk_tile) * 2 + cta) * kSkWarps + widx;
+    const unsigned long long tag = p.sk_epoch << 8;
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(w);
+    for (int n = 0; n < 64; ++n) {     // each failed exchange means another piece arrived
+      const unsigned long long base = (cur & ~0xffull) == tag ? cur : tag;
+      const unsigned long long seen = atomicCAS(w, cur, base + 1);
+      if (seen == cur) {
+        last = static_cast<int>((base + 1) & 0xffull) == U.npieces;
+        break;
+      }
+      cur = seen;
+    }
+    if (last) atomicExch(w, tag);
+    __threadfence();
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return false;
+  __threadfence();
+  // the tile's total, in piece order, 8 columns at a time
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 8) {
+    if (!((mask >> (c / 32)) & 1u)) continue;
+    uint32_t v[8];
+    __syncwarp();
+    tmem_ld8(tacc + c, v);
+    tmem_ld_wait();
+    float acc[8];
+#pragma unroll 1
+    for (int j = 0; j < U.npieces; ++j) {
+      float x[8];
+      if (j == U.piece) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[e]);
+      } else {
+        const float* src = chunk(slot0 + j, c & ~31) + (c & 31);
+        const uint4 w0 = ld_global_cg_v4(src), w1 = ld_global_cg_v4(src + 4);
+        x[0] = __uint_as_float(w0.x);
+        x[1] = __uint_as_float(w0.y);
+        x[2] = __uint_as_float(w0.z);
+        x[3] = __uint_as_float(w0.w);
+        x[4] = __uint_as_float(w1.x);
+        x[5] = __uint_as_float(w1.y);
+        x[6] = __uint_as_float(w1.z);
+        x[7] = __uint_as_float(w1.w);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = j == 0 ? x[e] : acc[e] + x[e];
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = __float_as_uint(acc[e]);
+    tmem_st8(tacc + c, v);
+  }
+  tmem_st_wait();
+  return true;
+}
+
 // EPIW = 4 or 8 epilogue warps: with 8, two warps share each TMEM lane quarter and
 // take half of the tile's columns each (more loads in flight for epilogues that read
 // saved tensors); with 4, fewer warps compete for issue slots with the producer and
@@ -98,8 +222,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
       for (int s = 0; s < STAGES; ++s) armed[s] = -1;
       bool ok = true;
       bool first_stage = true;
-      for (int u = pair; u < p.total_units && ok; u += npairs) {
-        const Unit U = decode_unit(p, u);
+      WorkIter it(p, pair, npairs);
+      Unit U;
+      while (ok && it.next(p, U)) {
         const GroupDesc& G = p.grp[U.g];
         // walk the unit's k-range segment by segment; a segment's fields live in registers
         const int nseg = G.nseg;
@@ -155,8 +280,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = pair; u < p.total_units && ok; u += npairs) {
-        const Unit U = decode_unit(p, u);
+      WorkIter it(p, pair, npairs);
+      Unit U;
+      while (ok && it.next(p, U)) {
         const GroupDesc& G = p.grp[U.g];
         if (!wait_phase(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p)) { ok = false; break; }
         tc_fence_after_sync();
@@ -206,14 +332,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
     const uint32_t tempty_even[2] = {mapa_shared(tempty_bar(0), 0), mapa_shared(tempty_bar(1), 0)};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = pair; u < p.total_units; u += npairs) {
-      const Unit U = decode_unit(p, u);
+    WorkIter it(p, pair, npairs);
+    Unit U;
+    while (it.next(p, U)) {
       const GroupDesc& G = p.grp[U.g];
       const bool ready = wait_phase(tfull_bar(acc), acc_phase, abort_flag, p);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after_sync();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      epilogue_tile<BN>(p, G, U, tacc, U.tm * (2 * kBM) + static_cast<int>(rank) * kBM + row_in_tile, part, EPIW / 4);
+      // a split-tail piece: the last piece of its tile to arrive finishes the tile
+      const bool finish = U.npieces == 1 ||
+                          sk_piece_arrive<BN>(p, G, U, tacc, static_cast<int>(rank), row_in_tile, part, EPIW / 4,
+                                              warp - 2);
+      if (finish)
+        epilogue_tile<BN>(p, G, U, tacc, U.tm * (2 * kBM) + static_cast<int>(rank) * kBM + row_in_tile, part,
+                          EPIW / 4);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_even[acc]);

@@ -86,7 +86,31 @@ struct TcParams {
   // nothing it reads, so it starts at once (on SMs the previous kernel has freed) and
   // waits for that kernel only before it exits, keeping the stream's completion order
   int pdl_late;
+  // Split tail (CTA-pair kernel).  Units [0, sk_dp_units) are whole tiles dealt
+  // round-robin to the pairs.  The sk_tail tiles after them, which would fill only part
+  // of a last wave, are each cut into sk_splits equal k-ranges (of sk_kb k-blocks in
+  // all), and these pieces follow, k-range major (every tail tile's first piece, then
+  // every second piece, ...), so that pairs working at the same time read the same
+  // k-slices of the operands.  Every piece stores its f32 partial sums in sk_part; the
+  // last piece of a tile to arrive (an arrival word in sk_flags per tile, CTA and
+  // epilogue warp, tagged with sk_epoch) adds the others to its accumulator in piece
+  // order and runs the epilogue.  No CTA waits for another.  sk_splits == 0: every unit
+  // is a whole tile.
+  int sk_dp_units;
+  int sk_tail;
+  int sk_splits;
+  int sk_kb;
+  float* sk_part;                 // [sk_tail * sk_splits pieces][2 CTAs][BN/32][128 rows][32] f32
+  unsigned long long* sk_flags;   // [sk_tail][2 CTAs][kSkWarps]
+  unsigned long long sk_epoch;    // below 2^56
+  int sk_cap_pieces;              // pieces / tail tiles the regions are sized for (host)
+  int sk_cap_tiles;
 };
+
+// Arrival words per tile and CTA (one per epilogue warp, at most 8), and the most
+// pieces a tail tile is cut into.
+constexpr int kSkWarps = 8;
+constexpr int kSkMaxSplits = 4;
 
 template <int BN, int STAGES>
 struct TcCfg {
@@ -102,6 +126,8 @@ struct TcCfg {
 
 struct Unit {
   int g, tm, tn, split, kb0, kb1;
+  int piece, npieces;   // split tail: piece `piece` of the `npieces` computing this tile
+  int sk_tile;          // split tail: the tile's index in the tail
 };
 
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
@@ -121,6 +147,9 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   U.tm = rem / nb;
   U.tn = b * band + rem % nb;
   U.split = split;
+  U.piece = 0;
+  U.npieces = 1;
+  U.sk_tile = 0;
   if (G.per_plane) {
     U.kb0 = 0;
     U.kb1 = G.kb_total;
@@ -130,6 +159,31 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, int u) {
   }
   return U;
 }
+
+// The units of one CTA (or CTA pair) `q` of `nq`, round-robin: whole tiles, then the
+// split tail's pieces.  Every role of the CTA walks the same sequence.
+struct WorkIter {
+  int u, nq, end;
+  __device__ __forceinline__ WorkIter(const TcParams& p, int q, int nq_)
+      : u(q), nq(nq_), end(p.sk_splits > 0 ? p.sk_dp_units + p.sk_tail * p.sk_splits : p.total_units) {}
+  __device__ __forceinline__ bool next(const TcParams& p, Unit& U) {
+    if (u >= end) return false;
+    if (p.sk_splits == 0 || u < p.sk_dp_units) {
+      U = decode_unit(p, u);
+    } else {
+      const int j = u - p.sk_dp_units;
+      const int s = j / p.sk_tail, t = j - s * p.sk_tail;
+      U = decode_unit(p, p.sk_dp_units + t);
+      U.kb0 = static_cast<int>(static_cast<long long>(p.sk_kb) * s / p.sk_splits);
+      U.kb1 = static_cast<int>(static_cast<long long>(p.sk_kb) * (s + 1) / p.sk_splits);
+      U.piece = s;
+      U.npieces = p.sk_splits;
+      U.sk_tile = t;
+    }
+    u += nq;
+    return true;
+  }
+};
 
 // Bounded wait: true when the phase completed, false on abort (flag set by another
 // role, or this wait timed out, which sets the flag and the status word).  The limit

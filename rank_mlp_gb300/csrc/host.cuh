@@ -171,6 +171,39 @@ struct Carve {
 
 constexpr size_t kWsHeader = 256;
 
+// Split tail of the pair GEMMs (see TcParams): the partial-sum and arrival-word
+// regions are carved from the caller's workspace, sized for the call's largest pair
+// GEMM and at most kSkMaxPieces pieces (256 KB of partial sums each), whatever the
+// device.  A tail of fewer than 128 tiles is cut into 2 to kSkMaxSplits k-ranges when
+// the model in plan_pairs (lora_api.cu) expects the launch to gain at least
+// kSkMinGain, and a tile has at least kSkMinKb k-blocks.
+constexpr int kSkMaxPieces = 256;
+constexpr int kSkMaxTail = 128;
+constexpr int kSkMinKb = 8;
+constexpr double kSkMinGain = 0.02;
+
+// Tiles of a pair-kernel output [M x N]: 256 x 256, or 256 x (128 + 128) for the
+// gate/up interleave (N = i, split_n).
+inline int64_t pair_tiles(int64_t M, int64_t N, bool split_n = false) {
+  return ceil_div(M, 2 * kBM) * ceil_div(N, split_n ? 128 : 256);
+}
+
+// The split-tail regions of one call: partial slots [pieces][2][8][128][32] f32 and
+// arrival words [tail tiles][2][kSkWarps].
+struct SkRegion {
+  float* part = nullptr;
+  unsigned long long* flags = nullptr;
+  int pieces = 0, tiles = 0;
+};
+inline SkRegion carve_sk(Carve& c, int64_t max_tiles) {
+  SkRegion r;
+  r.tiles = static_cast<int>(max_tiles < kSkMaxTail ? max_tiles : kSkMaxTail);
+  r.pieces = static_cast<int>(kSkMaxSplits * r.tiles < kSkMaxPieces ? kSkMaxSplits * r.tiles : kSkMaxPieces);
+  r.part = c.take_n<float>(static_cast<int64_t>(r.pieces) * 2 * 8 * kBM * 32);
+  r.flags = c.take_n<unsigned long long>(static_cast<int64_t>(r.tiles) * 2 * kSkWarps);
+  return r;
+}
+
 // Builds the TcParams of one GEMM launch.
 struct GemmPlan {
   TcParams p;
@@ -183,6 +216,13 @@ struct GemmPlan {
     std::memset(static_cast<void*>(&p), 0, sizeof(p));
     p.band = 8;
     p.timeout_ns = kTimeoutNs;
+  }
+  // Lets the launch split its tail (pair kernels) with this call's regions.
+  void split_tail(const SkRegion& r) {
+    p.sk_part = r.part;
+    p.sk_flags = r.flags;
+    p.sk_cap_pieces = r.pieces;
+    p.sk_cap_tiles = r.tiles;
   }
 
   int add_map(const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t bi, uint32_t bo) {
@@ -237,7 +277,9 @@ struct GemmPlan {
     S.a = a;
     S.b0 = b0;
     S.b1 = b1;
-    S.kblocks = static_cast<int>(ceil_div(K, kBK));
+    // k-blocks wholly past kvalid hold only zero padding: they are not walked, so every
+    // k-block of a segment issues at least one MMA
+    S.kblocks = static_cast<int>(ceil_div(kvalid < K ? kvalid : K, kBK));
     S.kvalid = static_cast<int>(kvalid);
     G.kb_total += S.kblocks;
   }
@@ -249,6 +291,8 @@ struct GemmPlan {
       u += p.grp[g].tiles_m * p.grp[g].tiles_n * p.grp[g].splits;
     }
     p.total_units = u;
+    p.sk_dp_units = u;
+    p.sk_splits = 0;
     int maxtn = 1;
     for (int g = 0; g < p.ngroups; ++g) maxtn = p.grp[g].tiles_n > maxtn ? p.grp[g].tiles_n : maxtn;
     p.band = maxtn < 16 ? maxtn : 16;

@@ -3,7 +3,10 @@
 // operations share (adapter packing, rank-r projections, reductions over tokens), and
 // the status, trace and RoPE-table entry points.  The operations' entry points are in
 // lora_linear.cu, lora_mlp.cu and lora_qkvo.cu; include/lora_gb300.h is the contract.
+#include <unistd.h>
+
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <mutex>
 #include <vector>
@@ -110,6 +113,72 @@ static int take_expiry() {
   return n > 0 ? 1 : 0;
 }
 
+// Split-tail mode (lora_set_split_tail): 0 automatic, 1 never, S = 2..kSkMaxSplits
+// every tail in S pieces whenever the launch allows it.  The environment variable
+// LORA_SPLIT_TAIL sets the initial mode.
+static std::atomic<int> g_split_tail{[] {
+  const char* e = std::getenv("LORA_SPLIT_TAIL");
+  return (e != nullptr && e[0] >= '1' && e[0] <= '0' + kSkMaxSplits && e[1] == 0) ? e[0] - '0' : 0;
+}()};
+
+// Launch tags of the split tail's arrival words: distinct for every launch of the
+// process, and started from a per-process value so that words left by another process
+// in reused memory do not match (56 bits; the low 8 bits of a word count arrivals).
+static unsigned long long next_sk_epoch() {
+  static std::atomic<unsigned long long> counter{[] {
+    unsigned long long z = static_cast<unsigned long long>(
+                               std::chrono::steady_clock::now().time_since_epoch().count()) ^
+                           (static_cast<unsigned long long>(getpid()) << 32);
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;      // splitmix64 finaliser
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    return z ^ (z >> 31);
+  }()};
+  return counter.fetch_add(1) & ((1ull << 56) - 1);
+}
+
+// Chooses the pair launch's schedule and returns the pairs its grid needs.  With T
+// tiles on P pairs, round-robin whole tiles take ceil(T / P) tile-times.  The tail
+// (T mod P tiles after the full waves, or all T when T < P) may instead be cut into S
+// k-ranges: the tail then takes ceil(tail * S / P) / S tile-times, plus the partial
+// sums' cost for the piece that finishes a tile, measured at about the time of
+// 8 + 24 (S - 1) k-blocks of MMAs (its own partial sums stored, each other piece's read
+// back eight columns at a time).  In automatic mode the S in 2..kSkMaxSplits with the
+// smallest estimate is used when it saves at least kSkMinGain of the launch; a mode
+// S >= 2 uses S pieces whatever the estimate.
+static int plan_pairs(TcParams& p, int pairs) {
+  const int T = p.total_units;
+  p.sk_dp_units = T;
+  p.sk_splits = 0;
+  const int round_robin = T < pairs ? T : pairs;
+  const int mode = g_split_tail.load(std::memory_order_relaxed);
+  if (p.sk_part == nullptr || p.sk_flags == nullptr || mode == 1) return round_robin;
+  const int kb = p.grp[0].kb_total;
+  for (int g = 0; g < p.ngroups; ++g)
+    if (p.grp[g].splits != 1 || p.grp[g].per_plane || p.grp[g].kb_total != kb) return round_robin;
+  if (kb < kSkMinKb) return round_robin;
+  const int W = T / pairs;
+  const int tail = W >= 1 ? T - W * pairs : T;
+  if (tail == 0 || tail > p.sk_cap_tiles) return round_robin;
+  int best_s = 0;
+  double best = 1e30;
+  for (int S = 2; S <= kSkMaxSplits; ++S) {
+    if (tail * S > p.sk_cap_pieces || kb < 2 * S) break;
+    const double est = static_cast<double>((tail * S + pairs - 1) / pairs) / S + (8.0 + 24.0 * (S - 1)) / kb;
+    if ((mode == 0 && est < best - 1e-12) || mode == S) {
+      best = est;
+      best_s = S;
+    }
+  }
+  if (best_s == 0 || (mode == 0 && (1.0 - best) / (W + 1) < kSkMinGain)) return round_robin;
+  p.sk_dp_units = T - tail;
+  p.sk_tail = tail;
+  p.sk_splits = best_s;
+  p.sk_kb = kb;
+  p.sk_epoch = next_sk_epoch();
+  const int units = T - tail + tail * best_s;
+  return units < pairs ? units : pairs;
+}
+
 lora_status_t launch_gemm(int variant, const TcParams& plan, int kind, cudaStream_t st) {
   if (plan.total_units <= 0) return LORA_OK;
   if (variant == VP_KK) {
@@ -122,8 +191,7 @@ lora_status_t launch_gemm(int variant, const TcParams& plan, int kind, cudaStrea
   p.inject_stall = take_expiry();
   int grid;
   if (variant_pair(variant)) {
-    const int pairs = num_sms() / 2;
-    grid = 2 * (p.total_units < pairs ? p.total_units : pairs);
+    grid = 2 * plan_pairs(p, num_sms() / 2);
   } else {
     grid = p.total_units < num_sms() ? p.total_units : num_sms();
   }
@@ -431,6 +499,14 @@ extern "C" lora_status_t lora_set_wait_timeout(uint64_t ns) {
 }
 
 extern "C" uint64_t lora_wait_timeout(void) { return g_timeout_ns.load(); }
+
+extern "C" lora_status_t lora_set_split_tail(int mode) {
+  if (mode < 0 || mode > kSkMaxSplits) return LORA_ERR_INVALID_ARG;
+  g_split_tail.store(mode);
+  return LORA_OK;
+}
+
+extern "C" int lora_split_tail(void) { return g_split_tail.load(); }
 
 extern "C" lora_status_t lora_test_expire_waits(int launches) {
   if (launches < 0 || launches > 64) return LORA_ERR_INVALID_ARG;

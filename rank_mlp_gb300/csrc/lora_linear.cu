@@ -13,6 +13,7 @@ namespace {
 
 struct LinearLayout {
   int kf;
+  size_t ws_fwd_base;   // the forward without the split-tail regions (last in its layout)
   size_t ws_fwd, ws_bwd, saved;
 };
 
@@ -27,6 +28,8 @@ LinearLayout linear_layout(int64_t M, int64_t in, int64_t out, int r) {
     c.take_n<bf16>(out * kf);   // BF
     c.take_n<float>(rank_projection_part(M, kf, ceil_div(in, kBK)));
     c.take_n<bf16>(M * kf);     // T when there is no saved blob
+    L.ws_fwd_base = c.off;
+    carve_sk(c, pair_tiles(M, out));
     L.ws_fwd = c.off;
   }
   {
@@ -37,6 +40,7 @@ LinearLayout linear_layout(int64_t M, int64_t in, int64_t out, int r) {
     c.take_n<bf16>(M * kf);     // U
     c.take_n<float>(rank_projection_part(M, kf, ceil_div(out, kBK)));
     c.take_n<float>(token_grad_part(M, kf, &out, 1) + token_grad_part(M, kf, &in, 1));   // dB, dA slabs
+    carve_sk(c, pair_tiles(M, in));
     L.ws_bwd = c.off;
   }
   {
@@ -62,13 +66,15 @@ extern "C" size_t lora_linear_workspace_bytes(int64_t M, int64_t in, int64_t out
 
 size_t lgb::linear_forward_workspace_bytes(int64_t M, int64_t in, int64_t out, int r) {
   if (M < 0 || in <= 0 || out <= 0 || r < 1) return 0;
-  return linear_layout(M, in, out, r).ws_fwd;
+  return linear_layout(M, in, out, r).ws_fwd_base;
 }
 
-extern "C" lora_status_t lora_linear_forward(int64_t M, int64_t in, int64_t out, int r, float s, const void* x,
-                                             lora_linear_t lin, void* y, void* saved, void* ws, size_t ws_bytes,
-                                             cudaStream_t stream) {
-  NvtxRange nvtx_range("lora_linear_forward");
+// The forward; with split_tail false the projection runs whole tiles only and ws needs
+// only the part of the layout before the split-tail regions
+// (linear_forward_workspace_bytes).
+static lora_status_t linear_forward_impl(int64_t M, int64_t in, int64_t out, int r, float s, const void* x,
+                                         lora_linear_t lin, void* y, void* saved, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream, bool split_tail) {
   lora_status_t st = check_common(M, r, s);
   check_size(in, st);
   check_size(out, st);
@@ -82,7 +88,7 @@ extern "C" lora_status_t lora_linear_forward(int64_t M, int64_t in, int64_t out,
       !aligned(lin.B, 2) || !aligned(ws, 256) || (saved && !aligned(saved, 256)))
     return LORA_ERR_ALIGNMENT;
   const LinearLayout L = linear_layout(M, in, out, r);
-  if (ws_bytes < L.ws_fwd) return LORA_ERR_WORKSPACE;
+  if (ws_bytes < (split_tail ? L.ws_fwd : L.ws_fwd_base)) return LORA_ERR_WORKSPACE;
   if (M == 0) return LORA_OK;
   const int kf = L.kf;
   Carve c(ws);
@@ -92,6 +98,7 @@ extern "C" lora_status_t lora_linear_forward(int64_t M, int64_t in, int64_t out,
   float* part = c.take_n<float>(rank_projection_part(M, kf, ceil_div(in, kBK)));
   bf16* T = c.take_n<bf16>(M * kf);
   if (saved) T = static_cast<bf16*>(saved);
+  const SkRegion sk = split_tail ? carve_sk(c, pair_tiles(M, out)) : SkRegion();
 
   PackParams pk;
   std::memset(static_cast<void*>(&pk), 0, sizeof(pk));
@@ -110,8 +117,22 @@ extern "C" lora_status_t lora_linear_forward(int64_t M, int64_t in, int64_t out,
   G.ldo = out;
   g.p.status = status;
   g.finish();
+  g.split_tail(sk);
   if (!g.ok) return LORA_ERR_CUDA;
   return launch_gemm(kBigKK, g.p, LORA_KIND_PROJ, stream);
+}
+
+extern "C" lora_status_t lora_linear_forward(int64_t M, int64_t in, int64_t out, int r, float s, const void* x,
+                                             lora_linear_t lin, void* y, void* saved, void* ws, size_t ws_bytes,
+                                             cudaStream_t stream) {
+  NvtxRange nvtx_range("lora_linear_forward");
+  return linear_forward_impl(M, in, out, r, s, x, lin, y, saved, ws, ws_bytes, stream, true);
+}
+
+lora_status_t lgb::linear_forward_whole_tiles(int64_t M, int64_t in, int64_t out, int r, float s, const void* x,
+                                              lora_linear_t lin, void* y, void* ws, size_t ws_bytes,
+                                              cudaStream_t stream) {
+  return linear_forward_impl(M, in, out, r, s, x, lin, y, nullptr, ws, ws_bytes, stream, false);
 }
 
 extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out, int r, float s, const void* x,
@@ -149,6 +170,7 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   float* part = c.take_n<float>(rank_projection_part(M, kf, ceil_div(out, kBK)));
   Deferred dr;
   defer_init(dr, c.take_n<float>(token_grad_part(M, kf, &out, 1) + token_grad_part(M, kf, &in, 1)));
+  const SkRegion sk = carve_sk(c, pair_tiles(M, in));
   const bf16* T = static_cast<const bf16*>(saved);
 
   PackParams pk;
@@ -168,6 +190,7 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   G.ldo = in;
   g.p.status = status;
   g.finish();
+  g.split_tail(sk);
   if (!g.ok) return LORA_ERR_CUDA;
   LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
 

@@ -28,6 +28,12 @@ static int64_t mlp_bwd_slabs(int64_t M, int64_t h, int64_t i, int kfd, int kfg, 
          token_grad_part(M, kfg, f2, 2, n_ex) + token_grad_part(M, kfg, &h, 1, n_ex);
 }
 
+// Largest pair-GEMM tile counts of the forward (gate/up, down) and backward (act', dx).
+static int64_t mlp_fwd_tiles(int64_t M, int64_t h, int64_t i) {
+  return imax(pair_tiles(M, i, true), pair_tiles(M, h));
+}
+static int64_t mlp_bwd_tiles(int64_t M, int64_t h, int64_t i) { return imax(pair_tiles(M, i), pair_tiles(M, h)); }
+
 // n_ex > 0: workspace of the per-example backward (one reduction slab per example).
 MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r, int64_t n_ex = 0) {
   MlpLayout L;
@@ -48,6 +54,7 @@ MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r, int64_t n_ex = 0) {
     c.take_n<bf16>(M * i);       // h, T_gu, T_d when there is no saved blob
     c.take_n<bf16>(M * kfg);
     c.take_n<bf16>(M * kfd);
+    carve_sk(c, mlp_fwd_tiles(M, h, i));
     L.ws_fwd = c.off;
   }
   {
@@ -64,6 +71,7 @@ MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r, int64_t n_ex = 0) {
     c.take_n<bf16>(M * kfg);     // V
     c.take_n<float>(mlp_bwd_rank_part(M, h, i, kfd, kfg));
     c.take_n<float>(mlp_bwd_slabs(M, h, i, kfd, kfg, n_ex));
+    carve_sk(c, mlp_bwd_tiles(M, h, i));
     L.ws_bwd = c.off;
   }
   {
@@ -129,6 +137,7 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
   bf16* hbuf = c.take_n<bf16>(M * i);
   bf16* tgu = c.take_n<bf16>(M * kfg);
   bf16* td = c.take_n<bf16>(M * kfd);
+  const SkRegion sk = carve_sk(c, mlp_fwd_tiles(M, h, i));
   bf16* gbuf = nullptr;
   bf16* ubuf = nullptr;
   if (saved) {
@@ -172,6 +181,7 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
     g.p.act = static_cast<int>(act);
     g.p.status = status;
     g.finish();
+    g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKK, g.p, LORA_KIND_GATE_UP, stream));
   }
@@ -189,6 +199,7 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
   G.ldo = h;
   g.p.status = status;
   g.finish();
+  g.split_tail(sk);
   if (!g.ok) return LORA_ERR_CUDA;
   return launch_gemm(kBigKK, g.p, LORA_KIND_PROJ, stream);
 }
@@ -247,6 +258,7 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   float* part = c.take_n<float>(mlp_bwd_rank_part(M, h, i, kfd, kfg));
   Deferred dr;
   defer_init(dr, c.take_n<float>(mlp_bwd_slabs(M, h, i, kfd, kfg, n_ex)));
+  const SkRegion sk = carve_sk(c, mlp_bwd_tiles(M, h, i));
 
   PackParams pk;
   std::memset(static_cast<void*>(&pk), 0, sizeof(pk));
@@ -280,6 +292,7 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
     g.p.act = static_cast<int>(act);
     g.p.status = status;
     g.finish();
+    g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_ACT_BWD, stream));
   }
@@ -307,6 +320,7 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
     G.ldo = h;
     g.p.status = status;
     g.finish();
+    g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
   }

@@ -26,6 +26,13 @@ static int64_t qkvo_bwd_slabs(int64_t M, int64_t h, int64_t nq, int64_t nkv, int
          token_grad_part(M, kfq, &h, 1);
 }
 
+// Largest pair-GEMM tile counts of the forward (q/k/v in one launch, o) and the
+// backward (d o_in, dx).
+static int64_t qkvo_fwd_tiles(int64_t M, int64_t h, int64_t nq, int64_t nkv) {
+  return imax(pair_tiles(M, nq) + 2 * pair_tiles(M, nkv), pair_tiles(M, h));
+}
+static int64_t qkvo_bwd_tiles(int64_t M, int64_t h, int64_t nq) { return imax(pair_tiles(M, nq), pair_tiles(M, h)); }
+
 QkvoLayout qkvo_layout(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r) {
   QkvoLayout L;
   L.kfq = fold_width(3, r);
@@ -45,6 +52,7 @@ QkvoLayout qkvo_layout(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r) {
     c.take_n<float>(p > p2 ? p : p2);
     c.take_n<bf16>(M * kfq);
     c.take_n<bf16>(M * kfo);
+    carve_sk(c, qkvo_fwd_tiles(M, h, nq, nkv));
     L.ws_fwd = c.off;
   }
   {
@@ -62,6 +70,7 @@ QkvoLayout qkvo_layout(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r) {
     c.take_n<bf16>(M * nkv);
     c.take_n<float>(qkvo_bwd_rank_part(M, h, nq, nkv, kfq, kfo));
     c.take_n<float>(qkvo_bwd_slabs(M, h, nq, nkv, kfq, kfo));
+    carve_sk(c, qkvo_bwd_tiles(M, h, nq));
     L.ws_bwd = c.off;
   }
   {
@@ -142,6 +151,7 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
   float* part = c.take_n<float>(pe > pe2 ? pe : pe2);
   bf16* tqkv = c.take_n<bf16>(M * kfq);
   bf16* to = c.take_n<bf16>(M * kfo);
+  const SkRegion sk = carve_sk(c, qkvo_fwd_tiles(M, h, n_q, n_kv));
   if (saved) {
     tqkv = static_cast<bf16*>(saved);
     to = reinterpret_cast<bf16*>(static_cast<uint8_t*>(saved) + L.off_to);
@@ -192,6 +202,7 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
     }
     g.p.status = status;
     g.finish();
+    g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKK, g.p, LORA_KIND_PROJ, stream));
   }
@@ -206,6 +217,7 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
     G.ldo = h;
     g.p.status = status;
     g.finish();
+    g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKK, g.p, LORA_KIND_PROJ, stream));
   }
@@ -272,6 +284,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
   float* part = c.take_n<float>(qkvo_bwd_rank_part(M, h, n_q, n_kv, kfq, kfo));
   Deferred dr;
   defer_init(dr, c.take_n<float>(qkvo_bwd_slabs(M, h, n_q, n_kv, kfq, kfo)));
+  const SkRegion sk = carve_sk(c, qkvo_bwd_tiles(M, h, n_q));
 
   PackParams pk;
   std::memset(static_cast<void*>(&pk), 0, sizeof(pk));
@@ -301,6 +314,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     G.ldo = n_q;
     g.p.status = status;
     g.finish();
+    g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
     // dB_o = s dy_o^T T_o and dA_o = s U_o^T o_in read nothing the d o_in GEMM writes
@@ -345,6 +359,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     G.ldo = h;
     g.p.status = status;
     g.finish();
+    g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
     const GradJob j4[3] = {{x, h, 0, d_q.dA, 1}, {x, h, r, d_k.dA, 1}, {x, h, 2 * r, d_v.dA, 1}};

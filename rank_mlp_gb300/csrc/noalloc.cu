@@ -99,5 +99,5 @@ extern "C" lora_status_t lora_linear_forward_noalloc(int64_t M, int64_t in, int6
   if (scratch == nullptr) return LORA_ERR_CUDA;
   // Everything the forward reads from the scratch it writes first, apart from the
   // status word, which keeps an unpolled error of an earlier call.
-  return lora_linear_forward(M, in, out, r, s, x, lin, y, nullptr, scratch, kNoAllocScratchBytes, stream);
+  return lgb::linear_forward_whole_tiles(M, in, out, r, s, x, lin, y, scratch, kNoAllocScratchBytes, stream);
 }

@@ -200,3 +200,12 @@ def test_expiry_hook_range(L):
     assert L.lora_test_expire_waits(-1) == 1
     assert L.lora_test_expire_waits(65) == 1
     assert L.lora_test_expire_waits(0) == 0
+
+
+def test_split_tail_mode_range(L):
+    assert L.lora_split_tail() == 0
+    assert L.lora_set_split_tail(-1) == 1
+    assert L.lora_set_split_tail(5) == 1
+    for m in (1, 2, 3, 4, 0):
+        assert L.lora_set_split_tail(m) == 0
+        assert L.lora_split_tail() == m
