@@ -19,7 +19,16 @@ namespace lgb {
 // Threads of a pair-kernel CTA: producer warp, MMA warp and EPIW epilogue warps.
 constexpr int pair_threads(int epiw) { return 64 + 32 * epiw; }
 
-template <int STAGES>
+// Staged epilogue (the activation-derivative GEMM at short K): each epilogue warp owns
+// a ring of kEpiSlots slots in shared memory; a slot holds one chunk (the warp's 32 rows
+// x COLS columns) of g and of u, loaded by TMA, and then the chunk's dg and du, written
+// in place and stored by TMA.
+constexpr int kEpiSlots = 4;
+constexpr int epi_tensor_bytes(int cols) { return 32 * cols * 2; }
+constexpr int epi_slot_bytes(int cols) { return 2 * epi_tensor_bytes(cols); }
+
+// STAGED = 0 (plain epilogues) or the staged epilogue's chunk width in columns.
+template <int STAGES, int EPIW = 4, int STAGED = 0>
 struct PairCfg {
   static constexpr int BN = 256;                       // accumulator columns per tile
   static constexpr int kBLocal = BN / 2;               // B rows held by each CTA
@@ -28,9 +37,12 @@ struct PairCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTxBytes = 2 * kStageBytes;     // both CTAs, counted on the even CTA
   static constexpr int kTmemCols = 512;
-  static constexpr int kBarBytes = 8 * (2 * STAGES + 5) + 16;
-  static constexpr int kSmemBytes = STAGES * kStageBytes + kBarBytes + 1024;
+  static constexpr int kEpiBytes = STAGED ? EPIW * kEpiSlots * epi_slot_bytes(STAGED) : 0;
+  static constexpr int kNumBars = 2 * STAGES + 5 + (STAGED ? EPIW * kEpiSlots : 0);
+  static constexpr int kBarBytes = 8 * kNumBars + 16;
+  static constexpr int kSmemBytes = STAGES * kStageBytes + kEpiBytes + kBarBytes + 1024;
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 // The 32-column accumulator chunks (bit k: columns 32k .. 32k + 31) that epilogue_tile
@@ -157,22 +169,174 @@ __device__ __forceinline__ bool sk_piece_arrive(const TcParams& p, const GroupDe
   return true;
 }
 
+// dg = dh u act'(g), du = dh act(g) for COLS columns of one row ("Model Patches and
+// Kernels", activation table: the derivative of the activation, recomputed from the
+// saved g): d the accumulator (dh), gw, uw the saved bf16 pairs; results as bf16 pairs.
+template <int ACT, int COLS>
+__device__ __forceinline__ void act_bwd_cols(const uint32_t (&d)[COLS], const uint32_t (&gw)[COLS / 2],
+                                             const uint32_t (&uw)[COLS / 2], uint32_t (&dg)[COLS / 2],
+                                             uint32_t (&du)[COLS / 2]) {
+#pragma unroll
+  for (int e = 0; e < COLS / 2; ++e) {
+    float a0, ap0, a1, ap1;
+    const float g0 = bf16_lo(gw[e]), g1 = bf16_hi(gw[e]);
+    const float u0 = bf16_lo(uw[e]), u1 = bf16_hi(uw[e]);
+    act_fwd_bwd<ACT>(g0, a0, ap0);
+    act_fwd_bwd<ACT>(g1, a1, ap1);
+    const float d0 = __uint_as_float(d[2 * e]), d1 = __uint_as_float(d[2 * e + 1]);
+    dg[e] = pack_bf16x2(d0 * u0 * ap0, d1 * u1 * ap1);
+    du[e] = pack_bf16x2(d0 * a0, d1 * a1);
+  }
+}
+
+// The staged activation-derivative epilogue of one epilogue warp (its TMEM lane
+// quarter q = warp & 3, its share of the tile's columns), for all its units.  The
+// warp walks its chunks of 32 rows x COLS columns in order across tiles; lane 0 keeps
+// the TMA loads of g, u kEpiSlots - 1 chunks ahead (into the slot whose dg, du store
+// has finished reading it), so the next tile's first loads fly while the warp waits
+// for that tile's accumulator.  Each chunk: wait for its slot, read dh from TMEM,
+// compute, write dg, du over g, u, make them visible to TMA and store both.  The
+// accumulator is released as soon as the tile's last chunk has been read from TMEM.
+// Rows past M and columns past N are zero-filled by the loads and dropped by the
+// stores.  The chunk's 32-byte rows sit in the 32-byte swizzle.
+template <int STAGES, int EPIW, int COLS>
+__device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_smem, uint32_t epi_bar0,
+                                               uint32_t tfull0, const uint32_t (&tempty_even)[2], uint32_t tmem_base,
+                                               volatile int* abort_flag, uint32_t rank, int pair, int npairs,
+                                               int warp) {
+  static_assert(COLS == 16, "chunk width");
+  constexpr int BN = 256;
+  constexpr int kParts = EPIW / 4;
+  constexpr int kSpan = BN / kParts;                   // columns per warp
+  constexpr int kChunks = kSpan / COLS;                // chunks per warp per tile
+  constexpr int kTensorBytes = epi_tensor_bytes(COLS);
+  constexpr int kSlotBytes = epi_slot_bytes(COLS);
+  const int lane = threadIdx.x & 31;
+  const int q = warp & 3;
+  const int widx = warp - 2;
+  const int part = widx >> 2;
+  const uint32_t ring = epi_smem + static_cast<uint32_t>(widx) * (kEpiSlots * kSlotBytes);
+  auto slot = [&](uint32_t n) { return ring + (n % kEpiSlots) * kSlotBytes; };
+  auto full = [&](uint32_t n) { return epi_bar0 + 8u * (widx * kEpiSlots + n % kEpiSlots); };
+  // this lane's row inside a chunk box and its 16-byte halves (32-byte swizzle: half j
+  // of row r sits at j ^ bit 2 of r)
+  const uint32_t sw = (static_cast<uint32_t>(lane) >> 2) & 1u;
+  const uint32_t off0 = lane * 32u + (sw << 4);
+  const uint32_t off1 = lane * 32u + ((sw ^ 1u) << 4);
+
+  // the loading cursor: unit and chunk of the next load
+  WorkIter ahead(p, pair, npairs);
+  Unit UA;
+  bool more = ahead.next(p, UA);
+  int ca = 0;
+  uint32_t issued = 0, used = 0;
+  auto issue = [&]() {
+    if (lane == 0) {
+      const GroupDesc& GA = p.grp[UA.g];
+      const int row0 = UA.tm * (2 * kBM) + static_cast<int>(rank) * kBM + q * 32;
+      const int col = UA.tn * BN + part * kSpan + ca * COLS;
+      const uint32_t b = full(issued), dst = slot(issued);
+      mbar_arrive_expect_tx(b, kSlotBytes);
+      tma_load_2d(dst, &p.maps[GA.emap[0]], b, col, row0);
+      tma_load_2d(dst + kTensorBytes, &p.maps[GA.emap[1]], b, col, row0);
+    }
+    ++issued;
+    if (++ca == kChunks) {
+      ca = 0;
+      more = ahead.next(p, UA);
+    }
+  };
+  for (int k = 0; k < kEpiSlots - 1 && more; ++k) issue();
+
+  WorkIter it(p, pair, npairs);
+  Unit U;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  bool ok = true;
+  while (ok && it.next(p, U)) {
+    const GroupDesc& G = p.grp[U.g];
+    const bool ready = wait_phase(tfull0 + 8u * acc, acc_phase, abort_flag, p);
+    if (!__all_sync(0xffffffffu, ready)) { ok = false; break; }
+    tc_fence_after_sync();
+    const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+    const int row0 = U.tm * (2 * kBM) + static_cast<int>(rank) * kBM + q * 32;
+#pragma unroll 1
+    for (int c = 0; c < kChunks; ++c) {
+      const int col = part * kSpan + c * COLS;
+      uint32_t d[COLS];
+      __syncwarp();
+      tmem_ld16(tacc + col, d);
+      const bool landed = wait_phase(full(used), (used / kEpiSlots) & 1u, abort_flag, p);
+      tmem_ld_wait();
+      if (c == kChunks - 1) {        // the accumulator is no longer needed: hand it back
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_even[acc]);
+      }
+      if (!__all_sync(0xffffffffu, landed)) { ok = false; break; }
+      const uint32_t s0 = slot(used);
+      const uint4 g0 = ld_shared_v4(s0 + off0), g1 = ld_shared_v4(s0 + off1);
+      const uint4 u0 = ld_shared_v4(s0 + kTensorBytes + off0), u1 = ld_shared_v4(s0 + kTensorBytes + off1);
+      const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+      uint32_t dg[8], du[8];
+      act_chunk(p.act, [&](auto tag) { act_bwd_cols<decltype(tag)::value, COLS>(d, gw, uw, dg, du); });
+      st_shared_v4(s0 + off0, make_uint4(dg[0], dg[1], dg[2], dg[3]));
+      st_shared_v4(s0 + off1, make_uint4(dg[4], dg[5], dg[6], dg[7]));
+      st_shared_v4(s0 + kTensorBytes + off0, make_uint4(du[0], du[1], du[2], du[3]));
+      st_shared_v4(s0 + kTensorBytes + off1, make_uint4(du[4], du[5], du[6], du[7]));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int gcol = U.tn * BN + col;
+        tma_store_2d(&p.maps[G.emap[2]], s0, gcol, row0);
+        tma_store_2d(&p.maps[G.emap[3]], s0 + kTensorBytes, gcol, row0);
+        bulk_commit_group();
+      }
+      ++used;
+      if (more) {
+        // the next load goes into the slot of chunk used - 1, whose store must have
+        // finished reading it (all stores but the one just committed)
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        issue();
+      }
+    }
+    if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+  }
+  if (lane == 0) {
+    // loads still in flight (after an abort) land before shared memory is released;
+    // every store completes before the kernel ends
+    for (uint32_t n = used; n < issued; ++n) wait_phase_drain(full(n), (n / kEpiSlots) & 1u, p);
+    bulk_wait_group_all();
+  }
+  __syncwarp();
+}
+
 // EPIW = 4 or 8 epilogue warps: with 8, two warps share each TMEM lane quarter and
 // take half of the tile's columns each (more loads in flight for epilogues that read
 // saved tensors); with 4, fewer warps compete for issue slots with the producer and
 // MMA lanes (better for arithmetic-heavy epilogues).
-template <int STAGES, bool B_MN, int EPIW>
+//
+// ACTB selects the epilogues compiled in: 0 the plain, activation, RoPE and partial
+// epilogues (epilogue_tile); the activation-derivative GEMM (every group EPI_ACT_BWD)
+// has variants of its own: 1 reads g, u and writes dg, du one row per thread
+// (epilogue_act_bwd_rows); 16 moves them through the epilogue warps' shared-memory
+// rings in chunks of 16 columns (staged_act_bwd; whole tiles only).
+template <int STAGES, bool B_MN, int EPIW, int ACTB = 0>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
   static_assert(EPIW == 4 || EPIW == 8, "epilogue warps");
-  using C = PairCfg<STAGES>;
+  static_assert(ACTB == 0 || ACTB == 1 || ACTB == 16, "epilogue selection");
+  constexpr int STAGED = ACTB == 16 ? 16 : 0;
+  using C = PairCfg<STAGES, EPIW, STAGED>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes + C::kEpiBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -198,6 +362,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
       mbar_init(tempty_bar(a), 2 * EPIW);  // every epilogue warp of both CTAs (even CTA's)
     }
     mbar_init(drain_bar, 1);
+    if constexpr (STAGED) {
+      for (int k = 0; k < EPIW * kEpiSlots; ++k) mbar_init(bar0 + 8u * (2 * STAGES + 5 + k), 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -330,6 +497,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
     const int part = (warp - 2) >> 2;
     const int row_in_tile = q * 32 + lane;
     const uint32_t tempty_even[2] = {mapa_shared(tempty_bar(0), 0), mapa_shared(tempty_bar(1), 0)};
+    if constexpr (STAGED) {
+      staged_act_bwd<STAGES, EPIW, STAGED>(p, sbase + STAGES * C::kStageBytes, bar0 + 8u * (2 * STAGES + 5),
+                                   tfull_bar(0), tempty_even, tmem_base, abort_flag, rank, pair, npairs, warp);
+    } else {
     int acc = 0;
     uint32_t acc_phase = 0;
     WorkIter it(p, pair, npairs);
@@ -344,13 +515,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
       const bool finish = U.npieces == 1 ||
                           sk_piece_arrive<BN>(p, G, U, tacc, static_cast<int>(rank), row_in_tile, part, EPIW / 4,
                                               warp - 2);
-      if (finish)
-        epilogue_tile<BN>(p, G, U, tacc, U.tm * (2 * kBM) + static_cast<int>(rank) * kBM + row_in_tile, part,
-                          EPIW / 4);
+      if (finish) {
+        const int row = U.tm * (2 * kBM) + static_cast<int>(rank) * kBM + row_in_tile;
+        if constexpr (ACTB == 1) {
+          epilogue_act_bwd_rows<BN>(p, G, U, tacc, row, part, EPIW / 4);
+        } else {
+          epilogue_tile<BN>(p, G, U, tacc, row, part, EPIW / 4);
+        }
+      }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_even[acc]);
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
     }
   }
 

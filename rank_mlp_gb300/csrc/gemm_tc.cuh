@@ -31,7 +31,7 @@ namespace lgb {
 constexpr int kBM = 128;       // accumulator rows = TMEM lanes
 constexpr int kBK = 64;        // one 128-byte swizzle row of bf16 per k-block
 constexpr int kThreads = 192;
-constexpr int kMaxMaps = 12;
+constexpr int kMaxMaps = 12;   // TMA maps per launch (operand segments and staged epilogue)
 constexpr int kMaxGroups = 3;
 constexpr int kMaxSegs = 4;
 constexpr unsigned kStatusTimeout = 1u;
@@ -62,6 +62,7 @@ struct GroupDesc {
   const void* in1;
   long long ldo, ldi;
   float* part;               // EPI_PARTIAL: [splits][tiles_m*128][tiles_n*BN] f32
+  int emap[4];               // EPI_ACT_BWD on the staged variant: maps of g, u (in) and dg, du (out)
 };
 
 struct TcParams {
@@ -399,71 +400,6 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
         }
       }
     }
-  } else if (G.epi == EPI_ACT_BWD) {
-    // accumulator = dh; saved g, u give dg = dh * u * act'(g), du = dh * act(g).  The
-    // g, u loads of the next 32-column chunk are in flight while this one is computed.
-    const __nv_bfloat16* gin = static_cast<const __nv_bfloat16*>(G.in0);
-    const __nv_bfloat16* uin = static_cast<const __nv_bfloat16*>(G.in1);
-    __nv_bfloat16* dgo = static_cast<__nv_bfloat16*>(G.out0);
-    __nv_bfloat16* duo = static_cast<__nv_bfloat16*>(G.out1);
-    const bool v8 = rows_v8_aligned(dgo, G.ldo) && rows_v8_aligned(duo, G.ldo);
-    const int span = BN / nparts, c_lo = part * span, c_hi = c_lo + span;
-    const long long rbase = static_cast<long long>(row) * G.ldi + U.tn * BN;
-    auto load_chunk = [&](int c, uint4 (&gw)[4], uint4 (&uw)[4]) {
-      const int col0 = U.tn * BN + c;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (row_ok && col0 + 8 * j + 8 <= G.N) {
-          gw[j] = __ldg(reinterpret_cast<const uint4*>(gin + rbase + c + 8 * j));
-          uw[j] = __ldg(reinterpret_cast<const uint4*>(uin + rbase + c + 8 * j));
-        } else {
-          gw[j] = make_uint4(0, 0, 0, 0);
-          uw[j] = make_uint4(0, 0, 0, 0);
-        }
-      }
-    };
-    uint4 gw[4], uw[4];
-    load_chunk(c_lo, gw, uw);
-#pragma unroll 1
-    for (int c = c_lo; c < c_hi; c += 32) {
-      uint4 gn[4], un[4];
-      if (c + 32 < c_hi) load_chunk(c + 32, gn, un);
-      const int col0 = U.tn * BN + c;
-      uint32_t v[32];
-      __syncwarp();
-      tmem_ld32(tacc + c, v);
-      tmem_ld_wait();
-      if (row_ok) {
-        const long long ooff = static_cast<long long>(row) * G.ldo + col0;
-        uint32_t og[16], ou[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t gg[4] = {gw[j].x, gw[j].y, gw[j].z, gw[j].w};
-          const uint32_t uu[4] = {uw[j].x, uw[j].y, uw[j].z, uw[j].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float a0, ap0, a1, ap1;
-            const float g0 = bf16_lo(gg[e]), g1 = bf16_hi(gg[e]);
-            const float u0 = bf16_lo(uu[e]), u1 = bf16_hi(uu[e]);
-            act_fwd_bwd_rt(g0, p.act, a0, ap0);
-            act_fwd_bwd_rt(g1, p.act, a1, ap1);
-            const float d0 = __uint_as_float(v[8 * j + 2 * e]);
-            const float d1 = __uint_as_float(v[8 * j + 2 * e + 1]);
-            og[4 * j + e] = pack_bf16x2(d0 * u0 * ap0, d1 * u1 * ap1);
-            ou[4 * j + e] = pack_bf16x2(d0 * a0, d1 * a1);
-          }
-        }
-        store_row32_bf16(dgo + ooff, og, col0, G.N, v8);
-        store_row32_bf16(duo + ooff, ou, col0, G.N, v8);
-      }
-      if (c + 32 < c_hi) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          gw[j] = gn[j];
-          uw[j] = un[j];
-        }
-      }
-    }
   } else if (G.epi == EPI_ROPE) {
     // EPI_STORE (bias included) followed by the rotary embedding of every head in the
     // tile ("Model Patches and Kernels", RoPE): the pair (c, c + half) of a head turns
@@ -557,6 +493,79 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
       tmem_ld_wait();
 #pragma unroll
       for (int j = 0; j < 32; j += 8) st_global_v8(dst + c + j, v + j);
+    }
+  }
+}
+
+// The activation-derivative epilogue with one row per thread (the CTA-pair kernel's
+// variant for long K, where each tile's MMAs hide it): the accumulator is dh; the saved
+// g, u of the row give dg = dh u act'(g), du = dh act(g).  The thread loads the g, u of
+// the next 32-column chunk while this one is computed.  Warp-collective like
+// epilogue_tile; rows past M are computed and dropped.
+template <int BN>
+__device__ __forceinline__ void epilogue_act_bwd_rows(const TcParams& p, const GroupDesc& G, const Unit& U,
+                                                      uint32_t tacc, int row, int part, int nparts) {
+  const bool row_ok = row < G.M;
+  const __nv_bfloat16* gin = static_cast<const __nv_bfloat16*>(G.in0);
+  const __nv_bfloat16* uin = static_cast<const __nv_bfloat16*>(G.in1);
+  __nv_bfloat16* dgo = static_cast<__nv_bfloat16*>(G.out0);
+  __nv_bfloat16* duo = static_cast<__nv_bfloat16*>(G.out1);
+  const bool v8 = rows_v8_aligned(dgo, G.ldo) && rows_v8_aligned(duo, G.ldo);
+  const int span = BN / nparts, c_lo = part * span, c_hi = c_lo + span;
+  const long long rbase = static_cast<long long>(row) * G.ldi + U.tn * BN;
+  auto load_chunk = [&](int c, uint4 (&gw)[4], uint4 (&uw)[4]) {
+    const int col0 = U.tn * BN + c;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (row_ok && col0 + 8 * j + 8 <= G.N) {
+        gw[j] = __ldg(reinterpret_cast<const uint4*>(gin + rbase + c + 8 * j));
+        uw[j] = __ldg(reinterpret_cast<const uint4*>(uin + rbase + c + 8 * j));
+      } else {
+        gw[j] = make_uint4(0, 0, 0, 0);
+        uw[j] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  uint4 gw[4], uw[4];
+  load_chunk(c_lo, gw, uw);
+#pragma unroll 1
+  for (int c = c_lo; c < c_hi; c += 32) {
+    uint4 gn[4], un[4];
+    if (c + 32 < c_hi) load_chunk(c + 32, gn, un);
+    const int col0 = U.tn * BN + c;
+    uint32_t v[32];
+    __syncwarp();
+    tmem_ld32(tacc + c, v);
+    tmem_ld_wait();
+    if (row_ok) {
+      const long long ooff = static_cast<long long>(row) * G.ldo + col0;
+      uint32_t og[16], ou[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t gg[4] = {gw[j].x, gw[j].y, gw[j].z, gw[j].w};
+        const uint32_t uu[4] = {uw[j].x, uw[j].y, uw[j].z, uw[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float a0, ap0, a1, ap1;
+          const float g0 = bf16_lo(gg[e]), g1 = bf16_hi(gg[e]);
+          const float u0 = bf16_lo(uu[e]), u1 = bf16_hi(uu[e]);
+          act_fwd_bwd_rt(g0, p.act, a0, ap0);
+          act_fwd_bwd_rt(g1, p.act, a1, ap1);
+          const float d0 = __uint_as_float(v[8 * j + 2 * e]);
+          const float d1 = __uint_as_float(v[8 * j + 2 * e + 1]);
+          og[4 * j + e] = pack_bf16x2(d0 * u0 * ap0, d1 * u1 * ap1);
+          ou[4 * j + e] = pack_bf16x2(d0 * a0, d1 * a1);
+        }
+      }
+      store_row32_bf16(dgo + ooff, og, col0, G.N, v8);
+      store_row32_bf16(duo + ooff, ou, col0, G.N, v8);
+    }
+    if (c + 32 < c_hi) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        gw[j] = gn[j];
+        uw[j] = un[j];
+      }
     }
   }
 }

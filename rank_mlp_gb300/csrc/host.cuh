@@ -28,8 +28,19 @@ enum Variant : int {
   V128_MNMN = 5,
   VP_KK8 = 6,      // VP_KK with 8 epilogue warps: short-K launches, where 4 warps' epilogue
                    // outlasts a tile's MMAs
-  kNumVariants = 7
+  VP_KMN_ACT = 7,   // VP_KMN for the activation-derivative GEMM: saved g, u in and dg, du out
+                    // one row per thread (6 stages)
+  VP_KMN_ACT16 = 8, // the same for short K: g, u and dg, du through shared memory by TMA
+                    // in 16-column chunks (5 stages leave room for the rings)
+  kNumVariants = 9
 };
+
+// An activation-derivative launch whose K is at most this many k-blocks runs
+// VP_KMN_ACT16: its tiles' MMAs are too short to hide the epilogue's traffic, and the
+// staged epilogue keeps more of it in flight.  Longer K needs the sixth stage to keep
+// the MMAs fed (measured: the staged variant at 5 stages, or at 6 with 8-column chunks,
+// was 5-15% slower there than one row per thread).
+constexpr int kActShortKBlocks = 32;
 
 // A forward pair launch whose longest K is at most this many 64-wide k-blocks runs
 // VP_KK8: a tile's MMAs (~0.28 us per k-block) then no longer cover the 4-warp
@@ -40,10 +51,14 @@ constexpr int kShortKBlocks = 32;
 // 32-bit integers and TMA coordinates are 32-bit.
 constexpr int64_t kMaxExtent = 0x7fffffff;
 
-constexpr bool variant_pair(int v) { return v == VP_KK || v == VP_KMN || v == VP_KK8; }
+constexpr bool variant_pair(int v) {
+  return v == VP_KK || v == VP_KMN || v == VP_KK8 || v == VP_KMN_ACT || v == VP_KMN_ACT16;
+}
 constexpr int variant_bn(int v) { return variant_pair(v) ? 256 : (v <= V64_MNMN ? 64 : 128); }
 constexpr bool variant_a_mn(int v) { return v == V64_MNMN || v == V128_MNMN; }
-constexpr bool variant_b_mn(int v) { return v == VP_KMN || v == V64_MNMN || v == V128_MNMN; }
+constexpr bool variant_b_mn(int v) {
+  return v == VP_KMN || v == VP_KMN_ACT || v == VP_KMN_ACT16 || v == V64_MNMN || v == V128_MNMN;
+}
 
 // The big projection GEMMs run on CTA pairs (256 x 256 tiles).
 constexpr int kBigKK = VP_KK;
@@ -99,7 +114,7 @@ int tc_smem_bytes(int variant);
 // Defined in lora_api.cu.
 int num_sms();
 bool encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
-                uint32_t box_inner, uint32_t box_outer);
+                uint32_t box_inner, uint32_t box_outer, int swizzle_bytes = 128);
 bool encode_map_planes(CUtensorMap* m, const void* base, uint64_t inner, uint64_t d1, uint64_t d2, uint64_t ld,
                        uint32_t box_inner, uint32_t box_d1);
 lora_status_t launch_gemm(int variant, const TcParams& p, int kind, cudaStream_t st);
@@ -225,10 +240,16 @@ struct GemmPlan {
     p.sk_cap_tiles = r.tiles;
   }
 
-  int add_map(const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t bi, uint32_t bo) {
+  int add_map(const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t bi, uint32_t bo,
+              int swizzle_bytes = 128) {
     if (!ok || p.nmaps >= kMaxMaps) { ok = false; return -1; }
-    if (!encode_map(&p.maps[p.nmaps], base, inner, outer, ld, bi, bo)) { ok = false; return -1; }
+    if (!encode_map(&p.maps[p.nmaps], base, inner, outer, ld, bi, bo, swizzle_bytes)) { ok = false; return -1; }
     return p.nmaps++;
+  }
+  // An epilogue operand or output [rows x cols] (row stride ld) moved by TMA in boxes of
+  // 32 rows x 16 columns (one warp's rows, 32 bytes of each), 32-byte swizzle.
+  int epi_map(const void* base, int64_t rows, int64_t cols, int64_t ld) {
+    return add_map(base, cols, rows, ld, 16, 32, 32);
   }
   // A operand, K-major: activation [rows x K] with row stride ld.
   int a_kmajor(const void* base, int64_t rows, int64_t K, int64_t ld) {

@@ -42,9 +42,10 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map with 128-byte swizzle; out-of-bounds elements read as zero.
+// 2-D bf16 map with a 128-byte, 32-byte or no swizzle (swizzle_bytes 128, 32, 0);
+// out-of-bounds elements read as zero.
 bool encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
-                uint32_t box_inner, uint32_t box_outer) {
+                uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr || inner == 0 || outer == 0) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -52,8 +53,11 @@ bool encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+            : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                  : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 3-D bf16 map {inner, d1, d2} with row stride ld (elements) and plane stride

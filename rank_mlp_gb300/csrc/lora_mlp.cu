@@ -277,24 +277,35 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   const ProjSeg p1 = {dy, bt_d, h};
   LGB_TRY(rank_projection(M, kfd, &p1, 1, ud, part, status, stream));
 
-  // dh = [dy | U_d] [W_d ; s A_d];  dg = dh u act'(g), du = dh act(g)
+  // dh = [dy | U_d] [W_d ; s A_d];  dg = dh u act'(g), du = dh act(g).  Short K: g, u read
+  // and dg, du written through shared memory (whole tiles: that variant has no split
+  // tail); long K: one row per thread.
   {
-    GemmPlan g(kBigKMN);
+    const bool staged = ceil_div(h, kBK) + ceil_div(r, kBK) <= kActShortKBlocks;
+    const int variant = staged ? VP_KMN_ACT16 : VP_KMN_ACT;
+    GemmPlan g(variant);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(i), EPI_ACT_BWD, false);
     GemmPlan::seg(G, g.a_kmajor(dy, M, h, h), g.b_mnmajor(down.W, i, h, i), -1, h, h);
     GemmPlan::seg(G, g.a_kmajor(ud, M, kfd, kfd), g.b_mnmajor(af_d, i, kfd, i), -1, kfd, r);
-    G.in0 = gsv;
-    G.in1 = usv;
-    G.ldi = i;
-    G.out0 = dg;
-    G.out1 = du;
-    G.ldo = i;
+    if (staged) {
+      G.emap[0] = g.epi_map(gsv, M, i, i);
+      G.emap[1] = g.epi_map(usv, M, i, i);
+      G.emap[2] = g.epi_map(dg, M, i, i);
+      G.emap[3] = g.epi_map(du, M, i, i);
+    } else {
+      G.in0 = gsv;
+      G.in1 = usv;
+      G.ldi = i;
+      G.out0 = dg;
+      G.out1 = du;
+      G.ldo = i;
+    }
     g.p.act = static_cast<int>(act);
     g.p.status = status;
     g.finish();
-    g.split_tail(sk);
+    if (!staged) g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
-    LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_ACT_BWD, stream));
+    LGB_TRY(launch_gemm(variant, g.p, LORA_KIND_ACT_BWD, stream));
   }
 
   // dB_d = s dy^T T_d and dA_d = s U_d^T h read nothing the dh GEMM writes: they start
