@@ -60,7 +60,7 @@ lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int nseg, 
 // f32 slab elements of a rank-r projection over ktotal_blocks 64-wide k-blocks.
 int64_t rank_projection_part(int64_t M, int kf, int64_t ktotal_blocks);
 
-// Reductions over tokens: for each job j, D_j[f x kf] = Q_j[tokens x f]^T * T[tokens x kf],
+// Reductions over tokens: for each job j, D_j[f x kf] = Q_j[tokens x f]^T * T_j[tokens x kf],
 // then out = s * D_j[:, col0 .. col0+r) written as [f x r] (dB) or transposed [r x f] (dA).
 struct GradJob {
   const void* Q;      // [M x f] token-major
@@ -68,6 +68,7 @@ struct GradJob {
   int col0;           // rank slot inside T
   void* dst;
   int trans;          // 1: dst is [r x f] (dA), 0: dst is [f x r] (dB)
+  const void* T;      // [M x kf] token-major rank-r operand
 };
 // f32 slab elements of the token reductions of n products (fs[j] features each).
 // n_ex > 0: per-example mode, one slab per example.
@@ -82,10 +83,10 @@ struct Deferred {
 };
 void defer_init(Deferred& d, float* slabs);
 lora_status_t defer_flush(Deferred& d, cudaStream_t st);
-// Reductions over tokens of the jobs (see lora_api.cu); late: the launch reads nothing
-// the previous kernel writes and writes nothing it reads (pdl_late).
-lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* T, const GradJob* jobs, int njobs,
-                          Deferred& defer, unsigned* status, cudaStream_t st, int64_t n_ex = 0, bool late = false);
+// Reductions over tokens of the jobs in one launch (see lora_api.cu); late: the launch
+// reads nothing the previous kernel writes and writes nothing it reads (pdl_late).
+lora_status_t token_grads(int64_t M, int r, int kf, float s, const GradJob* jobs, int njobs, Deferred& defer,
+                          unsigned* status, cudaStream_t st, int64_t n_ex = 0, bool late = false);
 
 lora_status_t launch_rope(const RopeParams& p, cudaStream_t st);
 

@@ -32,7 +32,7 @@ constexpr int kBM = 128;       // accumulator rows = TMEM lanes
 constexpr int kBK = 64;        // one 128-byte swizzle row of bf16 per k-block
 constexpr int kThreads = 192;
 constexpr int kMaxMaps = 12;   // TMA maps per launch (operand segments and staged epilogue)
-constexpr int kMaxGroups = 3;
+constexpr int kMaxGroups = 4;
 constexpr int kMaxSegs = 4;
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kStatusInput = 2u;   // a device-side input out of range (a RoPE position)
@@ -71,7 +71,7 @@ struct TcParams {
   int nmaps;
   int ngroups;
   int total_units;
-  int band;                  // raster: n-tiles per band, m fastest inside a band
+  int band;                  // raster: n-tiles per band, n fastest inside a band
   int act;
   unsigned int* status;
   unsigned long long timeout_ns;

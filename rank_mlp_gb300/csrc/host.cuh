@@ -76,6 +76,17 @@ inline bool pdl_enabled() {
   return on;
 }
 
+// Raster of the GEMM tiles: bands of this many n-tiles, the n-tile fastest inside a band
+// (environment LORA_RASTER_BAND overrides the default of 16, for measurements).
+inline int raster_band() {
+  static const int band = [] {
+    const char* e = std::getenv("LORA_RASTER_BAND");
+    const int v = e != nullptr ? std::atoi(e) : 0;
+    return v >= 1 && v <= 4096 ? v : 16;
+  }();
+  return band;
+}
+
 template <typename Kernel, typename Arg>
 inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const Arg& arg) {
   cudaLaunchConfig_t cfg = {};
@@ -153,6 +164,27 @@ inline int choose_splits(int64_t tiles, int64_t kb_total, int sms) {
   double best_cost = 1e30;
   for (int s = 1; s <= smax; ++s) {
     const double cost = static_cast<double>(ceil_div(tiles * s, sms)) / s;
+    if (cost < best_cost * (1.0 - 1e-9)) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+// Split-K factor of a rank-r projection (`tiles` 128-row tiles of kb_total k-blocks
+// each): like choose_splits, but a split pays for the launch that sums its partials,
+// worth about kReduceKBlocks k-blocks of one tile (a tile streams 24 KB per k-block:
+// ~0.25 us at one SM's share of the bandwidth; the reduce launch ~3 us).  Small
+// problems (the Qwen-shaped x A^T: 32 tiles of 14 k-blocks) then run unsplit.
+constexpr int kReduceKBlocks = 12;
+inline int choose_proj_splits(int64_t tiles, int64_t kb_total, int sms) {
+  if (tiles <= 0 || kb_total <= 0 || sms <= 0) return 1;
+  const int smax = max_splits(kb_total);
+  int best = 1;
+  double best_cost = 1e30;
+  for (int s = 1; s <= smax; ++s) {
+    const double cost = static_cast<double>(ceil_div(tiles * s, sms)) / s * kb_total + (s > 1 ? kReduceKBlocks : 0);
     if (cost < best_cost * (1.0 - 1e-9)) {
       best_cost = cost;
       best = s;
@@ -316,7 +348,8 @@ struct GemmPlan {
     p.sk_splits = 0;
     int maxtn = 1;
     for (int g = 0; g < p.ngroups; ++g) maxtn = p.grp[g].tiles_n > maxtn ? p.grp[g].tiles_n : maxtn;
-    p.band = maxtn < 16 ? maxtn : 16;
+    const int band = raster_band();
+    p.band = maxtn < band ? maxtn : band;
   }
 };
 

@@ -296,7 +296,7 @@ lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int nseg, 
   int64_t kb = 0;
   for (int s = 0; s < nseg; ++s) kb += ceil_div(segs[s].K, kBK);
   const int64_t tiles = ceil_div(M, kBM) * ceil_div(kf, g.bn);
-  const int splits = choose_splits(tiles, kb, num_sms());
+  const int splits = choose_proj_splits(tiles, kb, num_sms());
   GroupDesc& G = g.group(static_cast<int>(M), kf, splits > 1 ? EPI_PARTIAL : EPI_STORE, false);
   G.splits = splits;
   for (int s = 0; s < nseg; ++s) {
@@ -358,44 +358,57 @@ lora_status_t defer_flush(Deferred& d, cudaStream_t st) {
   return r;
 }
 
-// Jobs with the same Q share one slab (several rank slots out of one product).
-// n_ex == 0: the sums over all M tokens.  n_ex > 0: one result per example (example e
-// = tokens [e seq, (e+1) seq), seq = M / n_ex), each written at dst + e * r * f; the
-// products read 3-D views {features, seq, examples} so no k-block straddles two
-// examples (rows past seq read as zero).  The slabs start at defer.cursor and the
-// sums are left to defer_flush.
+// Jobs with the same Q and T share one group (and one slab: several rank slots out of
+// one product).  n_ex == 0: the sums over all M tokens.  n_ex > 0: one result per
+// example (example e = tokens [e seq, (e+1) seq), seq = M / n_ex), each written at
+// dst + e * r * f; the products read 3-D views {features, seq, examples} so no k-block
+// straddles two examples (rows past seq read as zero).  The slabs start at
+// defer.cursor and the sums are left to defer_flush.
 // late: the launch follows a kernel whose outputs it does not read (and whose inputs
 // it does not write), so it may start on SMs that kernel has freed (pdl_late).
-lora_status_t token_grads(int64_t M, int r, int kf, float s, const void* T, const GradJob* jobs, int njobs,
-                          Deferred& defer, unsigned* status, cudaStream_t st, int64_t n_ex, bool late) {
+lora_status_t token_grads(int64_t M, int r, int kf, float s, const GradJob* jobs, int njobs, Deferred& defer,
+                          unsigned* status, cudaStream_t st, int64_t n_ex, bool late) {
   const int variant = skinny_mnmn(kf);
   GemmPlan g(variant);
   g.p.pdl_late = late ? 1 : 0;
   const int64_t seq = n_ex > 0 ? M / n_ex : M;
-  const int tmap = n_ex > 0 ? g.b_mnmajor_planes(T, kf, seq, n_ex, kf) : g.b_mnmajor(T, kf, M, kf);
   const void* qs[kMaxGroups];
-  int nq = 0, group_of[kMaxGroups * 3];
+  const void* ts[kMaxGroups];
+  const void* tmap_src[kMaxGroups];
+  int tmap_of[kMaxGroups];
+  int nq = 0, nt = 0, group_of[kMaxGroups * 3];
   float* parts[kMaxGroups];
   float* cur = defer.cursor;
   const int slab_splits = n_ex > 0 ? static_cast<int>(n_ex) : max_splits(ceil_div(M, kBK));
   for (int j = 0; j < njobs; ++j) {
     int gi = -1;
     for (int q = 0; q < nq; ++q)
-      if (qs[q] == jobs[j].Q) gi = q;
+      if (qs[q] == jobs[j].Q && ts[q] == jobs[j].T) gi = q;
     if (gi < 0) {
+      if (nq >= kMaxGroups) return LORA_ERR_UNSUPPORTED;   // not reached: <= 4 per call site
+      // the rank-r operand's map, shared by the groups that read the same T
+      int tm = -1;
+      for (int k = 0; k < nt; ++k)
+        if (tmap_src[k] == jobs[j].T) tm = tmap_of[k];
+      if (tm < 0) {
+        tm = n_ex > 0 ? g.b_mnmajor_planes(jobs[j].T, kf, seq, n_ex, kf) : g.b_mnmajor(jobs[j].T, kf, M, kf);
+        tmap_src[nt] = jobs[j].T;
+        tmap_of[nt++] = tm;
+      }
       gi = nq++;
       qs[gi] = jobs[j].Q;
+      ts[gi] = jobs[j].T;
       const int64_t tiles = ceil_div(jobs[j].f, kBM) * ceil_div(kf, g.bn);
       GroupDesc& G = g.group(static_cast<int>(jobs[j].f), kf, EPI_PARTIAL, false);
       if (n_ex > 0) {
         G.splits = static_cast<int>(n_ex);
         G.per_plane = 1;
         const int a = g.a_mnmajor_planes(jobs[j].Q, jobs[j].f, seq, n_ex, jobs[j].f);
-        GemmPlan::seg(G, a, tmap, -1, seq, seq);
+        GemmPlan::seg(G, a, tm, -1, seq, seq);
       } else {
         G.splits = choose_splits(tiles, ceil_div(M, kBK), num_sms());
         const int a = g.a_mnmajor(jobs[j].Q, jobs[j].f, M, jobs[j].f);
-        GemmPlan::seg(G, a, tmap, -1, M, M);
+        GemmPlan::seg(G, a, tm, -1, M, M);
       }
       G.part = cur;
       parts[gi] = cur;

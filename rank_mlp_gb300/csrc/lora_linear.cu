@@ -194,10 +194,8 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   if (!g.ok) return LORA_ERR_CUDA;
   LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
 
-  const GradJob ja = {x, in, 0, grads.dA, 1};
-  // dB = s dy^T T and dA = s U^T x read nothing the dx GEMM writes
-  const GradJob jb = {dy, out, 0, grads.dB, 0};
-  LGB_TRY(token_grads(M, r, kf, s, T, &jb, 1, dr, status, stream, 0, true));
-  LGB_TRY(token_grads(M, r, kf, s, U, &ja, 1, dr, status, stream, 0, true));
+  // dB = s dy^T T and dA = s U^T x (one launch) read nothing the dx GEMM writes
+  const GradJob jobs[2] = {{dy, out, 0, grads.dB, 0, T}, {x, in, 0, grads.dA, 1, U}};
+  LGB_TRY(token_grads(M, r, kf, s, jobs, 2, dr, status, stream, 0, true));
   return defer_flush(dr, stream);
 }

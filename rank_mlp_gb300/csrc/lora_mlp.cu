@@ -308,12 +308,10 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
     LGB_TRY(launch_gemm(variant, g.p, LORA_KIND_ACT_BWD, stream));
   }
 
-  // dB_d = s dy^T T_d and dA_d = s U_d^T h read nothing the dh GEMM writes: they start
-  // on the SMs its last wave leaves idle
-  const GradJob j1 = {dy, h, 0, d_down.dB, 0};
-  LGB_TRY(token_grads(M, r, kfd, s, td, &j1, 1, dr, status, stream, n_ex, true));
-  const GradJob j2 = {hsv, i, 0, d_down.dA, 1};
-  LGB_TRY(token_grads(M, r, kfd, s, ud, &j2, 1, dr, status, stream, n_ex, true));
+  // dB_d = s dy^T T_d and dA_d = s U_d^T h (one launch) read nothing the dh GEMM writes:
+  // they start on the SMs its last wave leaves idle
+  const GradJob j1[2] = {{dy, h, 0, d_down.dB, 0, td}, {hsv, i, 0, d_down.dA, 1, ud}};
+  LGB_TRY(token_grads(M, r, kfd, s, j1, 2, dr, status, stream, n_ex, true));
 
   // V = [dg B_g | du B_u]
   const ProjSeg p3[2] = {{dg, bt_g, i}, {du, bt_u, i}};
@@ -336,12 +334,12 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
   }
 
-  // dB_g = s dg^T T_g, dB_u = s du^T T_u and dA_g = s V_g^T x, dA_u = s V_u^T x read
-  // nothing the dx GEMM writes: they start on the SMs its last wave leaves idle
-  const GradJob j3[2] = {{dg, i, 0, d_gate.dB, 0}, {du, i, r, d_up.dB, 0}};
-  LGB_TRY(token_grads(M, r, kfg, s, tgu, j3, 2, dr, status, stream, n_ex, true));
-  const GradJob j4[2] = {{x, h, 0, d_gate.dA, 1}, {x, h, r, d_up.dA, 1}};
-  LGB_TRY(token_grads(M, r, kfg, s, V, j4, 2, dr, status, stream, n_ex, true));
+  // dB_g = s dg^T T_g, dB_u = s du^T T_u and dA_g = s V_g^T x, dA_u = s V_u^T x (one
+  // launch) read nothing the dx GEMM writes: they start on the SMs its last wave leaves
+  // idle
+  const GradJob j3[4] = {{dg, i, 0, d_gate.dB, 0, tgu}, {du, i, r, d_up.dB, 0, tgu},
+                         {x, h, 0, d_gate.dA, 1, V}, {x, h, r, d_up.dA, 1, V}};
+  LGB_TRY(token_grads(M, r, kfg, s, j3, 4, dr, status, stream, n_ex, true));
   LGB_TRY(defer_flush(dr, stream));
   if (n_ex > 0 && sq_norms != nullptr) {
     NormParams np;

@@ -317,11 +317,10 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
-    // dB_o = s dy_o^T T_o and dA_o = s U_o^T o_in read nothing the d o_in GEMM writes
-    const GradJob j1 = {dyo, h, 0, d_o.dB, 0};
-    LGB_TRY(token_grads(M, r, kfo, s, to, &j1, 1, dr, status, stream, 0, true));
-    const GradJob j2 = {o_in, n_q, 0, d_o.dA, 1};
-    LGB_TRY(token_grads(M, r, kfo, s, uo, &j2, 1, dr, status, stream, 0, true));
+    // dB_o = s dy_o^T T_o and dA_o = s U_o^T o_in (one launch) read nothing the d o_in
+    // GEMM writes
+    const GradJob j1[2] = {{dyo, h, 0, d_o.dB, 0, to}, {o_in, n_q, 0, d_o.dA, 1, uo}};
+    LGB_TRY(token_grads(M, r, kfo, s, j1, 2, dr, status, stream, 0, true));
   }
   if (x) {
     if (rope != nullptr) {
@@ -362,11 +361,11 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
-    const GradJob j4[3] = {{x, h, 0, d_q.dA, 1}, {x, h, r, d_k.dA, 1}, {x, h, 2 * r, d_v.dA, 1}};
-    // the q, k, v dB and dA read nothing the dx GEMM writes
-    const GradJob j3[3] = {{dyq, n_q, 0, d_q.dB, 0}, {dyk, n_kv, r, d_k.dB, 0}, {dyv, n_kv, 2 * r, d_v.dB, 0}};
-    LGB_TRY(token_grads(M, r, kfq, s, tqkv, j3, 3, dr, status, stream, 0, true));
-    LGB_TRY(token_grads(M, r, kfq, s, V, j4, 3, dr, status, stream, 0, true));
+    // the q, k, v dB and dA (one launch) read nothing the dx GEMM writes
+    const GradJob j3[6] = {{dyq, n_q, 0, d_q.dB, 0, tqkv}, {dyk, n_kv, r, d_k.dB, 0, tqkv},
+                           {dyv, n_kv, 2 * r, d_v.dB, 0, tqkv}, {x, h, 0, d_q.dA, 1, V},
+                           {x, h, r, d_k.dA, 1, V}, {x, h, 2 * r, d_v.dA, 1, V}};
+    LGB_TRY(token_grads(M, r, kfq, s, j3, 6, dr, status, stream, 0, true));
   }
   return defer_flush(dr, stream);
 }

@@ -18,7 +18,7 @@ def test_traffic_row_is_per_kernel_and_workload():
     seven = bench.traffic_workload_key(synth.MLP_CONFIGS["llama7b"])
     qwen = bench.traffic_workload_key(synth.MLP_CONFIGS["qwen05b"])
     assert bench.ncu_traffic("gate_up", qwen) is None
-    assert bench.ncu_traffic("proj", seven) is None
+    assert bench.ncu_traffic("rank_proj", seven) is None
     got = bench.ncu_traffic("gate_up", seven)
     if got is not None:
         # at least the algorithmic bytes: x, W_g, W_u read once, h, g, u written once

@@ -150,10 +150,10 @@ def test_launches_per_call(lib):
     """The launch structure of each call.  MLP forward: pack, the two rank-r
     projections (x A^T, h A^T), the gate/up and down GEMMs, and one split-K reduction
     per rank-r projection that was split.  MLP backward: pack, two rank-r projections
-    (dy B_d, [dg du][B_g B_u]) with their split-K sums, four reductions over tokens
-    (dB_d, dA_d, dB_g|dB_u, dA_g|dA_u) whose sums share one launch at the end, and the
-    act' and dx GEMMs.  Q/K/V + O with
-    RoPE: the same per half, plus one transpose-rotation launch in the backward."""
+    (dy B_d, [dg du][B_g B_u]) with their split-K sums, the reductions over tokens in two
+    launches (dB_d and dA_d after the act' GEMM; dB_g, dB_u, dA_g, dA_u after the dx
+    GEMM) whose sums share one launch at the end, and the act' and dx GEMMs.  Q/K/V + O
+    with RoPE: the same per half, plus one transpose-rotation launch in the backward."""
     cfg = synth.MLP_CONFIGS["qwen05b"].replace(M=1024)
     ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg).items()}
     lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
@@ -169,7 +169,7 @@ def test_launches_per_call(lib):
     assert (f["pack"], f["rank_proj"], f["gate_up"], f["proj"]) == (1, 2, 1, 1), f
     assert f["reduce"] <= 2 and set(f) <= {"pack", "rank_proj", "gate_up", "proj", "reduce"}, f
     b = _kinds(lib, bwd)
-    assert (b["pack"], b["rank_proj"], b["rank_grad"], b["act_bwd"], b["dgrad"]) == (1, 2, 4, 1, 1), b
+    assert (b["pack"], b["rank_proj"], b["rank_grad"], b["act_bwd"], b["dgrad"]) == (1, 2, 2, 1, 1), b
     # split-K sums of the two rank-r projections (if split), then one for all four
     # reductions over tokens at the end of the call
     assert 1 <= b["reduce"] <= 3 and set(b) <= {"pack", "rank_proj", "rank_grad", "act_bwd", "dgrad",
@@ -191,8 +191,27 @@ def test_launches_per_call(lib):
     f = _kinds(lib, qfwd)
     assert (f["pack"], f["rank_proj"], f["proj"]) == (1, 2, 2), f
     b = _kinds(lib, qbwd)
-    assert (b["pack"], b["rope"], b["rank_proj"], b["rank_grad"], b["dgrad"]) == (1, 1, 2, 4, 2), b
+    assert (b["pack"], b["rope"], b["rank_proj"], b["rank_grad"], b["dgrad"]) == (1, 1, 2, 2, 2), b
     assert 1 <= b["reduce"] <= 3, b
+    assert lib.poll_status() == 0
+
+
+def test_qwen_shaped_step_launches(lib):
+    """The Qwen-shaped forward + backward (4096 tokens, h = 896, i = 4864, r = 16) makes
+    at most 15 launches: x A^T and dy B_d run unsplit (their split-K sums would cost
+    more than the split saves), and each backward's reductions over tokens take two
+    launches."""
+    cfg = synth.MLP_CONFIGS["qwen05b"]
+    ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg, seed=4).items()}
+    lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
+    y, saved = lib.mlp_forward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act)
+    lib.mlp_backward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, saved, ins["dy"])
+    torch.cuda.synchronize()
+    before = lib.launch_count()
+    y, saved = lib.mlp_forward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act)
+    lib.mlp_backward(ins["x"], lin("gate"), lin("up"), lin("down"), cfg.s, cfg.act, saved, ins["dy"])
+    torch.cuda.synchronize()
+    assert lib.launch_count() - before <= 15
     assert lib.poll_status() == 0
 
 
