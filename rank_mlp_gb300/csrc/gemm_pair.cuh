@@ -441,9 +441,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (leader && lane == 0) {
+      // This lane's instructions between MMAs are on the tensor pipe's critical path
+      // (tcgen05.mma issue keeps only a short queue), so the loop is kept lean: the
+      // shared-memory descriptors are those of stage 0 plus constant offsets, and the
+      // next stage's data is tested (without blocking) before this stage's last MMA is
+      // issued, so the common case needs no wait between stages.
       constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, BN, 0, B_MN ? 1 : 0);
+      const uint64_t adesc0 = smem_desc_sw128(sbase, 16u, 1024u);
+      const uint64_t bdesc0 = B_MN ? smem_desc_sw128(sbase + C::kABytes, 8192u, 1024u)
+                                   : smem_desc_sw128(sbase + C::kABytes, 16u, 1024u);
+      constexpr uint64_t kStageStep = C::kStageBytes >> 4;          // descriptor address units
+      constexpr uint64_t kAStep = 32 >> 4;                          // one 16-wide k step
+      constexpr uint64_t kBStep = B_MN ? (2048 >> 4) : (32 >> 4);
       int stage = 0;
       uint32_t phase = 0;
+      bool landed = false;       // the current stage's copies are known to have landed
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -463,22 +475,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
           seg_base += nkb;
           for (int j = j0; j < j1; ++j) {
             const int kc = j * kBK;
-            if (!wait_phase(full_bar(stage), phase, abort_flag, p)) { ok = false; break; }
+            if (!landed && !wait_phase(full_bar(stage), phase, abort_flag, p)) { ok = false; break; }
             tc_fence_after_sync();
-            const uint32_t sa = sbase + stage * C::kStageBytes;
-            const uint32_t sb = sa + C::kABytes;
+            const int nstage = stage + 1 == STAGES ? 0 : stage + 1;
+            const uint32_t nphase = stage + 1 == STAGES ? phase ^ 1u : phase;
+            const uint64_t ad = adesc0 + static_cast<uint64_t>(stage) * kStageStep;
+            const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage) * kStageStep;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
+              if (k == kBK / 16 - 1) landed = mbar_test_wait(full_bar(nstage), nphase);
               if (kc + 16 * k < kvalid) {
-                const uint64_t adesc = smem_desc_sw128(sa + 32u * k, 16u, 1024u);
-                const uint64_t bdesc = B_MN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
-                                            : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
-                tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
+                tc_mma_bf16_pair(d_tmem, ad + k * kAStep, bd + k * kBStep, idesc, accumulate);
                 accumulate = 1;
               }
             }
             tc_commit_pair_multicast(empty_bar(stage), 0x3);   // frees this stage in both CTAs
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            stage = nstage;
+            phase = nphase;
           }
         }
         if (!ok) break;

@@ -691,9 +691,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // lean MMA loop: see the CTA-pair kernel (descriptors from stage 0 plus offsets;
+      // the next stage tested before this stage's last MMA)
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN, A_MN ? 1 : 0, B_MN ? 1 : 0);
+      const uint64_t adesc0 = A_MN ? smem_desc_sw128(sbase, 8192u, 1024u) : smem_desc_sw128(sbase, 16u, 1024u);
+      const uint64_t bdesc0 = B_MN ? smem_desc_sw128(sbase + C::kABytes, 8192u, 1024u)
+                                   : smem_desc_sw128(sbase + C::kABytes, 16u, 1024u);
+      constexpr uint64_t kStageStep = C::kStageBytes >> 4;
+      constexpr uint64_t kAStep = A_MN ? (2048 >> 4) : (32 >> 4);
+      constexpr uint64_t kBStep = B_MN ? (2048 >> 4) : (32 >> 4);
       int stage = 0;
       uint32_t phase = 0;
+      bool landed = false;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -712,23 +721,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           seg_base += nkb;
           for (int j = j0; j < j1; ++j) {
             const int kc = j * kBK;
-            if (!wait_phase(full_bar(stage), phase, abort_flag, p)) { ok = false; break; }
+            if (!landed && !wait_phase(full_bar(stage), phase, abort_flag, p)) { ok = false; break; }
             tc_fence_after_sync();
-            const uint32_t sa = sbase + stage * C::kStageBytes;
-            const uint32_t sb = sa + C::kABytes;
+            const int nstage = stage + 1 == STAGES ? 0 : stage + 1;
+            const uint32_t nphase = stage + 1 == STAGES ? phase ^ 1u : phase;
+            const uint64_t ad = adesc0 + static_cast<uint64_t>(stage) * kStageStep;
+            const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage) * kStageStep;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
+              if (k == kBK / 16 - 1) landed = mbar_test_wait(full_bar(nstage), nphase);
               if (kc + 16 * k < kvalid) {
-                const uint64_t adesc = A_MN ? smem_desc_sw128(sa + 2048u * k, 8192u, 1024u)
-                                            : smem_desc_sw128(sa + 32u * k, 16u, 1024u);
-                const uint64_t bdesc = B_MN ? smem_desc_sw128(sb + 2048u * k, 8192u, 1024u)
-                                            : smem_desc_sw128(sb + 32u * k, 16u, 1024u);
-                tc_mma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
+                tc_mma_bf16(d_tmem, ad + k * kAStep, bd + k * kBStep, idesc, accumulate);
                 accumulate = 1;
               }
             }
             tc_commit(empty_bar(stage));     // frees this smem stage once its MMAs are done
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            stage = nstage;
+            phase = nphase;
           }
         }
         if (!ok) break;
