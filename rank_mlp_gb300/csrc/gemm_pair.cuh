@@ -19,15 +19,15 @@ namespace lgb {
 // Threads of a pair-kernel CTA: producer warp, MMA warp and EPIW epilogue warps.
 constexpr int pair_threads(int epiw) { return 64 + 32 * epiw; }
 
-// Staged epilogue (the activation-derivative GEMM at short K): each epilogue warp owns
-// a ring of kEpiSlots slots in shared memory; a slot holds one chunk (the warp's 32 rows
-// x COLS columns) of g and of u, loaded by TMA, and then the chunk's dg and du, written
-// in place and stored by TMA.
-constexpr int kEpiSlots = 4;
-constexpr int epi_tensor_bytes(int cols) { return 32 * cols * 2; }
-constexpr int epi_slot_bytes(int cols) { return 2 * epi_tensor_bytes(cols); }
+// Staged epilogue (the activation-derivative GEMM): each epilogue warp owns a ring of
+// SLOTS slots in shared memory; a slot holds one chunk (the warp's 32 rows x 16 columns)
+// of g and of u, loaded by TMA, and then the chunk's dg and du, written in place and
+// stored by TMA.
+constexpr int kEpiCols = 16;
+constexpr int kEpiTensorBytes = 32 * kEpiCols * 2;   // 1 KB: one tensor's chunk
+constexpr int kEpiSlotBytes = 2 * kEpiTensorBytes;
 
-// STAGED = 0 (plain epilogues) or the staged epilogue's chunk width in columns.
+// STAGED = 0 (plain epilogues) or the staged epilogue's slots per warp.
 template <int STAGES, int EPIW = 4, int STAGED = 0>
 struct PairCfg {
   static constexpr int BN = 256;                       // accumulator columns per tile
@@ -37,8 +37,8 @@ struct PairCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTxBytes = 2 * kStageBytes;     // both CTAs, counted on the even CTA
   static constexpr int kTmemCols = 512;
-  static constexpr int kEpiBytes = STAGED ? EPIW * kEpiSlots * epi_slot_bytes(STAGED) : 0;
-  static constexpr int kNumBars = 2 * STAGES + 5 + (STAGED ? EPIW * kEpiSlots : 0);
+  static constexpr int kEpiBytes = EPIW * STAGED * kEpiSlotBytes;
+  static constexpr int kNumBars = 2 * STAGES + 5 + EPIW * STAGED;
   static constexpr int kBarBytes = 8 * kNumBars + 16;
   static constexpr int kSmemBytes = STAGES * kStageBytes + kEpiBytes + kBarBytes + 1024;
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
@@ -169,15 +169,15 @@ __device__ __forceinline__ bool sk_piece_arrive(const TcParams& p, const GroupDe
   return true;
 }
 
-// dg = dh u act'(g), du = dh act(g) for COLS columns of one row ("Model Patches and
+// dg = dh u act'(g), du = dh act(g) for 16 columns of one row ("Model Patches and
 // Kernels", activation table: the derivative of the activation, recomputed from the
 // saved g): d the accumulator (dh), gw, uw the saved bf16 pairs; results as bf16 pairs.
-template <int ACT, int COLS>
-__device__ __forceinline__ void act_bwd_cols(const uint32_t (&d)[COLS], const uint32_t (&gw)[COLS / 2],
-                                             const uint32_t (&uw)[COLS / 2], uint32_t (&dg)[COLS / 2],
-                                             uint32_t (&du)[COLS / 2]) {
+template <int ACT>
+__device__ __forceinline__ void act_bwd_cols(const uint32_t (&d)[kEpiCols], const uint32_t (&gw)[kEpiCols / 2],
+                                             const uint32_t (&uw)[kEpiCols / 2], uint32_t (&dg)[kEpiCols / 2],
+                                             uint32_t (&du)[kEpiCols / 2]) {
 #pragma unroll
-  for (int e = 0; e < COLS / 2; ++e) {
+  for (int e = 0; e < kEpiCols / 2; ++e) {
     float a0, ap0, a1, ap1;
     const float g0 = bf16_lo(gw[e]), g1 = bf16_hi(gw[e]);
     const float u0 = bf16_lo(uw[e]), u1 = bf16_hi(uw[e]);
@@ -191,33 +191,34 @@ __device__ __forceinline__ void act_bwd_cols(const uint32_t (&d)[COLS], const ui
 
 // The staged activation-derivative epilogue of one epilogue warp (its TMEM lane
 // quarter q = warp & 3, its share of the tile's columns), for all its units.  The
-// warp walks its chunks of 32 rows x COLS columns in order across tiles; lane 0 keeps
-// the TMA loads of g, u kEpiSlots - 1 chunks ahead (into the slot whose dg, du store
-// has finished reading it), so the next tile's first loads fly while the warp waits
-// for that tile's accumulator.  Each chunk: wait for its slot, read dh from TMEM,
-// compute, write dg, du over g, u, make them visible to TMA and store both.  The
-// accumulator is released as soon as the tile's last chunk has been read from TMEM.
-// Rows past M and columns past N are zero-filled by the loads and dropped by the
-// stores.  The chunk's 32-byte rows sit in the 32-byte swizzle.
-template <int STAGES, int EPIW, int COLS>
+// warp walks its chunks of 32 rows x 16 columns in order across tiles; lane 0 keeps
+// the TMA loads of g, u SLOTS - 1 chunks ahead (into the slot whose dg, du store has
+// finished reading it), so the next tile's first loads fly while the warp waits for
+// that tile's accumulator.  Each chunk: wait for its slot, read dh from TMEM, compute,
+// write dg, du over g, u, make them visible to TMA and store both.  The accumulator is
+// released as soon as the tile's last chunk has been read from TMEM.  Rows past M and
+// columns past N are zero-filled by the loads and dropped by the stores.  The chunk's
+// 32-byte rows sit in the 32-byte swizzle.
+template <int STAGES, int EPIW, int SLOTS>
 __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_smem, uint32_t epi_bar0,
                                                uint32_t tfull0, const uint32_t (&tempty_even)[2], uint32_t tmem_base,
                                                volatile int* abort_flag, uint32_t rank, int pair, int npairs,
                                                int warp) {
-  static_assert(COLS == 16, "chunk width");
+  static_assert(SLOTS == 2 || SLOTS == 4, "ring slots");
+  constexpr int COLS = kEpiCols;
   constexpr int BN = 256;
   constexpr int kParts = EPIW / 4;
   constexpr int kSpan = BN / kParts;                   // columns per warp
   constexpr int kChunks = kSpan / COLS;                // chunks per warp per tile
-  constexpr int kTensorBytes = epi_tensor_bytes(COLS);
-  constexpr int kSlotBytes = epi_slot_bytes(COLS);
+  constexpr int kTensorBytes = kEpiTensorBytes;
+  constexpr int kSlotBytes = kEpiSlotBytes;
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;
   const int widx = warp - 2;
   const int part = widx >> 2;
-  const uint32_t ring = epi_smem + static_cast<uint32_t>(widx) * (kEpiSlots * kSlotBytes);
-  auto slot = [&](uint32_t n) { return ring + (n % kEpiSlots) * kSlotBytes; };
-  auto full = [&](uint32_t n) { return epi_bar0 + 8u * (widx * kEpiSlots + n % kEpiSlots); };
+  const uint32_t ring = epi_smem + static_cast<uint32_t>(widx) * (SLOTS * kSlotBytes);
+  auto slot = [&](uint32_t n) { return ring + (n % SLOTS) * kSlotBytes; };
+  auto full = [&](uint32_t n) { return epi_bar0 + 8u * (widx * SLOTS + n % SLOTS); };
   // this lane's row inside a chunk box and its 16-byte halves (32-byte swizzle: half j
   // of row r sits at j ^ bit 2 of r)
   const uint32_t sw = (static_cast<uint32_t>(lane) >> 2) & 1u;
@@ -246,7 +247,7 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
       more = ahead.next(p, UA);
     }
   };
-  for (int k = 0; k < kEpiSlots - 1 && more; ++k) issue();
+  for (int k = 0; k < SLOTS - 1 && more; ++k) issue();
 
   WorkIter it(p, pair, npairs);
   Unit U;
@@ -266,7 +267,7 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
       uint32_t d[COLS];
       __syncwarp();
       tmem_ld16(tacc + col, d);
-      const bool landed = wait_phase(full(used), (used / kEpiSlots) & 1u, abort_flag, p);
+      const bool landed = wait_phase(full(used), (used / SLOTS) & 1u, abort_flag, p);
       tmem_ld_wait();
       if (c == kChunks - 1) {        // the accumulator is no longer needed: hand it back
         tc_fence_before_sync();
@@ -280,7 +281,7 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
       const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
       const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
       uint32_t dg[8], du[8];
-      act_chunk(p.act, [&](auto tag) { act_bwd_cols<decltype(tag)::value, COLS>(d, gw, uw, dg, du); });
+      act_chunk(p.act, [&](auto tag) { act_bwd_cols<decltype(tag)::value>(d, gw, uw, dg, du); });
       st_shared_v4(s0 + off0, make_uint4(dg[0], dg[1], dg[2], dg[3]));
       st_shared_v4(s0 + off1, make_uint4(dg[4], dg[5], dg[6], dg[7]));
       st_shared_v4(s0 + kTensorBytes + off0, make_uint4(du[0], du[1], du[2], du[3]));
@@ -295,8 +296,9 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
       }
       ++used;
       if (more) {
-        // the next load goes into the slot of chunk used - 1, whose store must have
-        // finished reading it (all stores but the one just committed)
+        // the next load goes into the slot of chunk used + SLOTS - 1 - SLOTS = used - 1,
+        // whose store must have finished reading it (all stores but the one just
+        // committed)
         if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
         issue();
@@ -307,7 +309,7 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
   if (lane == 0) {
     // loads still in flight (after an abort) land before shared memory is released;
     // every store completes before the kernel ends
-    for (uint32_t n = used; n < issued; ++n) wait_phase_drain(full(n), (n / kEpiSlots) & 1u, p);
+    for (uint32_t n = used; n < issued; ++n) wait_phase_drain(full(n), (n / SLOTS) & 1u, p);
     bulk_wait_group_all();
   }
   __syncwarp();
@@ -321,14 +323,14 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
 // ACTB selects the epilogues compiled in: 0 the plain, activation, RoPE and partial
 // epilogues (epilogue_tile); the activation-derivative GEMM (every group EPI_ACT_BWD)
 // has variants of its own: 1 reads g, u and writes dg, du one row per thread
-// (epilogue_act_bwd_rows); 16 moves them through the epilogue warps' shared-memory
-// rings in chunks of 16 columns (staged_act_bwd; whole tiles only).
+// (epilogue_act_bwd_rows); 4 moves them through the epilogue warps' shared-memory
+// rings of 4 slots of 16 columns (staged_act_bwd; whole tiles only).
 template <int STAGES, bool B_MN, int EPIW, int ACTB = 0>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
   static_assert(EPIW == 4 || EPIW == 8, "epilogue warps");
-  static_assert(ACTB == 0 || ACTB == 1 || ACTB == 16, "epilogue selection");
-  constexpr int STAGED = ACTB == 16 ? 16 : 0;
+  static_assert(ACTB == 0 || ACTB == 1 || ACTB == 4, "epilogue selection");
+  constexpr int STAGED = ACTB >= 2 ? ACTB : 0;
   using C = PairCfg<STAGES, EPIW, STAGED>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
@@ -363,7 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
     }
     mbar_init(drain_bar, 1);
     if constexpr (STAGED) {
-      for (int k = 0; k < EPIW * kEpiSlots; ++k) mbar_init(bar0 + 8u * (2 * STAGES + 5 + k), 1);
+      for (int k = 0; k < EPIW * STAGED; ++k) mbar_init(bar0 + 8u * (2 * STAGES + 5 + k), 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -481,12 +483,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
             const uint32_t nphase = stage + 1 == STAGES ? phase ^ 1u : phase;
             const uint64_t ad = adesc0 + static_cast<uint64_t>(stage) * kStageStep;
             const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage) * kStageStep;
+            if (kc + kBK <= kvalid && accumulate) {
+              // a whole k-block after the unit's first: no per-step checks
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              if (k == kBK / 16 - 1) landed = mbar_test_wait(full_bar(nstage), nphase);
-              if (kc + 16 * k < kvalid) {
-                tc_mma_bf16_pair(d_tmem, ad + k * kAStep, bd + k * kBStep, idesc, accumulate);
-                accumulate = 1;
+              for (int k = 0; k < kBK / 16; ++k) {
+                if (k == kBK / 16 - 1) landed = mbar_test_wait(full_bar(nstage), nphase);
+                tc_mma_bf16_pair(d_tmem, ad + k * kAStep, bd + k * kBStep, idesc, 1u);
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k) {
+                if (k == kBK / 16 - 1) landed = mbar_test_wait(full_bar(nstage), nphase);
+                if (kc + 16 * k < kvalid) {
+                  tc_mma_bf16_pair(d_tmem, ad + k * kAStep, bd + k * kBStep, idesc, accumulate);
+                  accumulate = 1;
+                }
               }
             }
             tc_commit_pair_multicast(empty_bar(stage), 0x3);   // frees this stage in both CTAs

@@ -31,7 +31,7 @@ int tc_smem_bytes(int variant) {
     case VP_KK8:
     case VP_KMN: return PairCfg<6>::kSmemBytes;
     case VP_KMN_ACT: return PairCfg<6>::kSmemBytes;
-    case VP_KMN_ACT16: return PairCfg<5, 8, 16>::kSmemBytes;
+    case VP_KMN_ACT16: return PairCfg<5, 8, 4>::kSmemBytes;
     case V64_KK:
     case V64_MNMN: return TcCfg<64, 8>::kSmemBytes;
     default: return TcCfg<128, 6>::kSmemBytes;

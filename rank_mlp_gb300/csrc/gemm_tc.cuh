@@ -727,12 +727,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const uint32_t nphase = stage + 1 == STAGES ? phase ^ 1u : phase;
             const uint64_t ad = adesc0 + static_cast<uint64_t>(stage) * kStageStep;
             const uint64_t bd = bdesc0 + static_cast<uint64_t>(stage) * kStageStep;
+            if (kc + kBK <= kvalid && accumulate) {
+              // a whole k-block after the unit's first: no per-step checks
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              if (k == kBK / 16 - 1) landed = mbar_test_wait(full_bar(nstage), nphase);
-              if (kc + 16 * k < kvalid) {
-                tc_mma_bf16(d_tmem, ad + k * kAStep, bd + k * kBStep, idesc, accumulate);
-                accumulate = 1;
+              for (int k = 0; k < kBK / 16; ++k) {
+                if (k == kBK / 16 - 1) landed = mbar_test_wait(full_bar(nstage), nphase);
+                tc_mma_bf16(d_tmem, ad + k * kAStep, bd + k * kBStep, idesc, 1u);
+              }
+            } else {
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k) {
+                if (k == kBK / 16 - 1) landed = mbar_test_wait(full_bar(nstage), nphase);
+                if (kc + 16 * k < kvalid) {
+                  tc_mma_bf16(d_tmem, ad + k * kAStep, bd + k * kBStep, idesc, accumulate);
+                  accumulate = 1;
+                }
               }
             }
             tc_commit(empty_bar(stage));     // frees this smem stage once its MMAs are done

@@ -31,15 +31,15 @@ enum Variant : int {
   VP_KMN_ACT = 7,   // VP_KMN for the activation-derivative GEMM: saved g, u in and dg, du out
                     // one row per thread (6 stages)
   VP_KMN_ACT16 = 8, // the same for short K: g, u and dg, du through shared memory by TMA
-                    // in 16-column chunks (5 stages leave room for the rings)
+                    // in 16-column chunks, rings of 4 slots (5 stages leave room for them)
   kNumVariants = 9
 };
 
 // An activation-derivative launch whose K is at most this many k-blocks runs
 // VP_KMN_ACT16: its tiles' MMAs are too short to hide the epilogue's traffic, and the
 // staged epilogue keeps more of it in flight.  Longer K needs the sixth stage to keep
-// the MMAs fed (measured: the staged variant at 5 stages, or at 6 with 8-column chunks,
-// was 5-15% slower there than one row per thread).
+// the MMAs fed (measured: the staged variant at 5 stages, or at 6 stages with 8-column
+// chunks or with 2-slot rings, was 3-15% slower there than one row per thread).
 constexpr int kActShortKBlocks = 32;
 
 // A forward pair launch whose longest K is at most this many 64-wide k-blocks runs
