@@ -316,6 +316,17 @@ __device__ __forceinline__ void store_row32_bf16(__nv_bfloat16* dst, const uint3
       *reinterpret_cast<uint4*>(dst + 8 * j) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
 }
 
+// store_row32_bf16 with the whole-sector stores under an L2 cache policy.
+__device__ __forceinline__ void store_row32_bf16_hint(__nv_bfloat16* dst, const uint32_t (&w)[16], int col0, int N,
+                                                      bool v8, uint64_t pol) {
+  if (v8 && col0 + 32 <= N) {
+    st_global_v8_hint(dst, w, pol);
+    st_global_v8_hint(dst + 16, w + 8, pol);
+    return;
+  }
+  store_row32_bf16(dst, w, col0, N, false);
+}
+
 __device__ __forceinline__ bool rows_v8_aligned(const void* base, long long ld) {
   return (ld % 16) == 0 && (reinterpret_cast<uintptr_t>(base) & 31) == 0;
 }
@@ -391,12 +402,14 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
         });
         store_row32_bf16(hout + off, w, col0, G.N, v8);
         if (gout != nullptr) {
+          // g, u are saved for the backward: evict-first keeps the weight tiles in L2
+          const uint64_t pol = l2_evict_first_policy();
 #pragma unroll
           for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(vg[2 * e]), __uint_as_float(vg[2 * e + 1]));
-          store_row32_bf16(gout + off, w, col0, G.N, v8);
+          store_row32_bf16_hint(gout + off, w, col0, G.N, v8, pol);
 #pragma unroll
           for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(vu[2 * e]), __uint_as_float(vu[2 * e + 1]));
-          store_row32_bf16(uout + off, w, col0, G.N, v8);
+          store_row32_bf16_hint(uout + off, w, col0, G.N, v8, pol);
         }
       }
     }
@@ -513,13 +526,14 @@ __device__ __forceinline__ void epilogue_act_bwd_rows(const TcParams& p, const G
   const bool v8 = rows_v8_aligned(dgo, G.ldo) && rows_v8_aligned(duo, G.ldo);
   const int span = BN / nparts, c_lo = part * span, c_hi = c_lo + span;
   const long long rbase = static_cast<long long>(row) * G.ldi + U.tn * BN;
+  const uint64_t pol = l2_evict_first_policy();   // the saved g, u are read for the last time
   auto load_chunk = [&](int c, uint4 (&gw)[4], uint4 (&uw)[4]) {
     const int col0 = U.tn * BN + c;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (row_ok && col0 + 8 * j + 8 <= G.N) {
-        gw[j] = __ldg(reinterpret_cast<const uint4*>(gin + rbase + c + 8 * j));
-        uw[j] = __ldg(reinterpret_cast<const uint4*>(uin + rbase + c + 8 * j));
+        gw[j] = ld_global_nc_v4_hint(gin + rbase + c + 8 * j, pol);
+        uw[j] = ld_global_nc_v4_hint(uin + rbase + c + 8 * j, pol);
       } else {
         gw[j] = make_uint4(0, 0, 0, 0);
         uw[j] = make_uint4(0, 0, 0, 0);

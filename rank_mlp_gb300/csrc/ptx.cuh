@@ -308,6 +308,29 @@ __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
                : "memory");
 }
 
+// An L2 cache policy marking the lines an access touches evict-first: for data a kernel
+// streams once and nothing reads soon after (saved activations going to the backward,
+// saved activations read for the last time), so that they leave L2 before the operand
+// tiles the kernel reads again.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// st_global_v8 with an L2 cache policy.
+__device__ __forceinline__ void st_global_v8_hint(void* dst, const uint32_t* w, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(dst),
+               "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "l"(pol)
+               : "memory");
+}
+// 16-byte read-only load with an L2 cache policy.
+__device__ __forceinline__ uint4 ld_global_nc_v4_hint(const void* src, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(src), "l"(pol));
+  return r;
+}
 // 16-byte load cached in L2 only (data another CTA wrote during this launch).
 __device__ __forceinline__ uint4 ld_global_cg_v4(const void* src) {
   uint4 r;
