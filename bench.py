@@ -108,32 +108,45 @@ def cuda_timer(torch, stream):
 
 # ---------------------------------------------------------------------------- clocks
 
-CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+CLOCK_PERIOD_MS = 20
 
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every CLOCK_PERIOD_MS while the timed region runs.  start()
+    returns once the first sample is written (so sampling covers the region from its
+    first step); stop() keeps the samples stamped inside [start, stop]."""
 
     def __init__(self):
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader",
-                                          "-lms", "200", "-f", self.path],
+                                          "-lms", str(CLOCK_PERIOD_MS), "-f", self.path],
                                          stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        deadline = time.time() + 10.0
+        while time.time() < deadline and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
+        self.t0 = time.time()
 
     def stop(self):
         if self.proc is None:
             return None
+        self.t1 = time.time()
+        time.sleep(2e-3 * CLOCK_PERIOD_MS)     # the sample that covers the region's end
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -143,18 +156,37 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
+                if len(parts) >= 10:
                     rows.append(parts)
         os.unlink(self.path)
-        return parse_clock_rows(rows)
+        return parse_clock_rows(rows, self.t0, self.t1, CLOCK_PERIOD_MS * 1e-3)
 
 
-def parse_clock_rows(rows):
+def _stamp(s):
+    import datetime
+    for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+        try:
+            return datetime.datetime.strptime(s, fmt).timestamp()
+        except ValueError:
+            pass
+    return None
+
+
+def parse_clock_rows(rows, t0=None, t1=None, slack=0.0):
+    """Clock summary of nvidia-smi rows (CLOCK_FIELDS order): the rows stamped within
+    [t0 - slack, t1 + slack] when the stamps allow (else all rows); median SM clock
+    under load (samples above half the peak power seen), the reasons seen active."""
     def num(s):
         try:
             return float(s.split()[0])
         except (ValueError, IndexError):
             return None
+    window = "whole sampling"
+    if t0 is not None and t1 is not None:
+        inside = [r for r in rows if (lambda t: t is not None and t0 - slack <= t <= t1 + slack)(_stamp(r[0]))]
+        if inside:
+            rows, window = inside, "timed region"
+    rows = [r[1:] for r in rows]
     sm = [num(r[1]) for r in rows if num(r[1]) is not None]
     mx = [num(r[2]) for r in rows if num(r[2]) is not None]
     pw = [num(r[3]) for r in rows if num(r[3]) is not None]
@@ -165,7 +197,8 @@ def parse_clock_rows(rows):
     loaded = [num(r[1]) for r in rows if pw and num(r[3]) is not None and num(r[3]) >= 0.5 * pmax] or sm
     reasons = sorted({REASONS[j] for r in rows for j in range(4) if r[5 + j].lower() == "active"})
     return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx) if mx else None,
-            "reasons": reasons, "samples": len(rows), "power_w_max": pmax}
+            "sm_mhz_min": min(loaded), "reasons": reasons, "samples": len(rows), "power_w_max": pmax,
+            "window": window, "period_ms": CLOCK_PERIOD_MS}
 
 
 # ---------------------------------------------------------------------------- flops

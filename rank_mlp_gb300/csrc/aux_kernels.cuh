@@ -50,6 +50,9 @@ struct RedOut {
   long long ld;
   int trans;          // 0: dst[m * ld + c];  1: dst[c * ld + m]
   long long split_stride;  // per-split outputs: elements between consecutive splits' results
+  int vec4;           // 1: four consecutive columns per thread (16-byte slab loads; host checks the
+                      // alignment: col0, ncols multiples of 4, and for trans 0 an 8-byte-aligned
+                      // destination row of 4-column groups)
 };
 
 struct RedParams {

@@ -8,36 +8,39 @@
 
 namespace lgb {
 
-// Eight consecutive destination elements per thread (destination widths are multiples
-// of 8 and rows start 16-byte aligned): one index division and one 16-byte store each.
+// Eight consecutive destination elements of one row per thread (destination widths
+// are multiples of 8 and rows start 16-byte aligned): each block that overlaps them
+// contributes a run of columns read with one stride, the rest stay zero; one 16-byte
+// store.  Index arithmetic is 32-bit (the host keeps rows * cols below 2^31).
 __global__ void __launch_bounds__(256) pack_kernel(const __grid_constant__ PackParams p) {
   pdl_wait();
   pdl_launch_dependents();
   const PackJob& J = p.job[blockIdx.y];
-  const long long cols8 = J.cols / 8;
-  const long long total = static_cast<long long>(J.rows) * cols8;
-  for (long long idx = blockIdx.x * 256LL + threadIdx.x; idx < total; idx += 256LL * gridDim.x) {
-    const int a = static_cast<int>(idx / cols8);
-    const int b0 = static_cast<int>(idx - static_cast<long long>(a) * cols8) * 8;
+  const int cols8 = J.cols / 8;
+  const int total = J.rows * cols8;
+  for (int idx = blockIdx.x * 256 + threadIdx.x; idx < total; idx += 256 * gridDim.x) {
+    const int a = idx / cols8;
+    const int b0 = (idx - a * cols8) * 8;
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+    for (int k = 0; k < J.nblk; ++k) {
+      const PackBlock& B = J.blk[k];
+      const int i = a - B.ro, j0 = b0 - B.co;
+      if (i < 0 || i >= B.R || j0 + 8 <= 0 || j0 >= B.C) continue;
+      const long long step = B.trans ? B.lds : 1;
+      const __nv_bfloat16* src = B.src + (B.trans ? static_cast<long long>(i) : static_cast<long long>(i) * B.lds);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int j = j0 + e;
+        if (j >= 0 && j < B.C) v[e] = B.scale * __bfloat162float(src[j * step]);
+      }
+    }
     uint32_t w[4];
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      float v[2] = {0.0f, 0.0f};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int b = b0 + e + h;
-        for (int k = 0; k < J.nblk; ++k) {
-          const PackBlock& B = J.blk[k];
-          const int i = a - B.ro, j = b - B.co;
-          if (i >= 0 && i < B.R && j >= 0 && j < B.C) {
-            const long long s = B.trans ? static_cast<long long>(j) * B.lds + i
-                                        : static_cast<long long>(i) * B.lds + j;
-            v[h] = B.scale * __bfloat162float(B.src[s]);
-          }
-        }
-      }
-      __nv_bfloat162 pr = __floats2bfloat162_rn(v[0], v[1]);
-      w[e / 2] = *reinterpret_cast<uint32_t*>(&pr);
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 pr = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+      w[e] = *reinterpret_cast<uint32_t*>(&pr);
     }
     *reinterpret_cast<uint4*>(J.dst + static_cast<long long>(a) * J.cols + b0) = make_uint4(w[0], w[1], w[2], w[3]);
   }
@@ -49,6 +52,54 @@ __global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ Red
   const RedOut& O = p.out[blockIdx.y];
   const long long total = static_cast<long long>(O.rows) * O.ncols;
   const long long slab = O.rows_pad * O.width;
+  if (O.vec4 && !O.per_split) {
+    // Four columns per thread: the same sums, in the same order, as the scalar loop
+    // below.  trans 0: threads take consecutive 4-column groups of a row (16-byte loads,
+    // 8-byte stores); trans 1: consecutive rows of one group (each column's stores
+    // are consecutive in the destination).
+    const int groups = O.ncols / 4;
+    const int n = O.rows * groups;
+    for (int idx = blockIdx.x * 256 + threadIdx.x; idx < n; idx += 256 * gridDim.x) {
+      int m, g;
+      if (O.trans) {
+        g = idx / O.rows;
+        m = idx - g * O.rows;
+      } else {
+        m = idx / groups;
+        g = idx - m * groups;
+      }
+      const float* src = O.part + static_cast<long long>(m) * O.width + O.col0 + 4 * g;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+      for (int k = 0; k < O.splits; ++k) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src + k * slab));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      const __nv_bfloat16 b0 = __float2bfloat16_rn(O.scale * acc.x), b1 = __float2bfloat16_rn(O.scale * acc.y);
+      const __nv_bfloat16 b2 = __float2bfloat16_rn(O.scale * acc.z), b3 = __float2bfloat16_rn(O.scale * acc.w);
+      if (O.trans) {
+        __nv_bfloat16* d = O.dst + static_cast<long long>(4 * g) * O.ld + m;
+        d[0] = b0;
+        d[O.ld] = b1;
+        d[2 * O.ld] = b2;
+        d[3 * O.ld] = b3;
+      } else {
+        __nv_bfloat162 lo, hi;
+        lo.x = b0;
+        lo.y = b1;
+        hi.x = b2;
+        hi.y = b3;
+        uint2 w;
+        w.x = *reinterpret_cast<uint32_t*>(&lo);
+        w.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(O.dst + static_cast<long long>(m) * O.ld + 4 * g) = w;
+      }
+    }
+    return;
+  }
   for (long long idx = blockIdx.x * 256LL + threadIdx.x; idx < total; idx += 256LL * gridDim.x) {
     int m, c;
     if (O.trans) {

@@ -212,6 +212,7 @@ lora_status_t launch_pack(const PackParams& p, cudaStream_t st) {
   int64_t most = 1;
   for (int j = 0; j < p.njob; ++j) {
     const int64_t n = static_cast<int64_t>(p.job[j].rows) * (p.job[j].cols / 8);   // 8 elements per thread
+    if (static_cast<int64_t>(p.job[j].rows) * p.job[j].cols >= (int64_t(1) << 31)) return LORA_ERR_UNSUPPORTED;
     most = n > most ? n : most;
   }
   int64_t gx = ceil_div(most, 256);
@@ -234,11 +235,16 @@ lora_status_t launch_norms(const NormParams& p, int examples, cudaStream_t st) {
   return LORA_OK;
 }
 
-lora_status_t launch_reduce(const RedParams& p, cudaStream_t st) {
-  if (p.nout == 0) return LORA_OK;
+lora_status_t launch_reduce(const RedParams& plan, cudaStream_t st) {
+  if (plan.nout == 0) return LORA_OK;
+  RedParams p = plan;
   int64_t most = 1;
   for (int j = 0; j < p.nout; ++j) {
-    const int64_t n = static_cast<int64_t>(p.out[j].rows) * p.out[j].ncols;
+    RedOut& o = p.out[j];
+    const int64_t elems = static_cast<int64_t>(o.rows) * o.ncols;
+    o.vec4 = !o.per_split && o.ncols % 4 == 0 && o.col0 % 4 == 0 && o.width % 4 == 0 && elems < (int64_t(1) << 31) &&
+             (o.trans || (o.ld % 4 == 0 && aligned(o.dst, 8)));
+    const int64_t n = o.vec4 ? elems / 4 : elems;
     most = n > most ? n : most;
   }
   int64_t gx = ceil_div(most, 256);

@@ -62,16 +62,25 @@ def test_two_gloo_ranks_report_the_slowest_time():
 
 def test_clock_rows_parse():
     import bench
-    rows = [["0", "1965 MHz", "2070 MHz", "1200.5 W", "0x0", "Not Active", "Not Active", "Not Active",
-             "Active"],
-            ["0", "1980 MHz", "2070 MHz", "1250.0 W", "0x0", "Not Active", "Not Active", "Not Active",
-             "Not Active"],
-            ["0", "345 MHz", "2070 MHz", "150.0 W", "0x0", "Not Active", "Not Active", "Not Active",
-             "Not Active"]]
+    rows = [["2026/12/03 07:30:11.100", "0", "1965 MHz", "2070 MHz", "1200.5 W", "0x0", "Not Active",
+             "Not Active", "Not Active", "Active"],
+            ["2026/12/03 07:30:11.120", "0", "1980 MHz", "2070 MHz", "1250.0 W", "0x0", "Not Active",
+             "Not Active", "Not Active", "Not Active"],
+            ["2026/12/03 07:30:11.140", "0", "345 MHz", "2070 MHz", "150.0 W", "0x0", "Not Active",
+             "Not Active", "Not Active", "Not Active"]]
     c = bench.parse_clock_rows(rows)
     assert c["sm_mhz"] == pytest.approx(1972.5)       # idle sample left out
     assert c["sm_max_mhz"] == 2070
     assert c["reasons"] == ["sw_power_cap"]
+    assert c["samples"] == 3 and c["window"] == "whole sampling"
+    # only the samples stamped inside the timed region (plus the sampling period) count
+    t = bench._stamp("2026/12/03 07:30:11.115")
+    c = bench.parse_clock_rows(rows, t, t + 0.02, 0.0)
+    assert c["samples"] == 1 and c["sm_mhz"] == 1980 and c["reasons"] == []
+    assert c["window"] == "timed region"
+    # no stamp inside the region: every row counts
+    c = bench.parse_clock_rows(rows, t + 100.0, t + 101.0, 0.02)
+    assert c["samples"] == 3 and c["window"] == "whole sampling"
 
 
 def test_kernel_flops_sum_to_the_block_minus_rank_work():
