@@ -55,8 +55,9 @@ struct ProjSeg {
   const void* P;
   int64_t K;
 };
+// dst_t (optional): the same result transposed, [kf x ldt] (ldt >= M, a multiple of 8).
 lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int nseg, void* dst, float* part,
-                              unsigned* status, cudaStream_t st);
+                              unsigned* status, cudaStream_t st, void* dst_t = nullptr, int64_t ldt = 0);
 // f32 slab elements of a rank-r projection over ktotal_blocks 64-wide k-blocks.
 int64_t rank_projection_part(int64_t M, int kf, int64_t ktotal_blocks);
 
@@ -87,6 +88,24 @@ lora_status_t defer_flush(Deferred& d, cudaStream_t st);
 // reads nothing the previous kernel writes and writes nothing it reads (pdl_late).
 lora_status_t token_grads(int64_t M, int r, int kf, float s, const GradJob* jobs, int njobs, Deferred& defer,
                           unsigned* status, cudaStream_t st, int64_t n_ex = 0, bool late = false);
+
+// One pass over token-major gradients Q_p that gives both of their rank-r products
+// (rank_dual.cuh): V[M x kf] (columns [0, nv), nv = the slots' extent rounded to 16)
+// = sum_p Q_p Bt_p^T, and dB_p = s Q_p^T T_p[:, slot_p] written as [F_p x r].  T^T is
+// the transposed rank-r operand [kf x ldt].  V is summed from its f32 slab (vslab) at
+// once; the dB sums are left to `defer`.  Only for r <= 16 (dual_supported).
+struct DualJob {
+  const void* Q;      // [M x F] token-major
+  int64_t F;
+  const void* Bt;     // [kf x F] packed: this product's rows of B^T in its V slots, zero elsewhere
+  int t_row;          // first row of this product's slot in T^T
+  void* dB;           // [F x r]
+};
+inline bool dual_supported(int r, int kf) { return r <= 16 && kf >= 16; }
+// f32 elements of the V slab and of the dB slabs (sum over the jobs) of one pass.
+void dual_slab_elems(int64_t M, int r, const int64_t* F, int njobs, int64_t& v_elems, int64_t& db_elems);
+lora_status_t rank_dual(int64_t M, int r, int kf, float s, const DualJob* jobs, int njobs, const void* Tt,
+                        int64_t ldt, void* V, float* vslab, Deferred& defer, unsigned* status, cudaStream_t st);
 
 lora_status_t launch_rope(const RopeParams& p, cudaStream_t st);
 

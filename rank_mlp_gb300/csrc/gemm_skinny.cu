@@ -2,6 +2,7 @@
 // x A^T, and the reductions over tokens that give dA and dB).  HBM-bound; deep rings.
 #include "gemm_pair.cuh"
 #include "host.cuh"
+#include "rank_dual_impl.cuh"
 
 namespace lgb {
 
@@ -23,6 +24,13 @@ cudaError_t launch_tc_skinny(int variant, const TcParams& p, int grid, cudaStrea
     case V128_MNMN: return launch_one<128, 6, true, true>(p, grid, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_rank_dual(const DualParams& p, int grid, cudaStream_t st) {
+  static std::atomic<unsigned long long> configured{0};
+  const cudaError_t e = ensure_smem_limit(rank_dual_kernel, kDualSmemBytes, configured);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(rank_dual_kernel, dim3(grid), dim3(kThreads), kDualSmemBytes, st, p);
 }
 
 int tc_smem_bytes(int variant) {

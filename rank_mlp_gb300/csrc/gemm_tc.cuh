@@ -62,6 +62,7 @@ struct GroupDesc {
   const void* in1;
   long long ldo, ldi;
   float* part;               // EPI_PARTIAL: [splits][tiles_m*128][tiles_n*BN] f32
+  long long ldt;             // EPI_STORE with out1: out1 receives the tile transposed, [N x ldt]
   int emap[4];               // EPI_ACT_BWD on the staged variant: maps of g, u (in) and dg, du (out)
 };
 
@@ -370,6 +371,17 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
           for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
         }
         store_row32_bf16(out + static_cast<long long>(row) * G.ldo + col0, w, col0, G.N, v8);
+        if (G.out1 != nullptr) {
+          // the same values, transposed (a warp's 32 rows are consecutive there)
+          __nv_bfloat16* ot = static_cast<__nv_bfloat16*>(G.out1) + row;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = col0 + 2 * e;
+            if (c < G.N) ot[static_cast<long long>(c) * G.ldt] = __ushort_as_bfloat16(static_cast<unsigned short>(w[e]));
+            if (c + 1 < G.N)
+              ot[static_cast<long long>(c + 1) * G.ldt] = __ushort_as_bfloat16(static_cast<unsigned short>(w[e] >> 16));
+          }
+        }
       }
     }
   } else if (G.epi == EPI_ACT_FWD) {

@@ -15,6 +15,7 @@
 #include "lora_gb300.h"
 #include "aux_kernels.cuh"
 #include "gemm_tc.cuh"
+#include "rank_dual.cuh"
 
 namespace lgb {
 

@@ -296,7 +296,7 @@ PackJob& pack_job(PackParams& P, void* dst, int64_t rows, int64_t cols) {
 }
 
 lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int nseg, void* dst, float* part,
-                                     unsigned* status, cudaStream_t st) {
+                                     unsigned* status, cudaStream_t st, void* dst_t, int64_t ldt) {
   const int variant = skinny_kk(kf);
   GemmPlan g(variant);
   int64_t kb = 0;
@@ -315,6 +315,8 @@ lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int nseg, 
   } else {
     G.out0 = dst;
     G.ldo = kf;
+    G.out1 = dst_t;
+    G.ldt = ldt;
   }
   g.p.status = status;
   g.finish();
@@ -336,6 +338,13 @@ lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int nseg, 
     o.ncols = kf;
     o.ld = kf;
     o.trans = 0;
+    if (dst_t != nullptr) {       // the same sums, transposed
+      r.out[1] = o;
+      r.out[1].dst = static_cast<bf16*>(dst_t);
+      r.out[1].ld = ldt;
+      r.out[1].trans = 1;
+      r.nout = 2;
+    }
     LGB_TRY(launch_reduce(r, st));
   }
   return LORA_OK;
@@ -447,6 +456,129 @@ lora_status_t token_grads(int64_t M, int r, int kf, float s, const GradJob* jobs
   return LORA_OK;
 }
 
+
+// ---------------------------------------------------------------- one-pass rank-r products
+
+// The split of a one-pass launch into gt token ranges x gf feature ranges (one CTA
+// each): every range non-empty, at most kDualMaxBlocks feature blocks a CTA (its TMEM),
+// gt * gf within kDualMaxCtas (the SMs of a GB300; a fixed number, so that workspace
+// sizes do not depend on the device).  Cost, in units of one CTA's 128 x 128 tile: the
+// busiest CTA's tiles plus the partial sums' bytes (written and read back) spread over
+// the CTAs.
+struct DualPlan {
+  int gt = 0, gf = 0, nv = 0;
+};
+static DualPlan dual_plan(int64_t M, int r, const int64_t* F, int njobs) {
+  DualPlan P;
+  int slots = 0;
+  for (int j = 0; j < njobs; ++j) slots = r * (j + 1);
+  P.nv = static_cast<int>(round_up(slots, 16));
+  const int64_t tm = ceil_div(M, 128);
+  int64_t kb = 0, frows = 0;
+  for (int j = 0; j < njobs; ++j) {
+    kb += ceil_div(F[j], 128);
+    frows += ceil_div(F[j], 128) * 128;
+  }
+  constexpr int sms = kDualMaxCtas;
+  double best = 1e30;
+  for (int64_t gf = ceil_div(kb, kDualMaxBlocks); gf <= kb && gf <= sms; ++gf) {
+    const int64_t gt = tm < sms / gf ? tm : sms / gf;
+    if (gt < 1) break;
+    const double tiles = static_cast<double>(ceil_div(tm, gt) * ceil_div(kb, gf));
+    const double bytes = 2.0 * 4.0 * (static_cast<double>(gf) * tm * 128 * P.nv + static_cast<double>(gt) * frows * kDualNRMax);
+    const double cost = tiles + bytes / (static_cast<double>(kDualQBytes) * gt * gf);
+    if (cost < best) {
+      best = cost;
+      P.gt = static_cast<int>(gt);
+      P.gf = static_cast<int>(gf);
+    }
+  }
+  return P;
+}
+
+void dual_slab_elems(int64_t M, int r, const int64_t* F, int njobs, int64_t& v_elems, int64_t& db_elems) {
+  const DualPlan P = dual_plan(M, r, F, njobs);
+  v_elems = round_up(static_cast<int64_t>(P.gf) * ceil_div(M, 128) * 128 * P.nv, 64);
+  db_elems = 0;
+  for (int j = 0; j < njobs; ++j) db_elems += round_up(static_cast<int64_t>(P.gt) * ceil_div(F[j], 128) * 128 * kDualNRMax, 64);
+}
+
+lora_status_t rank_dual(int64_t M, int r, int kf, float s, const DualJob* jobs, int njobs, const void* Tt,
+                        int64_t ldt, void* V, float* vslab, Deferred& defer, unsigned* status, cudaStream_t st) {
+  if (M == 0) return LORA_OK;
+  if (njobs < 1 || njobs > kDualMaxProducts || !dual_supported(r, kf)) return LORA_ERR_UNSUPPORTED;
+  int64_t F[kDualMaxProducts];
+  for (int j = 0; j < njobs; ++j) F[j] = jobs[j].F;
+  const DualPlan P = dual_plan(M, r, F, njobs);
+  if (P.gt < 1 || P.gf < 1 || P.nv > kDualNVMax || P.nv > kf) return LORA_ERR_UNSUPPORTED;
+  DualParams d;
+  std::memset(static_cast<void*>(&d), 0, sizeof(d));
+  d.nprod = njobs;
+  d.tiles_m = static_cast<int>(ceil_div(M, 128));
+  d.nv = P.nv;
+  d.nr = kDualNRMax;
+  d.gt = P.gt;
+  d.gf = P.gf;
+  d.v_part = vslab;
+  d.status = status;
+  d.timeout_ns = g_timeout_ns.load();
+  float* cur = defer.cursor;
+  for (int j = 0; j < njobs; ++j) {
+    DualProduct& D = d.prod[j];
+    D.nkb = static_cast<int>(ceil_div(F[j], 128));
+    D.t_row = jobs[j].t_row;
+    D.q_map = 3 * j;
+    D.b_map = 3 * j + 1;
+    D.t_map = 3 * j + 2;
+    if (!encode_map(&d.maps[D.q_map], jobs[j].Q, F[j], M, F[j], 64, 128, 128) ||
+        !encode_map(&d.maps[D.b_map], jobs[j].Bt, F[j], kf, F[j], 64, P.nv, 128) ||
+        !encode_map(&d.maps[D.t_map], Tt, M, kf, ldt, 64, kDualNRMax, 128))
+      return LORA_ERR_CUDA;
+    D.db_part = cur;
+    cur += round_up(static_cast<int64_t>(P.gt) * D.nkb * 128 * kDualNRMax, 64);
+    d.kb_total += D.nkb;
+  }
+  defer.cursor = cur;
+  const int slot = trace_begin(LORA_KIND_RANK_GRAD, st);
+  cudaError_t e = launch_rank_dual(d, P.gt * P.gf, st);
+  trace_end(slot, st);
+  if (e != cudaSuccess) return LORA_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  // V now (the next GEMM reads it); the dB sums with the call's other reductions
+  RedParams rv;
+  std::memset(static_cast<void*>(&rv), 0, sizeof(rv));
+  rv.nout = 1;
+  RedOut& o = rv.out[0];
+  o.part = vslab;
+  o.rows = static_cast<int>(M);
+  o.rows_pad = d.tiles_m * 128;
+  o.width = P.nv;
+  o.splits = P.gf;
+  o.scale = 1.0f;
+  o.dst = static_cast<bf16*>(V);
+  o.col0 = 0;
+  o.ncols = P.nv;
+  o.ld = kf;
+  o.trans = 0;
+  LGB_TRY(launch_reduce(rv, st));
+  for (int j = 0; j < njobs; ++j) {
+    if (defer.rp.nout >= kMaxRedOuts) return LORA_ERR_UNSUPPORTED;   // not reached: <= 8 per call
+    RedOut& b = defer.rp.out[defer.rp.nout++];
+    b.part = d.prod[j].db_part;
+    b.rows = static_cast<int>(F[j]);
+    b.rows_pad = static_cast<long long>(d.prod[j].nkb) * 128;
+    b.width = kDualNRMax;
+    b.splits = P.gt;
+    b.per_split = 0;
+    b.scale = s;
+    b.dst = static_cast<bf16*>(jobs[j].dB);
+    b.col0 = 0;
+    b.ncols = r;
+    b.ld = r;
+    b.trans = 0;
+  }
+  return LORA_OK;
+}
 
 lora_status_t check_common(int64_t M, int r, float s) {
   if (M < 0 || r < 1 || !std::isfinite(s)) return LORA_ERR_INVALID_ARG;

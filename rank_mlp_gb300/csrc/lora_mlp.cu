@@ -15,17 +15,35 @@ struct MlpLayout {
   size_t ws_fwd, ws_bwd, saved;
   // saved blob offsets
   size_t off_g, off_u, off_h, off_tgu, off_td;
+  size_t off_tgut;   // T_gu transposed [kfg x ldt] (the backward's one pass over dg, du)
+  int64_t ldt;
 };
 
 // Backward scratch: the rank-r projections' split-K slabs (reused), then the four token
 // reductions' slabs (kept until the call's final reduce).
-static int64_t mlp_bwd_rank_part(int64_t M, int64_t h, int64_t i, int kfd, int kfg) {
-  return imax(rank_projection_part(M, kfd, ceil_div(h, kBK)), rank_projection_part(M, kfg, 2 * ceil_div(i, kBK)));
+// With one pass over dg, du (dual_supported): the V slab shares the projections' region
+// and the dB_g, dB_u slabs join the others.
+static bool mlp_dual(int r, int kfg, int64_t n_ex) { return n_ex == 0 && dual_supported(r, kfg); }
+static int64_t mlp_bwd_rank_part(int64_t M, int64_t h, int64_t i, int r, int kfd, int kfg, int64_t n_ex) {
+  int64_t p = imax(rank_projection_part(M, kfd, ceil_div(h, kBK)), rank_projection_part(M, kfg, 2 * ceil_div(i, kBK)));
+  if (mlp_dual(r, kfg, n_ex)) {
+    const int64_t F[2] = {i, i};
+    int64_t v = 0, db = 0;
+    dual_slab_elems(M, r, F, 2, v, db);
+    p = imax(p, v);
+  }
+  return p;
 }
-static int64_t mlp_bwd_slabs(int64_t M, int64_t h, int64_t i, int kfd, int kfg, int64_t n_ex) {
+static int64_t mlp_bwd_slabs(int64_t M, int64_t h, int64_t i, int r, int kfd, int kfg, int64_t n_ex) {
   const int64_t f2[2] = {i, i};
-  return token_grad_part(M, kfd, &h, 1, n_ex) + token_grad_part(M, kfd, &i, 1, n_ex) +
-         token_grad_part(M, kfg, f2, 2, n_ex) + token_grad_part(M, kfg, &h, 1, n_ex);
+  int64_t n = token_grad_part(M, kfd, &h, 1, n_ex) + token_grad_part(M, kfd, &i, 1, n_ex) +
+              token_grad_part(M, kfg, f2, 2, n_ex) + token_grad_part(M, kfg, &h, 1, n_ex);
+  if (mlp_dual(r, kfg, n_ex)) {
+    int64_t v = 0, db = 0;
+    dual_slab_elems(M, r, f2, 2, v, db);
+    n += db;
+  }
+  return n;
 }
 
 // Largest pair-GEMM tile counts of the forward (gate/up, down) and backward (act', dx).
@@ -69,8 +87,8 @@ MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r, int64_t n_ex = 0) {
     c.take_n<bf16>(M * i);       // dg
     c.take_n<bf16>(M * i);       // du
     c.take_n<bf16>(M * kfg);     // V
-    c.take_n<float>(mlp_bwd_rank_part(M, h, i, kfd, kfg));
-    c.take_n<float>(mlp_bwd_slabs(M, h, i, kfd, kfg, n_ex));
+    c.take_n<float>(mlp_bwd_rank_part(M, h, i, r, kfd, kfg, n_ex));
+    c.take_n<float>(mlp_bwd_slabs(M, h, i, r, kfd, kfg, n_ex));
     carve_sk(c, mlp_bwd_tiles(M, h, i));
     L.ws_bwd = c.off;
   }
@@ -81,6 +99,8 @@ MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r, int64_t n_ex = 0) {
     L.off_h = c.offset_of(sizeof(bf16) * M * i);
     L.off_tgu = c.offset_of(sizeof(bf16) * M * kfg);
     L.off_td = c.offset_of(sizeof(bf16) * M * kfd);
+    L.ldt = round_up(M, 8);
+    L.off_tgut = c.offset_of(sizeof(bf16) * kfg * L.ldt);
     L.saved = c.off;
   }
   return L;
@@ -140,8 +160,10 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
   const SkRegion sk = carve_sk(c, mlp_fwd_tiles(M, h, i));
   bf16* gbuf = nullptr;
   bf16* ubuf = nullptr;
+  bf16* tgut = nullptr;
   if (saved) {
     uint8_t* sv = static_cast<uint8_t*>(saved);
+    tgut = reinterpret_cast<bf16*>(sv + L.off_tgut);
     gbuf = reinterpret_cast<bf16*>(sv + L.off_g);
     ubuf = reinterpret_cast<bf16*>(sv + L.off_u);
     hbuf = reinterpret_cast<bf16*>(sv + L.off_h);
@@ -162,9 +184,9 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
   pack_block(pack_job(pk, bf_d, h, kfd), down.B, r, 0, 0, static_cast<int>(h), r, 0, s);
   LGB_TRY(launch_pack(pk, stream));
 
-  // T_gu = x [A_g; A_u]^T
+  // T_gu = x [A_g; A_u]^T (saved also transposed for the backward's pass over dg, du)
   const ProjSeg p1 = {x, acat_gu, h};
-  LGB_TRY(rank_projection(M, kfg, &p1, 1, tgu, part, status, stream));
+  LGB_TRY(rank_projection(M, kfg, &p1, 1, tgu, part, status, stream, tgut, L.ldt));
 
   // [g | u] = [x | T_gu] [W_g | s B_g ; W_u | s B_u]^T, gate and up halves per tile; h = act(g) u
   {
@@ -243,6 +265,8 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   const bf16* hsv = reinterpret_cast<const bf16*>(sv + L.off_h);
   const bf16* tgu = reinterpret_cast<const bf16*>(sv + L.off_tgu);
   const bf16* td = reinterpret_cast<const bf16*>(sv + L.off_td);
+  const bf16* tgut = reinterpret_cast<const bf16*>(sv + L.off_tgut);
+  const bool dual = mlp_dual(r, kfg, n_ex);
 
   Carve c(ws);
   unsigned* status = static_cast<unsigned*>(c.take(kWsHeader));
@@ -255,9 +279,9 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   bf16* dg = c.take_n<bf16>(M * i);
   bf16* du = c.take_n<bf16>(M * i);
   bf16* V = c.take_n<bf16>(M * kfg);
-  float* part = c.take_n<float>(mlp_bwd_rank_part(M, h, i, kfd, kfg));
+  float* part = c.take_n<float>(mlp_bwd_rank_part(M, h, i, r, kfd, kfg, n_ex));
   Deferred dr;
-  defer_init(dr, c.take_n<float>(mlp_bwd_slabs(M, h, i, kfd, kfg, n_ex)));
+  defer_init(dr, c.take_n<float>(mlp_bwd_slabs(M, h, i, r, kfd, kfg, n_ex)));
   const SkRegion sk = carve_sk(c, mlp_bwd_tiles(M, h, i));
 
   PackParams pk;
@@ -313,9 +337,15 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   const GradJob j1[2] = {{dy, h, 0, d_down.dB, 0, td}, {hsv, i, 0, d_down.dA, 1, ud}};
   LGB_TRY(token_grads(M, r, kfd, s, j1, 2, dr, status, stream, n_ex, true));
 
-  // V = [dg B_g | du B_u]
-  const ProjSeg p3[2] = {{dg, bt_g, i}, {du, bt_u, i}};
-  LGB_TRY(rank_projection(M, kfg, p3, 2, V, part, status, stream));
+  if (dual) {
+    // V = [dg B_g | du B_u], dB_g = s dg^T T_g and dB_u = s du^T T_u in one pass over dg, du
+    const DualJob jd[2] = {{dg, i, bt_g, 0, d_gate.dB}, {du, i, bt_u, r, d_up.dB}};
+    LGB_TRY(rank_dual(M, r, kfg, s, jd, 2, tgut, L.ldt, V, part, dr, status, stream));
+  } else {
+    // V = [dg B_g | du B_u]
+    const ProjSeg p3[2] = {{dg, bt_g, i}, {du, bt_u, i}};
+    LGB_TRY(rank_projection(M, kfg, p3, 2, V, part, status, stream));
+  }
 
 
   // dx = [dg | du | V] [W_g ; W_u ; s A_g ; s A_u]
@@ -334,12 +364,12 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
   }
 
-  // dB_g = s dg^T T_g, dB_u = s du^T T_u and dA_g = s V_g^T x, dA_u = s V_u^T x (one
-  // launch) read nothing the dx GEMM writes: they start on the SMs its last wave leaves
-  // idle
-  const GradJob j3[4] = {{dg, i, 0, d_gate.dB, 0, tgu}, {du, i, r, d_up.dB, 0, tgu},
-                         {x, h, 0, d_gate.dA, 1, V}, {x, h, r, d_up.dA, 1, V}};
-  LGB_TRY(token_grads(M, r, kfg, s, j3, 4, dr, status, stream, n_ex, true));
+  // dA_g = s V_g^T x, dA_u = s V_u^T x (and dB_g = s dg^T T_g, dB_u = s du^T T_u when
+  // the pass over dg, du has not made them) in one launch: they read nothing the dx GEMM
+  // writes and start on the SMs its last wave leaves idle
+  const GradJob j3[4] = {{x, h, 0, d_gate.dA, 1, V}, {x, h, r, d_up.dA, 1, V},
+                         {dg, i, 0, d_gate.dB, 0, tgu}, {du, i, r, d_up.dB, 0, tgu}};
+  LGB_TRY(token_grads(M, r, kfg, s, j3, dual ? 2 : 4, dr, status, stream, n_ex, true));
   LGB_TRY(defer_flush(dr, stream));
   if (n_ex > 0 && sq_norms != nullptr) {
     NormParams np;

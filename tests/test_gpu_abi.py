@@ -149,11 +149,13 @@ def _kinds(lib, fn):
 def test_launches_per_call(lib):
     """The launch structure of each call.  MLP forward: pack, the two rank-r
     projections (x A^T, h A^T), the gate/up and down GEMMs, and one split-K reduction
-    per rank-r projection that was split.  MLP backward: pack, two rank-r projections
-    (dy B_d, [dg du][B_g B_u]) with their split-K sums, the reductions over tokens in two
-    launches (dB_d and dA_d after the act' GEMM; dB_g, dB_u, dA_g, dA_u after the dx
-    GEMM) whose sums share one launch at the end, and the act' and dx GEMMs.  Q/K/V + O
-    with RoPE: the same per half, plus one transpose-rotation launch in the backward."""
+    per rank-r projection that was split.  MLP backward (rank 16): pack, the rank-r
+    projection dy B_d (with its split-K sums if split), the act' GEMM, the reductions
+    over tokens dB_d and dA_d in one launch, one pass over dg, du that gives V and
+    dB_g, dB_u (V's partial sums added at once), the dx GEMM, dA_g and dA_u in one
+    launch, and one sum launch at the end for every dA/dB.  Q/K/V + O with RoPE: the
+    same per half (the reductions over tokens as separate launches), plus one
+    transpose-rotation launch in the backward."""
     cfg = synth.MLP_CONFIGS["qwen05b"].replace(M=1024)
     ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg).items()}
     lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
@@ -169,10 +171,9 @@ def test_launches_per_call(lib):
     assert (f["pack"], f["rank_proj"], f["gate_up"], f["proj"]) == (1, 2, 1, 1), f
     assert f["reduce"] <= 2 and set(f) <= {"pack", "rank_proj", "gate_up", "proj", "reduce"}, f
     b = _kinds(lib, bwd)
-    assert (b["pack"], b["rank_proj"], b["rank_grad"], b["act_bwd"], b["dgrad"]) == (1, 2, 2, 1, 1), b
-    # split-K sums of the two rank-r projections (if split), then one for all four
-    # reductions over tokens at the end of the call
-    assert 1 <= b["reduce"] <= 3 and set(b) <= {"pack", "rank_proj", "rank_grad", "act_bwd", "dgrad",
+    assert (b["pack"], b["rank_proj"], b["rank_grad"], b["act_bwd"], b["dgrad"]) == (1, 1, 3, 1, 1), b
+    # V's sums, dy B_d's split-K sums (if split), then one for every dA/dB at the end
+    assert 2 <= b["reduce"] <= 3 and set(b) <= {"pack", "rank_proj", "rank_grad", "act_bwd", "dgrad",
                                                   "reduce"}, b
 
     qc = synth.QKVO_CONFIGS["gqa7b"].replace(M=512, h=512, heads_q=4, heads_kv=2, head_dim=128)
@@ -199,8 +200,8 @@ def test_launches_per_call(lib):
 def test_qwen_shaped_step_launches(lib):
     """The Qwen-shaped forward + backward (4096 tokens, h = 896, i = 4864, r = 16) makes
     at most 15 launches: x A^T and dy B_d run unsplit (their split-K sums would cost
-    more than the split saves), and each backward's reductions over tokens take two
-    launches."""
+    more than the split saves), one pass over dg, du gives V and dB_g, dB_u, and each
+    backward's reductions over tokens take two more launches."""
     cfg = synth.MLP_CONFIGS["qwen05b"]
     ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg, seed=4).items()}
     lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
