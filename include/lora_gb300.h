@@ -146,7 +146,8 @@ lora_status_t lora_linear_forward_noalloc(int64_t M, int64_t in, int64_t out, in
 /* ---------------------------------------------------------------- gated MLP
  * x [M x h] -> y [M x h] through gate/up [i x h] and down [h x i] ("opake_lora_mlp").
  * saved (NULL for inference) receives g, u, h and the rank-r projections for
- * backward. */
+ * backward (x [A_g; A_u]^T also transposed, for the backward's single pass over dg, du
+ * when r <= 16). */
 size_t lora_mlp_saved_bytes(int64_t M, int64_t h, int64_t i, int r);
 size_t lora_mlp_workspace_bytes(int64_t M, int64_t h, int64_t i, int r);
 lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r, float s, lora_act_t act,
