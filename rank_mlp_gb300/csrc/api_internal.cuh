@@ -93,7 +93,7 @@ lora_status_t token_grads(int64_t M, int r, int kf, float s, const GradJob* jobs
 // (rank_dual.cuh): V[M x kf] (columns [0, nv), nv = the slots' extent rounded to 16)
 // = sum_p Q_p Bt_p^T, and dB_p = s Q_p^T T_p[:, slot_p] written as [F_p x r].  T^T is
 // the transposed rank-r operand [kf x ldt].  V is summed from its f32 slab (vslab) at
-// once; the dB sums are left to `defer`.  Only for r <= 16 (dual_supported).
+// once; the dB sums are left to `defer`.  Only where dual_supported.
 struct DualJob {
   const void* Q;      // [M x F] token-major
   int64_t F;
@@ -101,7 +101,10 @@ struct DualJob {
   int t_row;          // first row of this product's slot in T^T
   void* dB;           // [F x r]
 };
-inline bool dual_supported(int r, int kf) { return r <= 16 && kf >= 16; }
+inline bool dual_supported(int r, int kf, int nprod) {
+  return nprod >= 1 && nprod <= kDualMaxProducts && r <= kDualNRMax && nprod * r <= kDualNVMax &&
+         kf >= static_cast<int>(round_up(nprod * r, 16));
+}
 // f32 elements of the V slab and of the dB slabs (sum over the jobs) of one pass.
 void dual_slab_elems(int64_t M, int r, const int64_t* F, int njobs, int64_t& v_elems, int64_t& db_elems);
 lora_status_t rank_dual(int64_t M, int r, int kf, float s, const DualJob* jobs, int njobs, const void* Tt,

@@ -506,7 +506,7 @@ void dual_slab_elems(int64_t M, int r, const int64_t* F, int njobs, int64_t& v_e
 lora_status_t rank_dual(int64_t M, int r, int kf, float s, const DualJob* jobs, int njobs, const void* Tt,
                         int64_t ldt, void* V, float* vslab, Deferred& defer, unsigned* status, cudaStream_t st) {
   if (M == 0) return LORA_OK;
-  if (njobs < 1 || njobs > kDualMaxProducts || !dual_supported(r, kf)) return LORA_ERR_UNSUPPORTED;
+  if (!dual_supported(r, kf, njobs)) return LORA_ERR_UNSUPPORTED;
   int64_t F[kDualMaxProducts];
   for (int j = 0; j < njobs; ++j) F[j] = jobs[j].F;
   const DualPlan P = dual_plan(M, r, F, njobs);

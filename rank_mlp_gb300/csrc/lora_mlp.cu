@@ -23,7 +23,7 @@ struct MlpLayout {
 // reductions' slabs (kept until the call's final reduce).
 // With one pass over dg, du (dual_supported): the V slab shares the projections' region
 // and the dB_g, dB_u slabs join the others.
-static bool mlp_dual(int r, int kfg, int64_t n_ex) { return n_ex == 0 && dual_supported(r, kfg); }
+static bool mlp_dual(int r, int kfg, int64_t n_ex) { return n_ex == 0 && dual_supported(r, kfg, 2); }
 static int64_t mlp_bwd_rank_part(int64_t M, int64_t h, int64_t i, int r, int kfd, int kfg, int64_t n_ex) {
   int64_t p = imax(rank_projection_part(M, kfd, ceil_div(h, kBK)), rank_projection_part(M, kfg, 2 * ceil_div(i, kBK)));
   if (mlp_dual(r, kfg, n_ex)) {
@@ -184,9 +184,10 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
   pack_block(pack_job(pk, bf_d, h, kfd), down.B, r, 0, 0, static_cast<int>(h), r, 0, s);
   LGB_TRY(launch_pack(pk, stream));
 
-  // T_gu = x [A_g; A_u]^T (saved also transposed for the backward's pass over dg, du)
+  // T_gu = x [A_g; A_u]^T (saved also transposed where the backward's pass over dg, du
+  // reads it)
   const ProjSeg p1 = {x, acat_gu, h};
-  LGB_TRY(rank_projection(M, kfg, &p1, 1, tgu, part, status, stream, tgut, L.ldt));
+  LGB_TRY(rank_projection(M, kfg, &p1, 1, tgu, part, status, stream, mlp_dual(r, kfg, 0) ? tgut : nullptr, L.ldt));
 
   // [g | u] = [x | T_gu] [W_g | s B_g ; W_u | s B_u]^T, gate and up halves per tile; h = act(g) u
   {
@@ -333,7 +334,8 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   }
 
   // dB_d = s dy^T T_d and dA_d = s U_d^T h (one launch) read nothing the dh GEMM writes:
-  // they start on the SMs its last wave leaves idle
+  // they start on the SMs its last wave leaves idle.  (A single pass over dy for U_d and
+  // dB_d, as for dg, du below, measured no better: dy is a quarter of dg, du's bytes.)
   const GradJob j1[2] = {{dy, h, 0, d_down.dB, 0, td}, {hsv, i, 0, d_down.dA, 1, ud}};
   LGB_TRY(token_grads(M, r, kfd, s, j1, 2, dr, status, stream, n_ex, true));
 
@@ -367,9 +369,9 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   // dA_g = s V_g^T x, dA_u = s V_u^T x (and dB_g = s dg^T T_g, dB_u = s du^T T_u when
   // the pass over dg, du has not made them) in one launch: they read nothing the dx GEMM
   // writes and start on the SMs its last wave leaves idle
-  const GradJob j3[4] = {{x, h, 0, d_gate.dA, 1, V}, {x, h, r, d_up.dA, 1, V},
-                         {dg, i, 0, d_gate.dB, 0, tgu}, {du, i, r, d_up.dB, 0, tgu}};
-  LGB_TRY(token_grads(M, r, kfg, s, j3, dual ? 2 : 4, dr, status, stream, n_ex, true));
+  const GradJob j3[4] = {{dg, i, 0, d_gate.dB, 0, tgu}, {du, i, r, d_up.dB, 0, tgu},
+                         {x, h, 0, d_gate.dA, 1, V}, {x, h, r, d_up.dA, 1, V}};
+  LGB_TRY(token_grads(M, r, kfg, s, dual ? j3 + 2 : j3, dual ? 2 : 4, dr, status, stream, n_ex, true));
   LGB_TRY(defer_flush(dr, stream));
   if (n_ex > 0 && sq_norms != nullptr) {
     NormParams np;

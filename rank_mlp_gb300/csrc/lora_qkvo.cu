@@ -13,17 +13,46 @@ namespace {
 struct QkvoLayout {
   int kfq, kfo;
   size_t ws_fwd, ws_bwd, saved, off_to;
+  size_t off_tqkvt, off_tot;   // the rank-r projections transposed, [kf x ldt] (single passes
+  int64_t ldt;                 // over dy_q, dy_k, dy_v and over dy_o in the backward)
 };
 
-// Backward scratch, as for the MLP: rank-r projection slabs, then the token reductions'.
-static int64_t qkvo_bwd_rank_part(int64_t M, int64_t h, int64_t nq, int64_t nkv, int kfq, int kfo) {
-  return imax(rank_projection_part(M, kfo, ceil_div(h, kBK)),
-              rank_projection_part(M, kfq, ceil_div(nq, kBK) + 2 * ceil_div(nkv, kBK)));
+// Single passes over the backward's gradients (dual_supported): the q/k/v half's three
+// products and the o half's one.
+static bool qkv_dual(int r, int kfq) { return dual_supported(r, kfq, 3); }
+static bool o_dual(int r, int kfo) { return dual_supported(r, kfo, 1); }
+
+// Backward scratch, as for the MLP: rank-r projection slabs (and the single passes' V
+// slabs), then the token reductions' (and the single passes' dB slabs).
+static int64_t qkvo_bwd_rank_part(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r, int kfq, int kfo) {
+  int64_t p = imax(rank_projection_part(M, kfo, ceil_div(h, kBK)),
+                   rank_projection_part(M, kfq, ceil_div(nq, kBK) + 2 * ceil_div(nkv, kBK)));
+  int64_t v = 0, db = 0;
+  if (o_dual(r, kfo)) {
+    dual_slab_elems(M, r, &h, 1, v, db);
+    p = imax(p, v);
+  }
+  if (qkv_dual(r, kfq)) {
+    const int64_t f3[3] = {nq, nkv, nkv};
+    dual_slab_elems(M, r, f3, 3, v, db);
+    p = imax(p, v);
+  }
+  return p;
 }
-static int64_t qkvo_bwd_slabs(int64_t M, int64_t h, int64_t nq, int64_t nkv, int kfq, int kfo) {
+static int64_t qkvo_bwd_slabs(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r, int kfq, int kfo) {
   const int64_t f3[3] = {nq, nkv, nkv};
-  return token_grad_part(M, kfo, &h, 1) + token_grad_part(M, kfo, &nq, 1) + token_grad_part(M, kfq, f3, 3) +
-         token_grad_part(M, kfq, &h, 1);
+  int64_t n = token_grad_part(M, kfo, &h, 1) + token_grad_part(M, kfo, &nq, 1) + token_grad_part(M, kfq, f3, 3) +
+              token_grad_part(M, kfq, &h, 1);
+  int64_t v = 0, db = 0;
+  if (o_dual(r, kfo)) {
+    dual_slab_elems(M, r, &h, 1, v, db);
+    n += db;
+  }
+  if (qkv_dual(r, kfq)) {
+    dual_slab_elems(M, r, f3, 3, v, db);
+    n += db;
+  }
+  return n;
 }
 
 // Largest pair-GEMM tile counts of the forward (q/k/v in one launch, o) and the
@@ -68,8 +97,8 @@ QkvoLayout qkvo_layout(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r) {
     c.take_n<bf16>(M * kfq);
     c.take_n<bf16>(M * nq);     // dy_q, dy_k turned back by the transpose RoPE rotation
     c.take_n<bf16>(M * nkv);
-    c.take_n<float>(qkvo_bwd_rank_part(M, h, nq, nkv, kfq, kfo));
-    c.take_n<float>(qkvo_bwd_slabs(M, h, nq, nkv, kfq, kfo));
+    c.take_n<float>(qkvo_bwd_rank_part(M, h, nq, nkv, r, kfq, kfo));
+    c.take_n<float>(qkvo_bwd_slabs(M, h, nq, nkv, r, kfq, kfo));
     carve_sk(c, qkvo_bwd_tiles(M, h, nq));
     L.ws_bwd = c.off;
   }
@@ -77,6 +106,9 @@ QkvoLayout qkvo_layout(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r) {
     Carve c(nullptr);
     c.offset_of(sizeof(bf16) * M * kfq);
     L.off_to = c.offset_of(sizeof(bf16) * M * kfo);
+    L.ldt = round_up(M, 8);
+    L.off_tqkvt = c.offset_of(sizeof(bf16) * kfq * L.ldt);
+    L.off_tot = c.offset_of(sizeof(bf16) * kfo * L.ldt);
     L.saved = c.off;
   }
   return L;
@@ -152,9 +184,13 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
   bf16* tqkv = c.take_n<bf16>(M * kfq);
   bf16* to = c.take_n<bf16>(M * kfo);
   const SkRegion sk = carve_sk(c, qkvo_fwd_tiles(M, h, n_q, n_kv));
+  bf16* tqkv_t = nullptr;
+  bf16* to_t = nullptr;
   if (saved) {
     tqkv = static_cast<bf16*>(saved);
     to = reinterpret_cast<bf16*>(static_cast<uint8_t*>(saved) + L.off_to);
+    tqkv_t = reinterpret_cast<bf16*>(static_cast<uint8_t*>(saved) + L.off_tqkvt);
+    to_t = reinterpret_cast<bf16*>(static_cast<uint8_t*>(saved) + L.off_tot);
   }
 
   PackParams pk;
@@ -176,7 +212,7 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
 
   if (x) {
     const ProjSeg p1 = {x, acat, h};
-    LGB_TRY(rank_projection(M, kfq, &p1, 1, tqkv, part, status, stream));
+    LGB_TRY(rank_projection(M, kfq, &p1, 1, tqkv, part, status, stream, qkv_dual(r, kfq) ? tqkv_t : nullptr, L.ldt));
     GemmPlan g(kBigKK);
     const int ax = g.a_kmajor(x, M, h, h);
     const int at = g.a_kmajor(tqkv, M, kfq, kfq);
@@ -208,7 +244,7 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
   }
   if (o_in) {
     const ProjSeg p2 = {o_in, acat_o, n_q};
-    LGB_TRY(rank_projection(M, kfo, &p2, 1, to, part, status, stream));
+    LGB_TRY(rank_projection(M, kfo, &p2, 1, to, part, status, stream, o_dual(r, kfo) ? to_t : nullptr, L.ldt));
     GemmPlan g(kBigKK);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(h), EPI_STORE, false);
     GemmPlan::seg(G, g.a_kmajor(o_in, M, n_q, n_q), g.b_kmajor(o.W, h, n_q, n_q, g.b_rows_full()), -1, n_q, n_q);
@@ -269,6 +305,8 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
   const int kfq = L.kfq, kfo = L.kfo;
   const bf16* tqkv = static_cast<const bf16*>(saved);
   const bf16* to = reinterpret_cast<const bf16*>(static_cast<const uint8_t*>(saved) + L.off_to);
+  const bf16* tqkv_t = reinterpret_cast<const bf16*>(static_cast<const uint8_t*>(saved) + L.off_tqkvt);
+  const bf16* to_t = reinterpret_cast<const bf16*>(static_cast<const uint8_t*>(saved) + L.off_tot);
   Carve c(ws);
   unsigned* status = static_cast<unsigned*>(c.take(kWsHeader));
   bf16* btq = c.take_n<bf16>(kfq * n_q);
@@ -281,9 +319,9 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
   bf16* V = c.take_n<bf16>(M * kfq);
   bf16* dyq_r = c.take_n<bf16>(M * n_q);
   bf16* dyk_r = c.take_n<bf16>(M * n_kv);
-  float* part = c.take_n<float>(qkvo_bwd_rank_part(M, h, n_q, n_kv, kfq, kfo));
+  float* part = c.take_n<float>(qkvo_bwd_rank_part(M, h, n_q, n_kv, r, kfq, kfo));
   Deferred dr;
-  defer_init(dr, c.take_n<float>(qkvo_bwd_slabs(M, h, n_q, n_kv, kfq, kfo)));
+  defer_init(dr, c.take_n<float>(qkvo_bwd_slabs(M, h, n_q, n_kv, r, kfq, kfo)));
   const SkRegion sk = carve_sk(c, qkvo_bwd_tiles(M, h, n_q));
 
   PackParams pk;
@@ -304,8 +342,15 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
   LGB_TRY(launch_pack(pk, stream));
 
   if (o_in) {
-    const ProjSeg p1 = {dyo, bt_o, h};
-    LGB_TRY(rank_projection(M, kfo, &p1, 1, uo, part, status, stream));
+    const bool dual = o_dual(r, kfo);
+    if (dual) {
+      // U_o = dy_o B_o and dB_o = s dy_o^T T_o in one pass over dy_o
+      const DualJob jd = {dyo, h, bt_o, 0, d_o.dB};
+      LGB_TRY(rank_dual(M, r, kfo, s, &jd, 1, to_t, L.ldt, uo, part, dr, status, stream));
+    } else {
+      const ProjSeg p1 = {dyo, bt_o, h};
+      LGB_TRY(rank_projection(M, kfo, &p1, 1, uo, part, status, stream));
+    }
     GemmPlan g(kBigKMN);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(n_q), EPI_STORE, false);
     GemmPlan::seg(G, g.a_kmajor(dyo, M, h, h), g.b_mnmajor(o.W, n_q, h, n_q), -1, h, h);
@@ -317,10 +362,10 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
-    // dB_o = s dy_o^T T_o and dA_o = s U_o^T o_in (one launch) read nothing the d o_in
-    // GEMM writes
+    // dA_o = s U_o^T o_in (and dB_o = s dy_o^T T_o when the pass over dy_o has not made
+    // it) in one launch: they read nothing the d o_in GEMM writes
     const GradJob j1[2] = {{dyo, h, 0, d_o.dB, 0, to}, {o_in, n_q, 0, d_o.dA, 1, uo}};
-    LGB_TRY(token_grads(M, r, kfo, s, j1, 2, dr, status, stream, 0, true));
+    LGB_TRY(token_grads(M, r, kfo, s, dual ? j1 + 1 : j1, dual ? 1 : 2, dr, status, stream, 0, true));
   }
   if (x) {
     if (rope != nullptr) {
@@ -346,8 +391,15 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
       dyq = dyq_r;
       dyk = dyk_r;
     }
-    const ProjSeg p3[3] = {{dyq, btq, n_q}, {dyk, btk, n_kv}, {dyv, btv, n_kv}};
-    LGB_TRY(rank_projection(M, kfq, p3, 3, V, part, status, stream));
+    const bool dual = qkv_dual(r, kfq);
+    if (dual) {
+      // V = [dy_q B_q | dy_k B_k | dy_v B_v] and dB_q, dB_k, dB_v in one pass over them
+      const DualJob jd[3] = {{dyq, n_q, btq, 0, d_q.dB}, {dyk, n_kv, btk, r, d_k.dB}, {dyv, n_kv, btv, 2 * r, d_v.dB}};
+      LGB_TRY(rank_dual(M, r, kfq, s, jd, 3, tqkv_t, L.ldt, V, part, dr, status, stream));
+    } else {
+      const ProjSeg p3[3] = {{dyq, btq, n_q}, {dyk, btk, n_kv}, {dyv, btv, n_kv}};
+      LGB_TRY(rank_projection(M, kfq, p3, 3, V, part, status, stream));
+    }
     GemmPlan g(kBigKMN);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(h), EPI_STORE, false);
     GemmPlan::seg(G, g.a_kmajor(dyq, M, n_q, n_q), g.b_mnmajor(q.W, h, n_q, h), -1, n_q, n_q);
@@ -361,11 +413,12 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
     LGB_TRY(launch_gemm(kBigKMN, g.p, LORA_KIND_DGRAD, stream));
-    // the q, k, v dB and dA (one launch) read nothing the dx GEMM writes
+    // the q, k, v dA (and dB when the pass over dy_q, dy_k, dy_v has not made them) in one
+    // launch: they read nothing the dx GEMM writes
     const GradJob j3[6] = {{dyq, n_q, 0, d_q.dB, 0, tqkv}, {dyk, n_kv, r, d_k.dB, 0, tqkv},
                            {dyv, n_kv, 2 * r, d_v.dB, 0, tqkv}, {x, h, 0, d_q.dA, 1, V},
                            {x, h, r, d_k.dA, 1, V}, {x, h, 2 * r, d_v.dA, 1, V}};
-    LGB_TRY(token_grads(M, r, kfq, s, j3, 6, dr, status, stream, 0, true));
+    LGB_TRY(token_grads(M, r, kfq, s, dual ? j3 + 3 : j3, dual ? 3 : 6, dr, status, stream, 0, true));
   }
   return defer_flush(dr, stream);
 }

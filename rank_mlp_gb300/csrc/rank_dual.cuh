@@ -1,5 +1,6 @@
-// One pass over a token-major gradient Q (dg and du of the gated MLP) that makes both
-// of its rank-r products ("Model Patches and Kernels", the LoRA backward):
+// One pass over token-major gradients Q_p (dg and du of the gated MLP; dy_q, dy_k,
+// dy_v or dy_o of the attention projections) that makes both of their rank-r products
+// ("Model Patches and Kernels", the LoRA backward):
 //
 //   V[:, slots]  = sum over products p of  Q_p B_p            (a projection: M x NV)
 //   dB_p         = s Q_p^T T_p[:, slot_p]                      (a reduction over tokens: F_p x r)
@@ -20,7 +21,7 @@
 
 namespace lgb {
 
-constexpr int kDualMaxProducts = 2;
+constexpr int kDualMaxProducts = 3;
 constexpr int kDualMaxCtas = 152;
 constexpr int kDualStages = 4;
 constexpr int kDualNVMax = 32;                         // projection accumulator columns

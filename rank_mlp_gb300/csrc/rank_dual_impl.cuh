@@ -33,8 +33,12 @@ __device__ __forceinline__ void dual_wait_drain(uint32_t bar, uint32_t parity, c
 
 // Feature block kb of the concatenated products: its product and local block.
 __device__ __forceinline__ void dual_block(const DualParams& p, int kb, int& prod, int& lb) {
-  prod = (p.nprod > 1 && kb >= p.prod[0].nkb) ? 1 : 0;
-  lb = prod ? kb - p.prod[0].nkb : kb;
+  prod = 0;
+  lb = kb;
+  while (prod + 1 < p.nprod && lb >= p.prod[prod].nkb) {
+    lb -= p.prod[prod].nkb;
+    ++prod;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) rank_dual_kernel(const __grid_constant__ DualParams p) {
@@ -66,9 +70,15 @@ __global__ void __launch_bounds__(kThreads, 1) rank_dual_kernel(const __grid_con
   const int t1 = static_cast<int>(static_cast<long long>(p.tiles_m) * (gti + 1) / p.gt);
   const int k0 = static_cast<int>(static_cast<long long>(p.kb_total) * gfi / p.gf);
   const int k1 = static_cast<int>(static_cast<long long>(p.kb_total) * (gfi + 1) / p.gf);
-  // products with feature blocks in this range
-  const bool has0 = k0 < p.prod[0].nkb;
-  const bool has1 = p.nprod > 1 && k1 > p.prod[0].nkb;
+  // products with feature blocks in this range (bit p)
+  unsigned present = 0;
+  {
+    int base = 0;
+    for (int q = 0; q < p.nprod; ++q) {
+      if (k0 < base + p.prod[q].nkb && k1 > base) present |= 1u << q;
+      base += p.prod[q].nkb;
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kDualStages; ++s) {
@@ -106,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) rank_dual_kernel(const __grid_con
       for (int s = 0; s < kDualStages; ++s) armed[s] = -1;
       int tarmed[2] = {-1, -1};
       bool ok = true;
-      const uint32_t tbytes = static_cast<uint32_t>((has0 ? 1 : 0) + (has1 ? 1 : 0)) * 2u * 64u * p.nr * 2u;
+      const uint32_t tbytes = static_cast<uint32_t>(__popc(present)) * 2u * 64u * p.nr * 2u;
       const uint32_t sbytes = static_cast<uint32_t>(kDualQBytes + 2 * 64 * p.nv * 2);
       for (int t = t0; t < t1 && ok; ++t) {
         const int slot = (t - t0) & 1;
@@ -116,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) rank_dual_kernel(const __grid_con
         mbar_arrive_expect_tx(tfull_bar(slot), tbytes);
         tarmed[slot] = static_cast<int>(tphase);
         for (int q = 0; q < p.nprod; ++q) {
-          if ((q == 0 && !has0) || (q == 1 && !has1)) continue;
+          if (!((present >> q) & 1u)) continue;
           const uint32_t dst = tbase + slot * kDualSlotBytes + q * kDualTBytes;
           for (int c = 0; c < 2; ++c)
             tma_load_2d(dst + c * (p.nr * 128), &p.maps[p.prod[q].t_map], tfull_bar(slot), t * 128 + 64 * c,

@@ -153,9 +153,9 @@ def test_launches_per_call(lib):
     projection dy B_d (with its split-K sums if split), the act' GEMM, the reductions
     over tokens dB_d and dA_d in one launch, one pass over dg, du that gives V and
     dB_g, dB_u (V's partial sums added at once), the dx GEMM, dA_g and dA_u in one
-    launch, and one sum launch at the end for every dA/dB.  Q/K/V + O with RoPE: the
-    same per half (the reductions over tokens as separate launches), plus one
-    transpose-rotation launch in the backward."""
+    launch, and one sum launch at the end for every dA/dB.  Q/K/V + O with RoPE (rank
+    8): per half one pass over the output gradients for the projection and dB, then
+    dA; plus one transpose-rotation launch in the backward."""
     cfg = synth.MLP_CONFIGS["qwen05b"].replace(M=1024)
     ins = {k: x.to(DEV) for k, x in synth.make_mlp_inputs(cfg).items()}
     lin = lambda n: (ins["W_" + n], ins["A_" + n], ins["B_" + n])  # noqa: E731
@@ -192,8 +192,10 @@ def test_launches_per_call(lib):
     f = _kinds(lib, qfwd)
     assert (f["pack"], f["rank_proj"], f["proj"]) == (1, 2, 2), f
     b = _kinds(lib, qbwd)
-    assert (b["pack"], b["rope"], b["rank_proj"], b["rank_grad"], b["dgrad"]) == (1, 1, 2, 2, 2), b
-    assert 1 <= b["reduce"] <= 3, b
+    # rank 8: one pass over dy_o (U_o, dB_o) and one over dy_q, dy_k, dy_v (V, dB_q, dB_k,
+    # dB_v), each with its partial sums, then dA_o and the q, k, v dA, and the final sums
+    assert (b["pack"], b["rope"], b["rank_proj"], b["rank_grad"], b["dgrad"]) == (1, 1, 0, 4, 2), b
+    assert b["reduce"] == 3, b
     assert lib.poll_status() == 0
 
 
