@@ -55,9 +55,11 @@ struct ProjSeg {
   const void* P;
   int64_t K;
 };
-// dst_t (optional): the same result transposed, [kf x ldt] (ldt >= M, a multiple of 8).
+// dst_t (optional): columns [0, ntrans) of the result transposed, [ntrans x ldt] (ldt >= M,
+// a multiple of 8).
 lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int nseg, void* dst, float* part,
-                              unsigned* status, cudaStream_t st, void* dst_t = nullptr, int64_t ldt = 0);
+                              unsigned* status, cudaStream_t st, void* dst_t = nullptr, int64_t ldt = 0,
+                              int ntrans = 0);
 // f32 slab elements of a rank-r projection over ktotal_blocks 64-wide k-blocks.
 int64_t rank_projection_part(int64_t M, int kf, int64_t ktotal_blocks);
 

@@ -62,7 +62,8 @@ struct GroupDesc {
   const void* in1;
   long long ldo, ldi;
   float* part;               // EPI_PARTIAL: [splits][tiles_m*128][tiles_n*BN] f32
-  long long ldt;             // EPI_STORE with out1: out1 receives the tile transposed, [N x ldt]
+  long long ldt;             // EPI_STORE with out1: out1 receives columns [0, ntc) of the
+  int ntc;                   // tile transposed, [ntc x ldt]
   int emap[4];               // EPI_ACT_BWD on the staged variant: maps of g, u (in) and dg, du (out)
 };
 
@@ -377,8 +378,8 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const GroupDesc
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c = col0 + 2 * e;
-            if (c < G.N) ot[static_cast<long long>(c) * G.ldt] = __ushort_as_bfloat16(static_cast<unsigned short>(w[e]));
-            if (c + 1 < G.N)
+            if (c < G.ntc) ot[static_cast<long long>(c) * G.ldt] = __ushort_as_bfloat16(static_cast<unsigned short>(w[e]));
+            if (c + 1 < G.ntc)
               ot[static_cast<long long>(c + 1) * G.ldt] = __ushort_as_bfloat16(static_cast<unsigned short>(w[e] >> 16));
           }
         }

@@ -296,7 +296,7 @@ PackJob& pack_job(PackParams& P, void* dst, int64_t rows, int64_t cols) {
 }
 
 lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int nseg, void* dst, float* part,
-                                     unsigned* status, cudaStream_t st, void* dst_t, int64_t ldt) {
+                                     unsigned* status, cudaStream_t st, void* dst_t, int64_t ldt, int ntrans) {
   const int variant = skinny_kk(kf);
   GemmPlan g(variant);
   int64_t kb = 0;
@@ -317,6 +317,7 @@ lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int nseg, 
     G.ldo = kf;
     G.out1 = dst_t;
     G.ldt = ldt;
+    G.ntc = ntrans;
   }
   g.p.status = status;
   g.finish();
@@ -342,6 +343,7 @@ lora_status_t rank_projection(int64_t M, int kf, const ProjSeg* segs, int nseg, 
       r.out[1] = o;
       r.out[1].dst = static_cast<bf16*>(dst_t);
       r.out[1].ld = ldt;
+      r.out[1].ncols = ntrans;
       r.out[1].trans = 1;
       r.nout = 2;
     }

@@ -187,7 +187,8 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
   // T_gu = x [A_g; A_u]^T (saved also transposed where the backward's pass over dg, du
   // reads it)
   const ProjSeg p1 = {x, acat_gu, h};
-  LGB_TRY(rank_projection(M, kfg, &p1, 1, tgu, part, status, stream, mlp_dual(r, kfg, 0) ? tgut : nullptr, L.ldt));
+  LGB_TRY(rank_projection(M, kfg, &p1, 1, tgu, part, status, stream, mlp_dual(r, kfg, 0) ? tgut : nullptr, L.ldt,
+                          2 * r));
 
   // [g | u] = [x | T_gu] [W_g | s B_g ; W_u | s B_u]^T, gate and up halves per tile; h = act(g) u
   {

@@ -212,7 +212,8 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
 
   if (x) {
     const ProjSeg p1 = {x, acat, h};
-    LGB_TRY(rank_projection(M, kfq, &p1, 1, tqkv, part, status, stream, qkv_dual(r, kfq) ? tqkv_t : nullptr, L.ldt));
+    LGB_TRY(rank_projection(M, kfq, &p1, 1, tqkv, part, status, stream, qkv_dual(r, kfq) ? tqkv_t : nullptr, L.ldt,
+                            3 * r));
     GemmPlan g(kBigKK);
     const int ax = g.a_kmajor(x, M, h, h);
     const int at = g.a_kmajor(tqkv, M, kfq, kfq);
@@ -244,7 +245,7 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
   }
   if (o_in) {
     const ProjSeg p2 = {o_in, acat_o, n_q};
-    LGB_TRY(rank_projection(M, kfo, &p2, 1, to, part, status, stream, o_dual(r, kfo) ? to_t : nullptr, L.ldt));
+    LGB_TRY(rank_projection(M, kfo, &p2, 1, to, part, status, stream, o_dual(r, kfo) ? to_t : nullptr, L.ldt, r));
     GemmPlan g(kBigKK);
     GroupDesc& G = g.group(static_cast<int>(M), static_cast<int>(h), EPI_STORE, false);
     GemmPlan::seg(G, g.a_kmajor(o_in, M, n_q, n_q), g.b_kmajor(o.W, h, n_q, n_q, g.b_rows_full()), -1, n_q, n_q);

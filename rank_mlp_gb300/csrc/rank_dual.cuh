@@ -37,12 +37,15 @@ constexpr int kDualSlotBytes = kDualMaxProducts * kDualTBytes;
 constexpr int kDualNumBars = 2 * kDualStages + 9;
 constexpr int kDualSmemBytes = kDualStages * kDualStageBytes + 2 * kDualSlotBytes + 8 * kDualNumBars + 16 + 1024;
 static_assert(kDualStageBytes % 1024 == 0 && kDualSlotBytes % 1024 == 0, "dual alignment");
+static_assert(kDualSmemBytes <= 232448, "shared memory per CTA");
 
 struct DualProduct {
   int q_map, b_map, t_map;   // tensor maps: Q [M x F] (box 64 x 128), B^T [NV x F] (box 64 x NV),
                              // T^T [kf x M] (box 64 x NR)
   int nkb;                   // 128-feature blocks of this product
-  int t_row;                 // first T^T row of this product's rank slot
+  int t_row;                 // first T^T row of this product's rank slot (rows past the
+                             // products' slots may hold anything: they reach only
+                             // reduction columns past r, which are never written out)
   float* db_part;            // [gt][nkb * 128][NR] f32 partial dB
 };
 
