@@ -235,6 +235,7 @@ lora_status_t launch_norms(const NormParams& p, int examples, cudaStream_t st) {
   return LORA_OK;
 }
 
+constexpr int kVec4MaxSplits = 8;
 lora_status_t launch_reduce(const RedParams& plan, cudaStream_t st) {
   if (plan.nout == 0) return LORA_OK;
   RedParams p = plan;
@@ -242,8 +243,10 @@ lora_status_t launch_reduce(const RedParams& plan, cudaStream_t st) {
   for (int j = 0; j < p.nout; ++j) {
     RedOut& o = p.out[j];
     const int64_t elems = static_cast<int64_t>(o.rows) * o.ncols;
+    // four columns a thread, unless the sums are long (more than kVec4MaxSplits slabs):
+    // then a thread per column, four times the threads to hide the loads' latency
     o.vec4 = !o.per_split && o.ncols % 4 == 0 && o.col0 % 4 == 0 && o.width % 4 == 0 && elems < (int64_t(1) << 31) &&
-             (o.trans || (o.ld % 4 == 0 && aligned(o.dst, 8)));
+             (o.trans || (o.ld % 4 == 0 && aligned(o.dst, 8))) && o.splits <= kVec4MaxSplits;
     const int64_t n = o.vec4 ? elems / 4 : elems;
     most = n > most ? n : most;
   }
