@@ -155,16 +155,19 @@ inline int max_splits(int64_t kb_total) {
   return static_cast<int>(s);
 }
 
-// Split-K factor for `tiles` output tiles on `sms` SMs: the one (<= max_splits) that
-// minimises waves per split, ceil(tiles * s / sms) / s, i.e. the busy time of the
-// slowest SM; ties go to fewer splits (less partial traffic).
+// Split factor (over tokens) of a reduction over tokens: `tiles` 128-row output tiles
+// of kb_total k-blocks each on `sms` SMs.  Minimises the slowest SM's k-blocks,
+// ceil(tiles * s / sms) / s * kb_total, plus kSlabKBlocks per split for reading its f32
+// partial tile back in the final sums (a 32 KB slab tile against 24 KB a k-block
+// streams); ties go to fewer splits.
+constexpr int kSlabKBlocks = 2;
 inline int choose_splits(int64_t tiles, int64_t kb_total, int sms) {
   if (tiles <= 0 || kb_total <= 0 || sms <= 0) return 1;
   const int smax = max_splits(kb_total);
   int best = 1;
   double best_cost = 1e30;
   for (int s = 1; s <= smax; ++s) {
-    const double cost = static_cast<double>(ceil_div(tiles * s, sms)) / s;
+    const double cost = static_cast<double>(ceil_div(tiles * s, sms)) / s * kb_total + kSlabKBlocks * s;
     if (cost < best_cost * (1.0 - 1e-9)) {
       best_cost = cost;
       best = s;

@@ -117,6 +117,21 @@ def test_mlp_ranks(lib, r):
         parity(k, g[k], b[k])
 
 
+@pytest.mark.parametrize("r", [5, 16])
+def test_mlp_single_pass_ragged(lib, r):
+    """The backward's single pass over dg, du (V and dB_g, dB_u from one read, r <= 16)
+    on ragged extents: 1000 tokens (7 whole 128-token tiles and a part) and i = 1400
+    (10 whole 128-feature blocks and a part), so its CTAs split both the token tiles and
+    the feature blocks, and the last of each is partly outside the tensors."""
+    cfg = synth.MLP_CONFIGS["tiny"].replace(M=1000, h=384, i=1400, r=r, alpha=2 * r)
+    t, v = _mlp_inputs(cfg, seed=11 + r)
+    y, g = mlp_gpu(lib, t, cfg)
+    f, b = mlp_oracle(v, cfg)
+    parity("y", y, f["y"])
+    for k in MLP_GRADS:
+        parity(k, g[k], b[k])
+
+
 def test_mlp_zero_b_is_the_base_mlp(lib):
     """B = 0: the adapters contribute nothing and every dA is exactly zero."""
     cfg = synth.MLP_CONFIGS["tiny"].replace(M=300)
@@ -149,6 +164,21 @@ def test_mlp_zero_scale_and_adapter_term(lib):
 def test_qkvo_small(lib):
     cfg = synth.QKVO_CONFIGS["gqa7b"].replace(M=200, h=256, heads_q=4, heads_kv=2, head_dim=64)
     ins = synth.make_qkvo_inputs(cfg)
+    t = {k: x.to(DEV) for k, x in ins.items()}
+    out, g = qkvo_gpu(lib, t, cfg)
+    f, b = qkvo_oracle(to_f64_dict(ins), cfg)
+    for k in ("q", "k", "v", "o"):
+        parity(k, out[k], f[k])
+    for k in b:
+        parity(k, g[k], b[k])
+
+
+def test_qkvo_single_pass_rank10(lib):
+    """Rank 10: the q/k/v half's single pass over dy_q, dy_k, dy_v carries three slots of
+    10 columns in a 32-column projection (3 r <= 32) and reads each slot's T^T rows from
+    a 16-row box that overlaps the next slot; 300 tokens (ragged)."""
+    cfg = synth.QKVO_CONFIGS["gqa7b"].replace(M=300, h=256, heads_q=4, heads_kv=2, head_dim=64, r=10, alpha=20)
+    ins = synth.make_qkvo_inputs(cfg, seed=5)
     t = {k: x.to(DEV) for k, x in ins.items()}
     out, g = qkvo_gpu(lib, t, cfg)
     f, b = qkvo_oracle(to_f64_dict(ins), cfg)
