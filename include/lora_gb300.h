@@ -104,14 +104,17 @@ typedef struct {
 
 /* ---------------------------------------------------------------- single linear
  * (1) for one projection ("opake_lora_w").  saved holds the rank-r projection x A^T
- * for backward; pass NULL for inference. */
+ * and the adapter packed for backward; pass NULL for inference. */
 size_t lora_linear_saved_bytes(int64_t M, int64_t in, int64_t out, int r);
 size_t lora_linear_workspace_bytes(int64_t M, int64_t in, int64_t out, int r);
 lora_status_t lora_linear_forward(int64_t M, int64_t in, int64_t out, int r, float s,
                                   const void* x, lora_linear_t lin, void* y, void* saved,
                                   void* ws, size_t ws_bytes, cudaStream_t stream);
 /* dx [M x in] = dy W + s (dy B) A;  dA = s (dy B)^T x;  dB = s dy^T (x A^T).
- * x is the forward input again; saved is what forward wrote. */
+ * x is the forward input again; saved is what forward wrote, including the adapter
+ * packed as this call's operands (with the forward's s): lin must be the forward's
+ * (its W is read here, its A and B only checked), and s the same, as autograd uses the
+ * tensors a forward saved. */
 lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out, int r, float s,
                                    const void* x, lora_linear_t lin, const void* saved,
                                    const void* dy, void* dx, lora_grads_t grads,
@@ -147,7 +150,7 @@ lora_status_t lora_linear_forward_noalloc(int64_t M, int64_t in, int64_t out, in
  * x [M x h] -> y [M x h] through gate/up [i x h] and down [h x i] ("opake_lora_mlp").
  * saved (NULL for inference) receives g, u, h and the rank-r projections for
  * backward (x [A_g; A_u]^T also transposed, for the backward's single pass over dg, du
- * when r <= 16). */
+ * when r <= 16), and the adapters packed as the backward's operands. */
 size_t lora_mlp_saved_bytes(int64_t M, int64_t h, int64_t i, int r);
 size_t lora_mlp_workspace_bytes(int64_t M, int64_t h, int64_t i, int r);
 lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r, float s, lora_act_t act,
@@ -156,7 +159,9 @@ lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r, float s, 
                                void* ws, size_t ws_bytes, cudaStream_t stream);
 /* Gradients of <dy, y>: dx [M x h] and dA/dB of gate, up and down.  Needs the
  * forward's x and saved blob (the activation and its derivative are recomputed from
- * the saved g, u). */
+ * the saved g, u).  The adapters enter as the forward packed them into saved (with its
+ * s), as autograd uses the tensors a forward saved: gate, up and down must be the
+ * forward's (their W is read here; their A and B only checked), and s the same. */
 lora_status_t lora_mlp_backward(int64_t M, int64_t h, int64_t i, int r, float s, lora_act_t act,
                                 const void* x, lora_linear_t gate, lora_linear_t up,
                                 lora_linear_t down, const void* saved, const void* dy,
@@ -215,7 +220,9 @@ lora_status_t lora_rope_table(float* cos, float* sin, int64_t n_pos, int head_di
  * aligned, added to q, k, v ("Fused LoRA operations": QKV fusion supports optional
  * frozen base-layer biases); a frozen bias gets no gradient, so backward does not
  * take it.  rope is NULL or the rotary embedding applied to q and k after the bias,
- * in the projection's epilogue (lora_rope_t above; ignored when x == NULL). */
+ * in the projection's epilogue (lora_rope_t above; ignored when x == NULL).  saved
+ * (NULL for inference) receives the rank-r projections (also transposed where the
+ * backward's single passes read them) and the adapters packed for backward. */
 size_t lora_qkvo_saved_bytes(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r);
 size_t lora_qkvo_workspace_bytes(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r);
 lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r, float s,
@@ -229,7 +236,9 @@ lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv,
  * x == NULL skips the q/k/v half, o_in == NULL the O half.  With rope (the one the
  * forward used), dyq and dyk are gradients of the rotated q and k: they are turned
  * back by the transpose rotation (into the workspace) before the projections'
- * backward. */
+ * backward.  The adapters enter as the forward packed them into saved (with its s):
+ * q, k, v, o must be the forward's (their W is read here; their A and B only
+ * checked), and s the same. */
 lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, int64_t n_kv, int r, float s,
                                  const void* x, lora_linear_t q, lora_linear_t k,
                                  lora_linear_t v, const void* o_in, lora_linear_t o,

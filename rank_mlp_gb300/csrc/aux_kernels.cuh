@@ -11,7 +11,7 @@
 
 namespace lgb {
 
-constexpr int kMaxPackJobs = 8;
+constexpr int kMaxPackJobs = 12;   // the Q/K/V + O forward's six and its backward's six
 constexpr int kMaxPackBlocks = 3;
 
 struct PackBlock {

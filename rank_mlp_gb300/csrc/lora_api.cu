@@ -42,10 +42,21 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// The driver's map encoder needs a current context on the calling thread, which a
+// thread that has made no runtime call yet lacks (e.g. the thread autograd runs a
+// backward on): the current device's primary context is made current, once per thread
+// and device.
+static void bind_current_device() {
+  thread_local int bound = -1;
+  int dev = -1;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev != bound && cudaSetDevice(dev) == cudaSuccess) bound = dev;
+}
+
 // 2-D bf16 map with a 128-byte, 32-byte or no swizzle (swizzle_bytes 128, 32, 0);
 // out-of-bounds elements read as zero.
 bool encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
                 uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
+  bind_current_device();
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr || inner == 0 || outer == 0) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -64,6 +75,7 @@ bool encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer
 // ld * d1; box {box_inner, box_d1, 1}.
 bool encode_map_planes(CUtensorMap* m, const void* base, uint64_t inner, uint64_t d1, uint64_t d2, uint64_t ld,
                        uint32_t box_inner, uint32_t box_d1) {
+  bind_current_device();
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr || inner == 0 || d1 == 0 || d2 == 0) return false;
   const cuuint64_t dims[3] = {inner, d1, d2};

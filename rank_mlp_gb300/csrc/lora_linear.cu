@@ -15,6 +15,7 @@ struct LinearLayout {
   int kf;
   size_t ws_fwd_base;   // the forward without the split-tail regions (last in its layout)
   size_t ws_fwd, ws_bwd, saved;
+  size_t off_bt, off_af;   // saved: the backward's packed operands B^T and s A
 };
 
 LinearLayout linear_layout(int64_t M, int64_t in, int64_t out, int r) {
@@ -35,8 +36,6 @@ LinearLayout linear_layout(int64_t M, int64_t in, int64_t out, int r) {
   {
     Carve c(nullptr);
     c.take(kWsHeader);
-    c.take_n<bf16>(kf * out);   // B^T
-    c.take_n<bf16>(kf * in);    // s A
     c.take_n<bf16>(M * kf);     // U
     c.take_n<float>(rank_projection_part(M, kf, ceil_div(out, kBK)));
     c.take_n<float>(token_grad_part(M, kf, &out, 1) + token_grad_part(M, kf, &in, 1));   // dB, dA slabs
@@ -46,6 +45,8 @@ LinearLayout linear_layout(int64_t M, int64_t in, int64_t out, int r) {
   {
     Carve c(nullptr);
     c.take_n<bf16>(M * kf);
+    L.off_bt = c.offset_of(sizeof(bf16) * kf * out);
+    L.off_af = c.offset_of(sizeof(bf16) * kf * in);
     L.saved = c.off;
   }
   return L;
@@ -104,6 +105,13 @@ static lora_status_t linear_forward_impl(int64_t M, int64_t in, int64_t out, int
   std::memset(static_cast<void*>(&pk), 0, sizeof(pk));
   pack_block(pack_job(pk, acat, kf, in), lin.A, in, 0, 0, r, static_cast<int>(in), 0, 1.0f);
   pack_block(pack_job(pk, bf, out, kf), lin.B, r, 0, 0, static_cast<int>(out), r, 0, s);
+  if (saved) {
+    // the backward's operands too (it reads them from saved, as autograd reads the
+    // tensors a forward saved)
+    uint8_t* sv = static_cast<uint8_t*>(saved);
+    pack_block(pack_job(pk, sv + L.off_bt, kf, out), lin.B, r, 0, 0, r, static_cast<int>(out), 1, 1.0f);
+    pack_block(pack_job(pk, sv + L.off_af, kf, in), lin.A, in, 0, 0, r, static_cast<int>(in), 0, s);
+  }
   LGB_TRY(launch_pack(pk, stream));
 
   const ProjSeg ps = {x, acat, in};
@@ -164,20 +172,15 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   const int kf = L.kf;
   Carve c(ws);
   unsigned* status = static_cast<unsigned*>(c.take(kWsHeader));
-  bf16* bt = c.take_n<bf16>(kf * out);
-  bf16* af = c.take_n<bf16>(kf * in);
+  // the adapter operands come packed from the forward (saved)
+  const bf16* bt = reinterpret_cast<const bf16*>(static_cast<const uint8_t*>(saved) + L.off_bt);
+  const bf16* af = reinterpret_cast<const bf16*>(static_cast<const uint8_t*>(saved) + L.off_af);
   bf16* U = c.take_n<bf16>(M * kf);
   float* part = c.take_n<float>(rank_projection_part(M, kf, ceil_div(out, kBK)));
   Deferred dr;
   defer_init(dr, c.take_n<float>(token_grad_part(M, kf, &out, 1) + token_grad_part(M, kf, &in, 1)));
   const SkRegion sk = carve_sk(c, pair_tiles(M, in));
   const bf16* T = static_cast<const bf16*>(saved);
-
-  PackParams pk;
-  std::memset(static_cast<void*>(&pk), 0, sizeof(pk));
-  pack_block(pack_job(pk, bt, kf, out), lin.B, r, 0, 0, r, static_cast<int>(out), 1, 1.0f);
-  pack_block(pack_job(pk, af, kf, in), lin.A, in, 0, 0, r, static_cast<int>(in), 0, s);
-  LGB_TRY(launch_pack(pk, stream));
 
   const ProjSeg ps = {dy, bt, out};
   LGB_TRY(rank_projection(M, kf, &ps, 1, U, part, status, stream));

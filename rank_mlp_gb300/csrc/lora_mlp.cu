@@ -17,7 +17,24 @@ struct MlpLayout {
   size_t off_g, off_u, off_h, off_tgu, off_td;
   size_t off_tgut;   // T_gu transposed [kfg x ldt] (the backward's one pass over dg, du)
   int64_t ldt;
+  // the backward's packed adapter operands, written by the forward's pack launch
+  size_t off_bt_d, off_af_d, off_bt_g, off_bt_u, off_af_gu;
 };
+
+// The backward's packed operands: B_d^T, s A_d, B_g^T and B_u^T (in their slots), s [A_g; A_u].
+struct MlpBwdPack {
+  bf16 *bt_d, *af_d, *bt_g, *bt_u, *af_gu;
+};
+void pack_mlp_bwd(PackParams& pk, const MlpBwdPack& P, lora_linear_t gate, lora_linear_t up, lora_linear_t down,
+                  int64_t h, int64_t i, int r, float s, int kfg, int kfd) {
+  pack_block(pack_job(pk, P.bt_d, kfd, h), down.B, r, 0, 0, r, static_cast<int>(h), 1, 1.0f);
+  pack_block(pack_job(pk, P.af_d, kfd, i), down.A, i, 0, 0, r, static_cast<int>(i), 0, s);
+  pack_block(pack_job(pk, P.bt_g, kfg, i), gate.B, r, 0, 0, r, static_cast<int>(i), 1, 1.0f);
+  pack_block(pack_job(pk, P.bt_u, kfg, i), up.B, r, r, 0, r, static_cast<int>(i), 1, 1.0f);
+  PackJob& J = pack_job(pk, P.af_gu, kfg, h);
+  pack_block(J, gate.A, h, 0, 0, r, static_cast<int>(h), 0, s);
+  pack_block(J, up.A, h, r, 0, r, static_cast<int>(h), 0, s);
+}
 
 // Backward scratch: the rank-r projections' split-K slabs (reused), then the four token
 // reductions' slabs (kept until the call's final reduce).
@@ -78,11 +95,6 @@ MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r, int64_t n_ex = 0) {
   {
     Carve c(nullptr);
     c.take(kWsHeader);
-    c.take_n<bf16>(kfd * h);     // B_d^T
-    c.take_n<bf16>(kfd * i);     // s A_d
-    c.take_n<bf16>(kfg * i);     // B_g^T
-    c.take_n<bf16>(kfg * i);     // B_u^T
-    c.take_n<bf16>(kfg * h);     // s [A_g; A_u]
     c.take_n<bf16>(M * kfd);     // U_d
     c.take_n<bf16>(M * i);       // dg
     c.take_n<bf16>(M * i);       // du
@@ -101,6 +113,11 @@ MlpLayout mlp_layout(int64_t M, int64_t h, int64_t i, int r, int64_t n_ex = 0) {
     L.off_td = c.offset_of(sizeof(bf16) * M * kfd);
     L.ldt = round_up(M, 8);
     L.off_tgut = c.offset_of(sizeof(bf16) * kfg * L.ldt);
+    L.off_bt_d = c.offset_of(sizeof(bf16) * kfd * h);
+    L.off_af_d = c.offset_of(sizeof(bf16) * kfd * i);
+    L.off_bt_g = c.offset_of(sizeof(bf16) * kfg * i);
+    L.off_bt_u = c.offset_of(sizeof(bf16) * kfg * i);
+    L.off_af_gu = c.offset_of(sizeof(bf16) * kfg * h);
     L.saved = c.off;
   }
   return L;
@@ -182,6 +199,15 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
   pack_block(pack_job(pk, bf_u, i, kfg), up.B, r, 0, r, static_cast<int>(i), r, 0, s);
   pack_block(pack_job(pk, acat_d, kfd, i), down.A, i, 0, 0, r, static_cast<int>(i), 0, 1.0f);
   pack_block(pack_job(pk, bf_d, h, kfd), down.B, r, 0, 0, static_cast<int>(h), r, 0, s);
+  if (saved) {
+    // the backward's operands too (it reads them from saved, as autograd reads the
+    // tensors a forward saved)
+    uint8_t* sv = static_cast<uint8_t*>(saved);
+    const MlpBwdPack P = {reinterpret_cast<bf16*>(sv + L.off_bt_d), reinterpret_cast<bf16*>(sv + L.off_af_d),
+                          reinterpret_cast<bf16*>(sv + L.off_bt_g), reinterpret_cast<bf16*>(sv + L.off_bt_u),
+                          reinterpret_cast<bf16*>(sv + L.off_af_gu)};
+    pack_mlp_bwd(pk, P, gate, up, down, h, i, r, s, kfg, kfd);
+  }
   LGB_TRY(launch_pack(pk, stream));
 
   // T_gu = x [A_g; A_u]^T (saved also transposed where the backward's pass over dg, du
@@ -272,11 +298,11 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
 
   Carve c(ws);
   unsigned* status = static_cast<unsigned*>(c.take(kWsHeader));
-  bf16* bt_d = c.take_n<bf16>(kfd * h);
-  bf16* af_d = c.take_n<bf16>(kfd * i);
-  bf16* bt_g = c.take_n<bf16>(kfg * i);
-  bf16* bt_u = c.take_n<bf16>(kfg * i);
-  bf16* af_gu = c.take_n<bf16>(kfg * h);
+  const bf16* bt_d = reinterpret_cast<const bf16*>(sv + L.off_bt_d);
+  const bf16* af_d = reinterpret_cast<const bf16*>(sv + L.off_af_d);
+  const bf16* bt_g = reinterpret_cast<const bf16*>(sv + L.off_bt_g);
+  const bf16* bt_u = reinterpret_cast<const bf16*>(sv + L.off_bt_u);
+  const bf16* af_gu = reinterpret_cast<const bf16*>(sv + L.off_af_gu);
   bf16* ud = c.take_n<bf16>(M * kfd);
   bf16* dg = c.take_n<bf16>(M * i);
   bf16* du = c.take_n<bf16>(M * i);
@@ -286,18 +312,7 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   defer_init(dr, c.take_n<float>(mlp_bwd_slabs(M, h, i, r, kfd, kfg, n_ex)));
   const SkRegion sk = carve_sk(c, mlp_bwd_tiles(M, h, i));
 
-  PackParams pk;
-  std::memset(static_cast<void*>(&pk), 0, sizeof(pk));
-  pack_block(pack_job(pk, bt_d, kfd, h), down.B, r, 0, 0, r, static_cast<int>(h), 1, 1.0f);
-  pack_block(pack_job(pk, af_d, kfd, i), down.A, i, 0, 0, r, static_cast<int>(i), 0, s);
-  pack_block(pack_job(pk, bt_g, kfg, i), gate.B, r, 0, 0, r, static_cast<int>(i), 1, 1.0f);
-  pack_block(pack_job(pk, bt_u, kfg, i), up.B, r, r, 0, r, static_cast<int>(i), 1, 1.0f);
-  {
-    PackJob& J = pack_job(pk, af_gu, kfg, h);
-    pack_block(J, gate.A, h, 0, 0, r, static_cast<int>(h), 0, s);
-    pack_block(J, up.A, h, r, 0, r, static_cast<int>(h), 0, s);
-  }
-  LGB_TRY(launch_pack(pk, stream));
+  // the adapter operands come packed from the forward (saved)
 
   // U_d = dy B_d
   const ProjSeg p1 = {dy, bt_d, h};

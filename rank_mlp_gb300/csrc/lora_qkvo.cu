@@ -15,6 +15,8 @@ struct QkvoLayout {
   size_t ws_fwd, ws_bwd, saved, off_to;
   size_t off_tqkvt, off_tot;   // the rank-r projections transposed, [kf x ldt] (single passes
   int64_t ldt;                 // over dy_q, dy_k, dy_v and over dy_o in the backward)
+  // the backward's packed adapter operands, written by the forward's pack launch
+  size_t off_btq, off_btk, off_btv, off_afqkv, off_bto, off_afo;
 };
 
 // Single passes over the backward's gradients (dual_supported): the q/k/v half's three
@@ -87,12 +89,6 @@ QkvoLayout qkvo_layout(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r) {
   {
     Carve c(nullptr);
     c.take(kWsHeader);
-    c.take_n<bf16>(kfq * nq);
-    c.take_n<bf16>(kfq * nkv);
-    c.take_n<bf16>(kfq * nkv);
-    c.take_n<bf16>(kfq * h);
-    c.take_n<bf16>(kfo * h);
-    c.take_n<bf16>(kfo * nq);
     c.take_n<bf16>(M * kfo);
     c.take_n<bf16>(M * kfq);
     c.take_n<bf16>(M * nq);     // dy_q, dy_k turned back by the transpose RoPE rotation
@@ -109,6 +105,12 @@ QkvoLayout qkvo_layout(int64_t M, int64_t h, int64_t nq, int64_t nkv, int r) {
     L.ldt = round_up(M, 8);
     L.off_tqkvt = c.offset_of(sizeof(bf16) * kfq * L.ldt);
     L.off_tot = c.offset_of(sizeof(bf16) * kfo * L.ldt);
+    L.off_btq = c.offset_of(sizeof(bf16) * kfq * nq);
+    L.off_btk = c.offset_of(sizeof(bf16) * kfq * nkv);
+    L.off_btv = c.offset_of(sizeof(bf16) * kfq * nkv);
+    L.off_afqkv = c.offset_of(sizeof(bf16) * kfq * h);
+    L.off_bto = c.offset_of(sizeof(bf16) * kfo * h);
+    L.off_afo = c.offset_of(sizeof(bf16) * kfo * nq);
     L.saved = c.off;
   }
   return L;
@@ -207,6 +209,24 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
   if (o_in) {
     pack_block(pack_job(pk, acat_o, kfo, n_q), o.A, n_q, 0, 0, r, static_cast<int>(n_q), 0, 1.0f);
     pack_block(pack_job(pk, bf_o, h, kfo), o.B, r, 0, 0, static_cast<int>(h), r, 0, s);
+  }
+  if (saved) {
+    // the backward's operands too (it reads them from saved, as autograd reads the
+    // tensors a forward saved)
+    uint8_t* sv = static_cast<uint8_t*>(saved);
+    if (x) {
+      pack_block(pack_job(pk, sv + L.off_btq, kfq, n_q), q.B, r, 0, 0, r, static_cast<int>(n_q), 1, 1.0f);
+      pack_block(pack_job(pk, sv + L.off_btk, kfq, n_kv), k.B, r, r, 0, r, static_cast<int>(n_kv), 1, 1.0f);
+      pack_block(pack_job(pk, sv + L.off_btv, kfq, n_kv), v.B, r, 2 * r, 0, r, static_cast<int>(n_kv), 1, 1.0f);
+      PackJob& J = pack_job(pk, sv + L.off_afqkv, kfq, h);
+      pack_block(J, q.A, h, 0, 0, r, static_cast<int>(h), 0, s);
+      pack_block(J, k.A, h, r, 0, r, static_cast<int>(h), 0, s);
+      pack_block(J, v.A, h, 2 * r, 0, r, static_cast<int>(h), 0, s);
+    }
+    if (o_in) {
+      pack_block(pack_job(pk, sv + L.off_bto, kfo, h), o.B, r, 0, 0, r, static_cast<int>(h), 1, 1.0f);
+      pack_block(pack_job(pk, sv + L.off_afo, kfo, n_q), o.A, n_q, 0, 0, r, static_cast<int>(n_q), 0, s);
+    }
   }
   LGB_TRY(launch_pack(pk, stream));
 
@@ -310,12 +330,14 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
   const bf16* to_t = reinterpret_cast<const bf16*>(static_cast<const uint8_t*>(saved) + L.off_tot);
   Carve c(ws);
   unsigned* status = static_cast<unsigned*>(c.take(kWsHeader));
-  bf16* btq = c.take_n<bf16>(kfq * n_q);
-  bf16* btk = c.take_n<bf16>(kfq * n_kv);
-  bf16* btv = c.take_n<bf16>(kfq * n_kv);
-  bf16* af_qkv = c.take_n<bf16>(kfq * h);
-  bf16* bt_o = c.take_n<bf16>(kfo * h);
-  bf16* af_o = c.take_n<bf16>(kfo * n_q);
+  // the adapter operands come packed from the forward (saved)
+  const uint8_t* svb = static_cast<const uint8_t*>(saved);
+  const bf16* btq = reinterpret_cast<const bf16*>(svb + L.off_btq);
+  const bf16* btk = reinterpret_cast<const bf16*>(svb + L.off_btk);
+  const bf16* btv = reinterpret_cast<const bf16*>(svb + L.off_btv);
+  const bf16* af_qkv = reinterpret_cast<const bf16*>(svb + L.off_afqkv);
+  const bf16* bt_o = reinterpret_cast<const bf16*>(svb + L.off_bto);
+  const bf16* af_o = reinterpret_cast<const bf16*>(svb + L.off_afo);
   bf16* uo = c.take_n<bf16>(M * kfo);
   bf16* V = c.take_n<bf16>(M * kfq);
   bf16* dyq_r = c.take_n<bf16>(M * n_q);
@@ -325,22 +347,6 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
   defer_init(dr, c.take_n<float>(qkvo_bwd_slabs(M, h, n_q, n_kv, r, kfq, kfo)));
   const SkRegion sk = carve_sk(c, qkvo_bwd_tiles(M, h, n_q));
 
-  PackParams pk;
-  std::memset(static_cast<void*>(&pk), 0, sizeof(pk));
-  if (x) {
-    pack_block(pack_job(pk, btq, kfq, n_q), q.B, r, 0, 0, r, static_cast<int>(n_q), 1, 1.0f);
-    pack_block(pack_job(pk, btk, kfq, n_kv), k.B, r, r, 0, r, static_cast<int>(n_kv), 1, 1.0f);
-    pack_block(pack_job(pk, btv, kfq, n_kv), v.B, r, 2 * r, 0, r, static_cast<int>(n_kv), 1, 1.0f);
-    PackJob& J = pack_job(pk, af_qkv, kfq, h);
-    pack_block(J, q.A, h, 0, 0, r, static_cast<int>(h), 0, s);
-    pack_block(J, k.A, h, r, 0, r, static_cast<int>(h), 0, s);
-    pack_block(J, v.A, h, 2 * r, 0, r, static_cast<int>(h), 0, s);
-  }
-  if (o_in) {
-    pack_block(pack_job(pk, bt_o, kfo, h), o.B, r, 0, 0, r, static_cast<int>(h), 1, 1.0f);
-    pack_block(pack_job(pk, af_o, kfo, n_q), o.A, n_q, 0, 0, r, static_cast<int>(n_q), 0, s);
-  }
-  LGB_TRY(launch_pack(pk, stream));
 
   if (o_in) {
     const bool dual = o_dual(r, kfo);
