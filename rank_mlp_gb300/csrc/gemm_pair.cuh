@@ -379,8 +379,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
   cluster_sync_all();                     // both CTAs' barriers exist before any remote arrive
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();                             // the previous kernel's writes are visible from here
-  pdl_launch_dependents();
+  if (p.pdl_seg == 0) {
+    pdl_wait();                           // the previous kernel's writes are visible from here
+    pdl_launch_dependents();
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -391,6 +393,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
       for (int s = 0; s < STAGES; ++s) armed[s] = -1;
       bool ok = true;
       bool first_stage = true;
+      bool waited = p.pdl_seg == 0;
       WorkIter it(p, pair, npairs);
       Unit U;
       while (ok && it.next(p, U)) {
@@ -407,6 +410,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
           const int a_row = U.tm * (2 * kBM) + static_cast<int>(rank) * kBM;
           const int b_row = (b1 >= 0) ? U.tn * C::kBLocal : U.tn * BN + static_cast<int>(rank) * C::kBLocal;
           seg_base += nkb;
+          if (!waited && sg >= p.pdl_seg && j0 < j1) {   // the previous kernel's rank-r operand
+            pdl_wait();
+            // dependents start only after this wait, so that a late-starting one (which
+            // reads earlier kernels' outputs at once) finds everything before this
+            // kernel complete
+            pdl_launch_dependents();
+            waited = true;
+          }
           for (int j = j0; j < j1; ++j) {
             const int kc = j * kBK;
             if (!wait_phase(empty_bar(stage), phase ^ 1u, abort_flag, p)) { ok = false; break; }
@@ -556,6 +567,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
   }
 
   if (*abort_flag) settle_after_abort();
+  if (p.pdl_seg > 0) pdl_wait();          // complete only after the previous kernel
   __syncwarp();
   tc_fence_before_sync();
   cluster_sync_all();                     // no remote arrive or MMA read of either CTA is pending

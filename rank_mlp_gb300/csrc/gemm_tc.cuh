@@ -89,6 +89,12 @@ struct TcParams {
   // nothing it reads, so it starts at once (on SMs the previous kernel has freed) and
   // waits for that kernel only before it exits, keeping the stream's completion order
   int pdl_late;
+  // CTA-pair kernel, > 0: only the K-segments from this index on read what the previous
+  // kernel writes (a rank-r operand), and nothing else of the launch touches its data:
+  // the producers wait for it just before their first load from such a segment (and
+  // only then let the next kernel launch), every thread again before it exits, so the
+  // earlier segments' copies and MMAs overlap the previous kernel's tail
+  int pdl_seg;
   // Split tail (CTA-pair kernel).  Units [0, sk_dp_units) are whole tiles dealt
   // round-robin to the pairs.  The sk_tail tiles after them, which would fill only part
   // of a last wave, are each cut into sk_splits equal k-ranges (of sk_kb k-blocks in

@@ -124,6 +124,7 @@ static lora_status_t linear_forward_impl(int64_t M, int64_t in, int64_t out, int
   G.out0 = y;
   G.ldo = out;
   g.p.status = status;
+  g.p.pdl_seg = 1;   // segments from 1 on read the previous kernel's rank-r output
   g.finish();
   g.split_tail(sk);
   if (!g.ok) return LORA_ERR_CUDA;
@@ -192,6 +193,7 @@ extern "C" lora_status_t lora_linear_backward(int64_t M, int64_t in, int64_t out
   G.out0 = dx;
   G.ldo = in;
   g.p.status = status;
+  g.p.pdl_seg = 1;   // segments from 1 on read the previous kernel's rank-r output
   g.finish();
   g.split_tail(sk);
   if (!g.ok) return LORA_ERR_CUDA;

@@ -230,6 +230,7 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
     G.ldo = i;
     g.p.act = static_cast<int>(act);
     g.p.status = status;
+    g.p.pdl_seg = 1;   // segments from 1 on read the previous kernel's rank-r output
     g.finish();
     g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
@@ -248,6 +249,7 @@ extern "C" lora_status_t lora_mlp_forward(int64_t M, int64_t h, int64_t i, int r
   G.out0 = y;
   G.ldo = h;
   g.p.status = status;
+  g.p.pdl_seg = 1;   // segments from 1 on read the previous kernel's rank-r output
   g.finish();
   g.split_tail(sk);
   if (!g.ok) return LORA_ERR_CUDA;
@@ -343,6 +345,7 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
     }
     g.p.act = static_cast<int>(act);
     g.p.status = status;
+    g.p.pdl_seg = 1;   // segments from 1 on read the previous kernel's rank-r output
     g.finish();
     if (!staged) g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
@@ -376,6 +379,7 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
     G.out0 = dx;
     G.ldo = h;
     g.p.status = status;
+    g.p.pdl_seg = 2;   // segments from 2 on read the previous kernel's rank-r output
     g.finish();
     g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;

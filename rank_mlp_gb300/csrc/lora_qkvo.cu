@@ -258,6 +258,7 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
       if (bias_qkv != nullptr) G.in0 = static_cast<const bf16*>(bias_qkv) + (p == 0 ? 0 : n_q + (p - 1) * n_kv);
     }
     g.p.status = status;
+    g.p.pdl_seg = 1;   // segments from 1 on read the previous kernel's rank-r output
     g.finish();
     g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
@@ -273,6 +274,7 @@ extern "C" lora_status_t lora_qkvo_forward(int64_t M, int64_t h, int64_t n_q, in
     G.out0 = yo;
     G.ldo = h;
     g.p.status = status;
+    g.p.pdl_seg = 1;   // segments from 1 on read the previous kernel's rank-r output
     g.finish();
     g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
@@ -365,6 +367,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     G.out0 = do_in;
     G.ldo = n_q;
     g.p.status = status;
+    g.p.pdl_seg = 1;   // segments from 1 on read the previous kernel's rank-r output
     g.finish();
     g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
@@ -416,6 +419,7 @@ extern "C" lora_status_t lora_qkvo_backward(int64_t M, int64_t h, int64_t n_q, i
     G.out0 = dx;
     G.ldo = h;
     g.p.status = status;
+    g.p.pdl_seg = 3;   // segments from 3 on read the previous kernel's rank-r output
     g.finish();
     g.split_tail(sk);
     if (!g.ok) return LORA_ERR_CUDA;
