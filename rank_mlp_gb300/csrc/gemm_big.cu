@@ -5,10 +5,10 @@
 
 namespace lgb {
 
-template <int STAGES, bool B_MN, int EPIW, int ACTB = 0>
+template <int STAGES, bool B_MN, int EPIW, int ACTB = 0, int ECOLS = 16>
 static cudaError_t launch_pair(const TcParams& p, int grid, cudaStream_t st) {
-  auto* k = tc_gemm_pair_kernel<STAGES, B_MN, EPIW, ACTB>;
-  constexpr int smem = PairCfg<STAGES, EPIW, ACTB >= 2 ? ACTB : 0>::kSmemBytes;
+  auto* k = tc_gemm_pair_kernel<STAGES, B_MN, EPIW, ACTB, ECOLS>;
+  constexpr int smem = PairCfg<STAGES, EPIW, ACTB >= 2 ? ACTB : 0, ECOLS>::kSmemBytes;
   static std::atomic<unsigned long long> configured{0};
   const cudaError_t e = ensure_smem_limit(k, smem, configured);
   if (e != cudaSuccess) return e;
@@ -24,7 +24,8 @@ cudaError_t launch_tc_big(int variant, const TcParams& p, int grid, cudaStream_t
     case VP_KMN: return launch_pair<6, true, 8>(p, grid, st);
     // act': g, u in and dg, du out one row per thread, or through shared memory (short K)
     case VP_KMN_ACT: return launch_pair<6, true, 8, 1>(p, grid, st);
-    case VP_KMN_ACT16: return launch_pair<5, true, 8, 4>(p, grid, st);
+    case VP_KMN_ACT16:
+      return launch_pair<kActStagedStages, true, kActStagedWarps, kActStagedSlots, kActStagedCols>(p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

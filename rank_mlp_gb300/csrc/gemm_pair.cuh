@@ -20,15 +20,14 @@ namespace lgb {
 constexpr int pair_threads(int epiw) { return 64 + 32 * epiw; }
 
 // Staged epilogue (the activation-derivative GEMM): each epilogue warp owns a ring of
-// SLOTS slots in shared memory; a slot holds one chunk (the warp's 32 rows x 16 columns)
-// of g and of u, loaded by TMA, and then the chunk's dg and du, written in place and
-// stored by TMA.
-constexpr int kEpiCols = 16;
-constexpr int kEpiTensorBytes = 32 * kEpiCols * 2;   // 1 KB: one tensor's chunk
-constexpr int kEpiSlotBytes = 2 * kEpiTensorBytes;
+// SLOTS slots in shared memory; a slot holds one chunk (the warp's 32 rows x ECOLS
+// columns) of g and of u, loaded by TMA, and then the chunk's dg and du, written in
+// place and stored by TMA.
+constexpr int epi_tensor_bytes(int ecols) { return 32 * ecols * 2; }   // one tensor's chunk
+constexpr int epi_slot_bytes(int ecols) { return 2 * epi_tensor_bytes(ecols); }
 
-// STAGED = 0 (plain epilogues) or the staged epilogue's slots per warp.
-template <int STAGES, int EPIW = 4, int STAGED = 0>
+// STAGED = 0 (plain epilogues) or the staged epilogue's slots per warp, of ECOLS columns.
+template <int STAGES, int EPIW = 4, int STAGED = 0, int ECOLS = 16>
 struct PairCfg {
   static constexpr int BN = 256;                       // accumulator columns per tile
   static constexpr int kBLocal = BN / 2;               // B rows held by each CTA
@@ -37,7 +36,7 @@ struct PairCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTxBytes = 2 * kStageBytes;     // both CTAs, counted on the even CTA
   static constexpr int kTmemCols = 512;
-  static constexpr int kEpiBytes = EPIW * STAGED * kEpiSlotBytes;
+  static constexpr int kEpiBytes = EPIW * STAGED * epi_slot_bytes(ECOLS);
   static constexpr int kNumBars = 2 * STAGES + 5 + EPIW * STAGED;
   static constexpr int kBarBytes = 8 * kNumBars + 16;
   static constexpr int kSmemBytes = STAGES * kStageBytes + kEpiBytes + kBarBytes + 1024;
@@ -173,11 +172,10 @@ __device__ __forceinline__ bool sk_piece_arrive(const TcParams& p, const GroupDe
 // Kernels", activation table: the derivative of the activation, recomputed from the
 // saved g): d the accumulator (dh), gw, uw the saved bf16 pairs; results as bf16 pairs.
 template <int ACT>
-__device__ __forceinline__ void act_bwd_cols(const uint32_t (&d)[kEpiCols], const uint32_t (&gw)[kEpiCols / 2],
-                                             const uint32_t (&uw)[kEpiCols / 2], uint32_t (&dg)[kEpiCols / 2],
-                                             uint32_t (&du)[kEpiCols / 2]) {
+__device__ __forceinline__ void act_bwd_cols(const uint32_t* d, const uint32_t (&gw)[8], const uint32_t (&uw)[8],
+                                             uint32_t (&dg)[8], uint32_t (&du)[8]) {
 #pragma unroll
-  for (int e = 0; e < kEpiCols / 2; ++e) {
+  for (int e = 0; e < 8; ++e) {
     float a0, ap0, a1, ap1;
     const float g0 = bf16_lo(gw[e]), g1 = bf16_hi(gw[e]);
     const float u0 = bf16_lo(uw[e]), u1 = bf16_hi(uw[e]);
@@ -191,27 +189,29 @@ __device__ __forceinline__ void act_bwd_cols(const uint32_t (&d)[kEpiCols], cons
 
 // The staged activation-derivative epilogue of one epilogue warp (its TMEM lane
 // quarter q = warp & 3, its share of the tile's columns), for all its units.  The
-// warp walks its chunks of 32 rows x 16 columns in order across tiles; lane 0 keeps
+// warp walks its chunks of 32 rows x COLS columns in order across tiles; lane 0 keeps
 // the TMA loads of g, u SLOTS - 1 chunks ahead (into the slot whose dg, du store has
 // finished reading it), so the next tile's first loads fly while the warp waits for
 // that tile's accumulator.  Each chunk: wait for its slot, read dh from TMEM, compute,
 // write dg, du over g, u, make them visible to TMA and store both.  The accumulator is
 // released as soon as the tile's last chunk has been read from TMEM.  Rows past M and
 // columns past N are zero-filled by the loads and dropped by the stores.  The chunk's
-// 32-byte rows sit in the 32-byte swizzle.
-template <int STAGES, int EPIW, int SLOTS>
+// rows (2 COLS bytes) sit in the swizzle of their width: 16-byte unit j of row r at
+// unit j ^ (r >> 2 & 1) for 32-byte rows, j ^ (r >> 1 & 3) for 64-byte rows.
+template <int STAGES, int EPIW, int SLOTS, int COLS>
 __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_smem, uint32_t epi_bar0,
                                                uint32_t tfull0, const uint32_t (&tempty_even)[2], uint32_t tmem_base,
                                                volatile int* abort_flag, uint32_t rank, int pair, int npairs,
                                                int warp) {
-  static_assert(SLOTS == 2 || SLOTS == 4, "ring slots");
-  constexpr int COLS = kEpiCols;
+  static_assert(SLOTS >= 2 && SLOTS <= 8, "ring slots");
+  static_assert(COLS == 16 || COLS == 32, "chunk columns");
   constexpr int BN = 256;
   constexpr int kParts = EPIW / 4;
   constexpr int kSpan = BN / kParts;                   // columns per warp
   constexpr int kChunks = kSpan / COLS;                // chunks per warp per tile
-  constexpr int kTensorBytes = kEpiTensorBytes;
-  constexpr int kSlotBytes = kEpiSlotBytes;
+  constexpr int kTensorBytes = epi_tensor_bytes(COLS);
+  constexpr int kSlotBytes = epi_slot_bytes(COLS);
+  constexpr int kHalves = COLS / 16;                   // 16-column pieces of a chunk
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;
   const int widx = warp - 2;
@@ -219,11 +219,9 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
   const uint32_t ring = epi_smem + static_cast<uint32_t>(widx) * (SLOTS * kSlotBytes);
   auto slot = [&](uint32_t n) { return ring + (n % SLOTS) * kSlotBytes; };
   auto full = [&](uint32_t n) { return epi_bar0 + 8u * (widx * SLOTS + n % SLOTS); };
-  // this lane's row inside a chunk box and its 16-byte halves (32-byte swizzle: half j
-  // of row r sits at j ^ bit 2 of r)
-  const uint32_t sw = (static_cast<uint32_t>(lane) >> 2) & 1u;
-  const uint32_t off0 = lane * 32u + (sw << 4);
-  const uint32_t off1 = lane * 32u + ((sw ^ 1u) << 4);
+  // this lane's row inside a chunk box and where its 16-byte units sit (the swizzle)
+  const uint32_t sw = COLS == 16 ? (static_cast<uint32_t>(lane) >> 2) & 1u : (static_cast<uint32_t>(lane) >> 1) & 3u;
+  auto unit_off = [&](int j) { return static_cast<uint32_t>(lane) * (2u * COLS) + ((static_cast<uint32_t>(j) ^ sw) << 4); };
 
   // the loading cursor: unit and chunk of the next load
   WorkIter ahead(p, pair, npairs);
@@ -266,7 +264,11 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
       const int col = part * kSpan + c * COLS;
       uint32_t d[COLS];
       __syncwarp();
-      tmem_ld16(tacc + col, d);
+      if constexpr (COLS == 16) {
+        tmem_ld16(tacc + col, d);
+      } else {
+        tmem_ld32(tacc + col, d);
+      }
       const bool landed = wait_phase(full(used), (used / SLOTS) & 1u, abort_flag, p);
       tmem_ld_wait();
       if (c == kChunks - 1) {        // the accumulator is no longer needed: hand it back
@@ -276,16 +278,20 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
       }
       if (!__all_sync(0xffffffffu, landed)) { ok = false; break; }
       const uint32_t s0 = slot(used);
-      const uint4 g0 = ld_shared_v4(s0 + off0), g1 = ld_shared_v4(s0 + off1);
-      const uint4 u0 = ld_shared_v4(s0 + kTensorBytes + off0), u1 = ld_shared_v4(s0 + kTensorBytes + off1);
-      const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-      const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-      uint32_t dg[8], du[8];
-      act_chunk(p.act, [&](auto tag) { act_bwd_cols<decltype(tag)::value>(d, gw, uw, dg, du); });
-      st_shared_v4(s0 + off0, make_uint4(dg[0], dg[1], dg[2], dg[3]));
-      st_shared_v4(s0 + off1, make_uint4(dg[4], dg[5], dg[6], dg[7]));
-      st_shared_v4(s0 + kTensorBytes + off0, make_uint4(du[0], du[1], du[2], du[3]));
-      st_shared_v4(s0 + kTensorBytes + off1, make_uint4(du[4], du[5], du[6], du[7]));
+#pragma unroll
+      for (int h = 0; h < kHalves; ++h) {
+        const uint32_t off0 = unit_off(2 * h), off1 = unit_off(2 * h + 1);
+        const uint4 g0 = ld_shared_v4(s0 + off0), g1 = ld_shared_v4(s0 + off1);
+        const uint4 u0 = ld_shared_v4(s0 + kTensorBytes + off0), u1 = ld_shared_v4(s0 + kTensorBytes + off1);
+        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        uint32_t dg[8], du[8];
+        act_chunk(p.act, [&](auto tag) { act_bwd_cols<decltype(tag)::value>(d + 16 * h, gw, uw, dg, du); });
+        st_shared_v4(s0 + off0, make_uint4(dg[0], dg[1], dg[2], dg[3]));
+        st_shared_v4(s0 + off1, make_uint4(dg[4], dg[5], dg[6], dg[7]));
+        st_shared_v4(s0 + kTensorBytes + off0, make_uint4(du[0], du[1], du[2], du[3]));
+        st_shared_v4(s0 + kTensorBytes + off1, make_uint4(du[4], du[5], du[6], du[7]));
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -323,15 +329,15 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
 // ACTB selects the epilogues compiled in: 0 the plain, activation, RoPE and partial
 // epilogues (epilogue_tile); the activation-derivative GEMM (every group EPI_ACT_BWD)
 // has variants of its own: 1 reads g, u and writes dg, du one row per thread
-// (epilogue_act_bwd_rows); 4 moves them through the epilogue warps' shared-memory
-// rings of 4 slots of 16 columns (staged_act_bwd; whole tiles only).
-template <int STAGES, bool B_MN, int EPIW, int ACTB = 0>
+// (epilogue_act_bwd_rows); 2-8 moves them through the epilogue warps' shared-memory
+// rings of that many slots of ECOLS columns (staged_act_bwd; whole tiles only).
+template <int STAGES, bool B_MN, int EPIW, int ACTB = 0, int ECOLS = 16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 1)
     tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
   static_assert(EPIW == 4 || EPIW == 8, "epilogue warps");
-  static_assert(ACTB == 0 || ACTB == 1 || ACTB == 4, "epilogue selection");
+  static_assert(ACTB >= 0 && ACTB <= 8, "epilogue selection");
   constexpr int STAGED = ACTB >= 2 ? ACTB : 0;
-  using C = PairCfg<STAGES, EPIW, STAGED>;
+  using C = PairCfg<STAGES, EPIW, STAGED, ECOLS>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -533,7 +539,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads(EPIW), 
     const int row_in_tile = q * 32 + lane;
     const uint32_t tempty_even[2] = {mapa_shared(tempty_bar(0), 0), mapa_shared(tempty_bar(1), 0)};
     if constexpr (STAGED) {
-      staged_act_bwd<STAGES, EPIW, STAGED>(p, sbase + STAGES * C::kStageBytes, bar0 + 8u * (2 * STAGES + 5),
+      staged_act_bwd<STAGES, EPIW, STAGED, ECOLS>(p, sbase + STAGES * C::kStageBytes, bar0 + 8u * (2 * STAGES + 5),
                                    tfull_bar(0), tempty_even, tmem_base, abort_flag, rank, pair, npairs, warp);
     } else {
     int acc = 0;

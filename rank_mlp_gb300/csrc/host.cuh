@@ -32,7 +32,7 @@ enum Variant : int {
   VP_KMN_ACT = 7,   // VP_KMN for the activation-derivative GEMM: saved g, u in and dg, du out
                     // one row per thread (6 stages)
   VP_KMN_ACT16 = 8, // the same for short K: g, u and dg, du through shared memory by TMA
-                    // in 16-column chunks, rings of 4 slots (5 stages leave room for them)
+                    // (kActStaged* below)
   kNumVariants = 9
 };
 
@@ -42,6 +42,17 @@ enum Variant : int {
 // the MMAs fed (measured: the staged variant at 5 stages, or at 6 stages with 8-column
 // chunks or with 2-slot rings, was 3-15% slower there than one row per thread).
 constexpr int kActShortKBlocks = 32;
+
+// VP_KMN_ACT16's shape: mainloop stages, epilogue warps, ring slots per epilogue warp
+// and columns per chunk (a chunk is one warp's 32 rows; 32 columns make 64-byte rows, so
+// that each TMA copy moves twice the bytes of a 16-column chunk).  Measured on the
+// 0.5B-shaped act' GEMM (15 k-blocks a tile): 5 stages with two 32-column slots 59.3 us
+// against 61.6 us for four 16-column slots; 4 or 3 stages with 3 or 4 such slots were no
+// faster than the 16-column ring, so the mainloop's fifth stage matters more than depth.
+constexpr int kActStagedStages = 5;
+constexpr int kActStagedWarps = 8;
+constexpr int kActStagedSlots = 2;
+constexpr int kActStagedCols = 32;
 
 // A forward pair launch whose longest K is at most this many 64-wide k-blocks runs
 // VP_KK8: a tile's MMAs (~0.28 us per k-block) then no longer cover the 4-warp
@@ -283,9 +294,9 @@ struct GemmPlan {
     return p.nmaps++;
   }
   // An epilogue operand or output [rows x cols] (row stride ld) moved by TMA in boxes of
-  // 32 rows x 16 columns (one warp's rows, 32 bytes of each), 32-byte swizzle.
+  // 32 rows x kActStagedCols columns (one warp's rows), in the swizzle of that row width.
   int epi_map(const void* base, int64_t rows, int64_t cols, int64_t ld) {
-    return add_map(base, cols, rows, ld, 16, 32, 32);
+    return add_map(base, cols, rows, ld, kActStagedCols, 32, 2 * kActStagedCols);
   }
   // A operand, K-major: activation [rows x K] with row stride ld.
   int a_kmajor(const void* base, int64_t rows, int64_t K, int64_t ld) {

@@ -52,7 +52,7 @@ static void bind_current_device() {
   if (cudaGetDevice(&dev) == cudaSuccess && dev != bound && cudaSetDevice(dev) == cudaSuccess) bound = dev;
 }
 
-// 2-D bf16 map with a 128-byte, 32-byte or no swizzle (swizzle_bytes 128, 32, 0);
+// 2-D bf16 map with a 128-byte, 64-byte, 32-byte or no swizzle (swizzle_bytes 128, 64, 32, 0);
 // out-of-bounds elements read as zero.
 bool encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
                 uint32_t box_inner, uint32_t box_outer, int swizzle_bytes) {
@@ -66,6 +66,7 @@ bool encode_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE,
             swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+            : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
             : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
                                   : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
