@@ -72,6 +72,7 @@ struct GradJob {
   void* dst;
   int trans;          // 1: dst is [r x f] (dA), 0: dst is [f x r] (dB)
   const void* T;      // [M x kf] token-major rank-r operand
+  int kf = 0;         // T's padded width when it differs from the call's kf (0: the call's)
 };
 // f32 slab elements of the token reductions of n products (fs[j] features each).
 // n_ex > 0: per-example mode, one slab per example.

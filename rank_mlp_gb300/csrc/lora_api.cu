@@ -413,7 +413,10 @@ lora_status_t token_grads(int64_t M, int r, int kf, float s, const GradJob* jobs
   float* parts[kMaxGroups];
   float* cur = defer.cursor;
   const int slab_splits = n_ex > 0 ? static_cast<int>(n_ex) : max_splits(ceil_div(M, kBK));
+  int kfs[kMaxGroups];
   for (int j = 0; j < njobs; ++j) {
+    const int kfj = jobs[j].kf > 0 ? jobs[j].kf : kf;
+    if (kfj > kf) return LORA_ERR_UNSUPPORTED;   // not reached: the call's kf is the widest
     int gi = -1;
     for (int q = 0; q < nq; ++q)
       if (qs[q] == jobs[j].Q && ts[q] == jobs[j].T) gi = q;
@@ -424,15 +427,15 @@ lora_status_t token_grads(int64_t M, int r, int kf, float s, const GradJob* jobs
       for (int k = 0; k < nt; ++k)
         if (tmap_src[k] == jobs[j].T) tm = tmap_of[k];
       if (tm < 0) {
-        tm = n_ex > 0 ? g.b_mnmajor_planes(jobs[j].T, kf, seq, n_ex, kf) : g.b_mnmajor(jobs[j].T, kf, M, kf);
+        tm = n_ex > 0 ? g.b_mnmajor_planes(jobs[j].T, kfj, seq, n_ex, kfj) : g.b_mnmajor(jobs[j].T, kfj, M, kfj);
         tmap_src[nt] = jobs[j].T;
         tmap_of[nt++] = tm;
       }
       gi = nq++;
       qs[gi] = jobs[j].Q;
       ts[gi] = jobs[j].T;
-      const int64_t tiles = ceil_div(jobs[j].f, kBM) * ceil_div(kf, g.bn);
-      GroupDesc& G = g.group(static_cast<int>(jobs[j].f), kf, EPI_PARTIAL, false);
+      const int64_t tiles = ceil_div(jobs[j].f, kBM) * ceil_div(kfj, g.bn);
+      GroupDesc& G = g.group(static_cast<int>(jobs[j].f), kfj, EPI_PARTIAL, false);
       if (n_ex > 0) {
         G.splits = static_cast<int>(n_ex);
         G.per_plane = 1;
@@ -445,7 +448,8 @@ lora_status_t token_grads(int64_t M, int r, int kf, float s, const GradJob* jobs
       }
       G.part = cur;
       parts[gi] = cur;
-      cur += round_up(partial_elems(jobs[j].f, kf, g.bn, slab_splits), 64);
+      kfs[gi] = kfj;
+      cur += round_up(partial_elems(jobs[j].f, kfj, g.bn, slab_splits), 64);
     }
     group_of[j] = gi;
   }
@@ -460,7 +464,7 @@ lora_status_t token_grads(int64_t M, int r, int kf, float s, const GradJob* jobs
     o.part = parts[group_of[j]];
     o.rows = static_cast<int>(jobs[j].f);
     o.rows_pad = round_up(jobs[j].f, kBM);
-    o.width = static_cast<int>(round_up(kf, g.bn));
+    o.width = static_cast<int>(round_up(kfs[group_of[j]], g.bn));
     o.splits = g.p.grp[group_of[j]].splits;
     o.per_split = n_ex > 0 ? 1 : 0;
     o.scale = s;

@@ -352,11 +352,15 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
     LGB_TRY(launch_gemm(variant, g.p, LORA_KIND_ACT_BWD, stream));
   }
 
-  // dB_d = s dy^T T_d and dA_d = s U_d^T h (one launch) read nothing the dh GEMM writes:
-  // they start on the SMs its last wave leaves idle.  (A single pass over dy for U_d and
-  // dB_d, as for dg, du below, measured no better: dy is a quarter of dg, du's bytes.)
-  const GradJob j1[2] = {{dy, h, 0, d_down.dB, 0, td}, {hsv, i, 0, d_down.dA, 1, ud}};
-  LGB_TRY(token_grads(M, r, kfd, s, j1, 2, dr, status, stream, n_ex, true));
+  // dB_d = s dy^T T_d and dA_d = s U_d^T h read nothing the dh GEMM writes.  With the
+  // one pass over dg, du below they join the launch after the dx GEMM (one launch
+  // fewer; on the 0.5B shape, whose dx GEMM leaves 24 SMs idle throughout, step -1.9%);
+  // otherwise they take a launch of their own here, which starts on the SMs the dh
+  // GEMM's last wave leaves idle.  (A single pass over dy for U_d and dB_d, as for dg,
+  // du below, measured no better: dy is a quarter of dg, du's bytes.)
+  const GradJob j1[2] = {{dy, h, 0, d_down.dB, 0, td, kfd}, {hsv, i, 0, d_down.dA, 1, ud, kfd}};
+  const bool merge_j1 = dual && skinny_bn(kfd) == skinny_bn(kfg);
+  if (!merge_j1) LGB_TRY(token_grads(M, r, kfd, s, j1, 2, dr, status, stream, n_ex, true));
 
   if (dual) {
     // V = [dg B_g | du B_u], dB_g = s dg^T T_g and dB_u = s du^T T_u in one pass over dg, du
@@ -387,11 +391,16 @@ static lora_status_t mlp_backward_impl(int64_t M, int64_t h, int64_t i, int r, f
   }
 
   // dA_g = s V_g^T x, dA_u = s V_u^T x (and dB_g = s dg^T T_g, dB_u = s du^T T_u when
-  // the pass over dg, du has not made them) in one launch: they read nothing the dx GEMM
-  // writes and start on the SMs its last wave leaves idle
+  // the pass over dg, du has not made them, or dB_d, dA_d when it has) in one launch:
+  // they read nothing the dx GEMM writes and start on the SMs its last wave leaves idle
   const GradJob j3[4] = {{dg, i, 0, d_gate.dB, 0, tgu}, {du, i, r, d_up.dB, 0, tgu},
                          {x, h, 0, d_gate.dA, 1, V}, {x, h, r, d_up.dA, 1, V}};
-  LGB_TRY(token_grads(M, r, kfg, s, dual ? j3 + 2 : j3, dual ? 2 : 4, dr, status, stream, n_ex, true));
+  if (merge_j1) {
+    const GradJob jm[4] = {j1[0], j1[1], j3[2], j3[3]};
+    LGB_TRY(token_grads(M, r, kfg, s, jm, 4, dr, status, stream, n_ex, true));
+  } else {
+    LGB_TRY(token_grads(M, r, kfg, s, dual ? j3 + 2 : j3, dual ? 2 : 4, dr, status, stream, n_ex, true));
+  }
   LGB_TRY(defer_flush(dr, stream));
   if (n_ex > 0 && sq_norms != nullptr) {
     NormParams np;
