@@ -19,6 +19,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -576,6 +577,16 @@ OTHER_WORKLOADS = (
 )
 
 
+# Warm-up work before each other workload's timed region: at least 3 steps and about
+# this many TFLOP, so that a small workload (a 0.5B-shaped step is ~0.22 TFLOP) runs
+# at the clocks it settles at rather than those the larger workload before it left.
+OTHER_WARMUP_TFLOP = 40.0
+
+
+def other_warmup_steps(total_flops: float) -> int:
+    return max(3, int(math.ceil(OTHER_WARMUP_TFLOP * 1e12 / total_flops)))
+
+
 def other_workloads(lib, args, world, device, stream):
     """Device-timed fwd+bwd of the other workloads (no oracle, no end-to-end copies),
     each with its own untraced timed region, under one clock record."""
@@ -600,16 +611,18 @@ def other_workloads(lib, args, world, device, stream):
             cfg = synth.QKVO_CONFIGS[name]
             w = qkvo_workload(lib, cfg, device, args.seed, rope=over.get("rope", False))
             desc = qkvo_name(cfg, over.get("rope", False))
-        m = measure(lib, w, steps, 3, world, device, stream, 0)
+        warm = other_warmup_steps(w.total_flops)
+        m = measure(lib, w, steps, warm, world, device, stream, 0)
         pf, _, _ = peak_fields(m.tflops, m.secs)
         out[label] = {"workload": desc, "ms_per_step": m.ms_step, "tokens_per_s": world * w.M / (m.ms_step * 1e-3),
                       "tflops": m.tflops, "pct_of_peak": pf["pct_of_peak"], "peak_tflops": pf["peak_tflops"],
-                      "steps": steps, "gpu_launches": m.launches}
+                      "steps": steps, "warmup": warm, "gpu_launches": m.launches}
         del w
         torch.cuda.empty_cache()
     out["clocks"] = clocks.stop() if rank == 0 else None
-    out["note"] = (f"each: 3 warm-up and {steps} untraced timed steps on device-resident inputs; pct_of_peak "
-                   "against the measured bf16 peak that applies to its timed region")
+    out["note"] = (f"each: warm-up of at least 3 steps and {OTHER_WARMUP_TFLOP:g} TFLOP (its 'warmup'), then "
+                   f"{steps} untraced timed steps on device-resident inputs; pct_of_peak against the measured "
+                   "bf16 peak that applies to its timed region")
     return out
 
 

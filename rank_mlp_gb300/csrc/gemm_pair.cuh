@@ -196,22 +196,20 @@ __device__ __forceinline__ void act_bwd_cols(const uint32_t* d, const uint32_t (
 // write dg, du over g, u, make them visible to TMA and store both.  The accumulator is
 // released as soon as the tile's last chunk has been read from TMEM.  Rows past M and
 // columns past N are zero-filled by the loads and dropped by the stores.  The chunk's
-// rows (2 COLS bytes) sit in the swizzle of their width: 16-byte unit j of row r at
-// unit j ^ (r >> 2 & 1) for 32-byte rows, j ^ (r >> 1 & 3) for 64-byte rows.
+// 64-byte rows sit in the 64-byte swizzle: 16-byte unit j of row r at unit j ^ (r >> 1 & 3).
 template <int STAGES, int EPIW, int SLOTS, int COLS>
 __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_smem, uint32_t epi_bar0,
                                                uint32_t tfull0, const uint32_t (&tempty_even)[2], uint32_t tmem_base,
                                                volatile int* abort_flag, uint32_t rank, int pair, int npairs,
                                                int warp) {
   static_assert(SLOTS >= 2 && SLOTS <= 8, "ring slots");
-  static_assert(COLS == 16 || COLS == 32, "chunk columns");
+  static_assert(COLS == 32, "chunk columns");
   constexpr int BN = 256;
   constexpr int kParts = EPIW / 4;
   constexpr int kSpan = BN / kParts;                   // columns per warp
   constexpr int kChunks = kSpan / COLS;                // chunks per warp per tile
   constexpr int kTensorBytes = epi_tensor_bytes(COLS);
   constexpr int kSlotBytes = epi_slot_bytes(COLS);
-  constexpr int kHalves = COLS / 16;                   // 16-column pieces of a chunk
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;
   const int widx = warp - 2;
@@ -220,7 +218,7 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
   auto slot = [&](uint32_t n) { return ring + (n % SLOTS) * kSlotBytes; };
   auto full = [&](uint32_t n) { return epi_bar0 + 8u * (widx * SLOTS + n % SLOTS); };
   // this lane's row inside a chunk box and where its 16-byte units sit (the swizzle)
-  const uint32_t sw = COLS == 16 ? (static_cast<uint32_t>(lane) >> 2) & 1u : (static_cast<uint32_t>(lane) >> 1) & 3u;
+  const uint32_t sw = (static_cast<uint32_t>(lane) >> 1) & 3u;
   auto unit_off = [&](int j) { return static_cast<uint32_t>(lane) * (2u * COLS) + ((static_cast<uint32_t>(j) ^ sw) << 4); };
 
   // the loading cursor: unit and chunk of the next load
@@ -259,39 +257,49 @@ __device__ __forceinline__ void staged_act_bwd(const TcParams& p, uint32_t epi_s
     tc_fence_after_sync();
     const uint32_t tacc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
     const int row0 = U.tm * (2 * kBM) + static_cast<int>(rank) * kBM + q * 32;
+    // dh is read from TMEM 16 columns at a time, each read issued one half-chunk ahead of
+    // its use, so that its latency overlaps the math of the half before
+    uint32_t dlo[16], dhi[16];
+    __syncwarp();
+    tmem_ld16(tacc + part * kSpan, dlo);
 #pragma unroll 1
     for (int c = 0; c < kChunks; ++c) {
       const int col = part * kSpan + c * COLS;
-      uint32_t d[COLS];
-      __syncwarp();
-      if constexpr (COLS == 16) {
-        tmem_ld16(tacc + col, d);
-      } else {
-        tmem_ld32(tacc + col, d);
-      }
       const bool landed = wait_phase(full(used), (used / SLOTS) & 1u, abort_flag, p);
-      tmem_ld_wait();
-      if (c == kChunks - 1) {        // the accumulator is no longer needed: hand it back
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(tempty_even[acc]);
+      tmem_ld_wait();                               // this chunk's first half
+      __syncwarp();
+      tmem_ld16(tacc + col + 16, dhi);
+      if (!__all_sync(0xffffffffu, landed)) {
+        tmem_ld_wait();
+        ok = false;
+        break;
       }
-      if (!__all_sync(0xffffffffu, landed)) { ok = false; break; }
       const uint32_t s0 = slot(used);
-#pragma unroll
-      for (int h = 0; h < kHalves; ++h) {
+      // dg, du of 16 columns (units 2h, 2h + 1 of the lane's row), written over g, u
+      auto half = [&](int h, const uint32_t (&d)[16]) {
         const uint32_t off0 = unit_off(2 * h), off1 = unit_off(2 * h + 1);
         const uint4 g0 = ld_shared_v4(s0 + off0), g1 = ld_shared_v4(s0 + off1);
         const uint4 u0 = ld_shared_v4(s0 + kTensorBytes + off0), u1 = ld_shared_v4(s0 + kTensorBytes + off1);
         const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
         uint32_t dg[8], du[8];
-        act_chunk(p.act, [&](auto tag) { act_bwd_cols<decltype(tag)::value>(d + 16 * h, gw, uw, dg, du); });
+        act_chunk(p.act, [&](auto tag) { act_bwd_cols<decltype(tag)::value>(d, gw, uw, dg, du); });
         st_shared_v4(s0 + off0, make_uint4(dg[0], dg[1], dg[2], dg[3]));
         st_shared_v4(s0 + off1, make_uint4(dg[4], dg[5], dg[6], dg[7]));
         st_shared_v4(s0 + kTensorBytes + off0, make_uint4(du[0], du[1], du[2], du[3]));
         st_shared_v4(s0 + kTensorBytes + off1, make_uint4(du[4], du[5], du[6], du[7]));
+      };
+      half(0, dlo);
+      tmem_ld_wait();                               // this chunk's second half
+      if (c + 1 < kChunks) {
+        __syncwarp();
+        tmem_ld16(tacc + col + COLS, dlo);          // the next chunk's first half
+      } else {                                      // the accumulator is no longer needed
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_even[acc]);
       }
+      half(1, dhi);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {

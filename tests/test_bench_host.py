@@ -36,3 +36,15 @@ def test_rank_override_keeps_the_scale():
     args = types.SimpleNamespace(workload="llama7b", act="geglu_erf", rank=0)
     cfg = bench.mlp_config(args)
     assert cfg.r == synth.MLP_CONFIGS["llama7b"].r and cfg.act == "geglu_erf"
+
+
+def test_other_workloads_warm_up_by_work():
+    """Each other workload warms up for at least 3 steps and about OTHER_WARMUP_TFLOP of
+    work, so a small workload is timed at its own settled clocks."""
+    for name in ("qwen05b", "llama7b", "gemma7b"):
+        f = synth.MLP_CONFIGS[name].flops()
+        n = bench.other_warmup_steps(f)
+        assert n >= 3 and n * f >= bench.OTHER_WARMUP_TFLOP * 1e12 and (n - 1) * f < max(
+            bench.OTHER_WARMUP_TFLOP * 1e12, 3 * f)
+    assert bench.other_warmup_steps(synth.MLP_CONFIGS["qwen05b"].flops()) > 100
+    assert bench.other_warmup_steps(1e15) == 3
