@@ -88,7 +88,9 @@ struct Deferred {
 void defer_init(Deferred& d, float* slabs);
 lora_status_t defer_flush(Deferred& d, cudaStream_t st);
 // Reductions over tokens of the jobs in one launch (see lora_api.cu); late: the launch
-// reads nothing the previous kernel writes and writes nothing it reads (pdl_late).
+// reads nothing the previous kernel writes and writes nothing it reads (pdl_late).  kf is
+// the widest rank operand of the jobs (it picks the tile width); a job's own kf, when
+// set, is its operand's width, with the same tile width (skinny_bn) as kf's.
 lora_status_t token_grads(int64_t M, int r, int kf, float s, const GradJob* jobs, int njobs, Deferred& defer,
                           unsigned* status, cudaStream_t st, int64_t n_ex = 0, bool late = false);
 

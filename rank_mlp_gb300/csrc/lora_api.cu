@@ -416,7 +416,9 @@ lora_status_t token_grads(int64_t M, int r, int kf, float s, const GradJob* jobs
   int kfs[kMaxGroups];
   for (int j = 0; j < njobs; ++j) {
     const int kfj = jobs[j].kf > 0 ? jobs[j].kf : kf;
-    if (kfj > kf) return LORA_ERR_UNSUPPORTED;   // not reached: the call's kf is the widest
+    // not reached: the call's kf is the widest, and the workspace sizes every job's slabs
+    // for the tile width of its own kf
+    if (kfj > kf || skinny_bn(kfj) != skinny_bn(kf)) return LORA_ERR_UNSUPPORTED;
     int gi = -1;
     for (int q = 0; q < nq; ++q)
       if (qs[q] == jobs[j].Q && ts[q] == jobs[j].T) gi = q;
