@@ -192,8 +192,9 @@ __device__ __forceinline__ void act_bwd_cols(const uint32_t* d, const uint32_t (
 // warp walks its chunks of 32 rows x COLS columns in order across tiles; lane 0 keeps
 // the TMA loads of g, u SLOTS - 1 chunks ahead (into the slot whose dg, du store has
 // finished reading it), so the next tile's first loads fly while the warp waits for
-// that tile's accumulator.  Each chunk: wait for its slot, read dh from TMEM, compute,
-// write dg, du over g, u, make them visible to TMA and store both.  The accumulator is
+// that tile's accumulator.  Each chunk: wait for its slot, read dh from TMEM (16 columns
+// at a time, each read issued before the math of the half before it), compute, write
+// dg, du over g, u, make them visible to TMA and store both.  The accumulator is
 // released as soon as the tile's last chunk has been read from TMEM.  Rows past M and
 // columns past N are zero-filled by the loads and dropped by the stores.  The chunk's
 // 64-byte rows sit in the 64-byte swizzle: 16-byte unit j of row r at unit j ^ (r >> 1 & 3).
